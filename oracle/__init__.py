@@ -1,0 +1,124 @@
+"""fp64 CPU oracle for the M2RNN recurrence -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never loads it and
+shares no code with it.
+
+The arithmetic lives in ``m2rnn_oracle.c`` (plain C, fp64, OpenMP over
+independent (batch, head) pairs).  It follows Eqs. (10)-(12) of "M2RNN:
+Non-Linear RNNs with Matrix-Valued States" (frame "Write, transform, retain,
+and read a matrix state" of the paper-discussion deck) for the forward pass,
+and the chain rule of the backup frame "the recurrent gradient needs both
+paths" for the backward pass.  This module only compiles that file, converts
+arrays to contiguous float64 and marshals pointers.
+
+Layouts: q, k [B,T,K]; v [B,T,N,V]; f [B,T,N]; W [N,V,V] with
+(H W)_{ij} = sum_l H_{il} W_{lj}; w_r [N,V]; H0/H_T [B,N,K,V]; y [B,T,N,V].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "m2rnn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libm2rnn_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_DP = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (fp64, no fast-math, no FMA contraction)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.m2rnn_oracle_threads.restype = ctypes.c_int
+            lib.m2rnn_oracle_fwd.restype = ctypes.c_int
+            lib.m2rnn_oracle_bwd.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def threads() -> int:
+    """OpenMP threads the oracle uses (honours OMP_NUM_THREADS)."""
+    return int(_load().m2rnn_oracle_threads())
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().to("cpu")
+        import torch
+        x = x.to(torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_DP)
+
+
+def _dims(q, v):
+    B, T, K = q.shape
+    N, V = v.shape[2], v.shape[3]
+    return B, T, N, K, V
+
+
+def fwd(q, k, v, f, W, w_r, H0=None, want_states: bool = False):
+    """Forward pass.  Returns dict(y, HT[, states]) as float64 arrays.
+
+    ``states`` (if requested) holds H_0..H_T as [B,N,T+1,K,V]."""
+    q, k, v, f, W, w_r, H0 = map(_f64, (q, k, v, f, W, w_r, H0))
+    B, T, N, K, V = _dims(q, v)
+    y = np.zeros((B, T, N, V))
+    HT = np.zeros((B, N, K, V))
+    states = np.zeros((B, N, T + 1, K, V)) if want_states else None
+    rc = _load().m2rnn_oracle_fwd(B, T, N, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(f),
+                                  _ptr(W), _ptr(w_r), _ptr(H0), _ptr(y), _ptr(HT),
+                                  _ptr(states))
+    if rc != 0:
+        raise RuntimeError(f"m2rnn_oracle_fwd failed: {rc}")
+    out = {"y": y, "HT": HT}
+    if want_states:
+        out["states"] = states
+    return out
+
+
+def bwd(q, k, v, f, W, w_r, dy, H0=None, dHT=None):
+    """BPTT backward.  Returns dict(dq, dk, dv, df, dW, dw_r, dH0) (float64)."""
+    q, k, v, f, W, w_r, dy, H0, dHT = map(_f64, (q, k, v, f, W, w_r, dy, H0, dHT))
+    B, T, N, K, V = _dims(q, v)
+    out = {
+        "dq": np.zeros((B, T, K)), "dk": np.zeros((B, T, K)),
+        "dv": np.zeros((B, T, N, V)), "df": np.zeros((B, T, N)),
+        "dW": np.zeros((N, V, V)), "dw_r": np.zeros((N, V)),
+        "dH0": np.zeros((B, N, K, V)),
+    }
+    rc = _load().m2rnn_oracle_bwd(B, T, N, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(f),
+                                  _ptr(W), _ptr(w_r), _ptr(H0), _ptr(dy), _ptr(dHT),
+                                  *(_ptr(out[n]) for n in
+                                    ("dq", "dk", "dv", "df", "dW", "dw_r", "dH0")))
+    if rc != 0:
+        raise RuntimeError(f"m2rnn_oracle_bwd failed: {rc}")
+    return out
