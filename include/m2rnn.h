@@ -1,0 +1,145 @@
+/*
+ * m2rnn.h -- C ABI of libm2rnn.so, the GB300 (sm_103a) M2RNN recurrence.
+ *
+ * The operation (paper "M2RNN: Non-Linear RNNs with Matrix-Valued States for
+ * Scalable Language Modeling", arXiv 2603.14360v2; discussion deck frame
+ * "Write, transform, retain, and read a matrix state", Eqs. (10)-(12)), per
+ * batch item b and value head n, for t = 1..T:
+ *
+ *     Z_t = tanh(H_{t-1} W + k_t v_t^T)          H_t, Z_t in R^{K x V}
+ *     H_t = f_t H_{t-1} + (1 - f_t) Z_t          W in R^{V x V}
+ *     y_t = H_t^T q_t + w_r (.) v_t              q_t, k_t in R^K; v_t, w_r in R^V
+ *
+ * with H_0 = 0 unless an initial state is passed.  q and k are shared by the
+ * N value heads (frame "Shared queries and keys buy more recurrent
+ * capacity": N_q = N_k = 1, N_v = N_f = N_w = N).  The backward pass is the
+ * chain rule of the backup frame "the recurrent gradient needs both paths"
+ * (R_t = C_t + q_t u_t^T, D_t = ((1-f_t) R_t) (.) (1 - Z_t (.) Z_t),
+ * C_{t-1} = f_t R_t + D_t W^T, df_t = <R_t, H_{t-1} - Z_t>, dW = sum H_{t-1}^T D_t)
+ * plus the value-residual and q/k/v terms that follow from Eqs. (10)-(12).
+ *
+ * Layouts (all row-major and contiguous; element type in brackets):
+ *   q, k          [B,T,K]     (in_dtype)
+ *   v             [B,T,N,V]   (in_dtype)
+ *   f             [B,T,N]     (in_dtype), values in [0,1]
+ *   W             [N,V,V]     (in_dtype); (H W)_{ij} = sum_l H_{il} W[n][l][j]
+ *   w_r           [N,V]       (in_dtype)
+ *   H0, H_T       [B,N,K,V]   (float32)
+ *   y, dy         [B,T,N,V]   (in_dtype)
+ *   ckpt          [B,N,nck,K,V] (float32), nck = ceil(T / ckpt_every);
+ *                 ckpt[b][n][c] is the state after c*ckpt_every steps
+ *                 (ckpt[b][n][0] = H0, or 0)
+ *   dq, dk        [B,T,K]     (float32), summed over the N heads
+ *   dv            [B,T,N,V]   (float32)
+ *   df            [B,T,N]     (float32)
+ *   dW            [N,V,V]     (float32), summed over b and t
+ *   dw_r          [N,V]       (float32), summed over b and t
+ *   dH_T, dH0     [B,N,K,V]   (float32)
+ *
+ * Supported shapes: K in {16, 32, 64, 128}, V in {16, 32}, B, N >= 1,
+ * T >= 0, B*T*N*V < 2^40.  T = 0 launches no recurrence and writes
+ * H_T = H0 (or 0).
+ *
+ * Ownership and execution: every tensor pointer is device memory (cudaMalloc
+ * or managed) owned by the caller, on the current device, 16-byte aligned.
+ * The library keeps no pointer after a call returns and allocates no device
+ * memory per call; scratch for the backward pass is a caller-provided
+ * workspace whose size m2rnn_bwd_workspace_size() reports.  Work is enqueued
+ * asynchronously on `stream` (a cudaStream_t; NULL = legacy default stream);
+ * the caller synchronises.  Outputs are overwritten, never accumulated into.
+ *
+ * Errors: every entry point returns an m2rnn_status.  Argument errors are
+ * detected on the host before anything is launched.  A kernel whose internal
+ * wait exceeds its time limit stops early, leaves its outputs unspecified and
+ * records M2RNN_ERR_TIMEOUT in a device status word that
+ * m2rnn_device_status() reads.  Nothing crosses the ABI as an exception.
+ */
+#ifndef M2RNN_H_
+#define M2RNN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    M2RNN_OK = 0,
+    M2RNN_ERR_INVALID_ARG = -1,       /* null required pointer, negative size, bad dtype */
+    M2RNN_ERR_UNSUPPORTED_SHAPE = -2, /* K, V or sizes outside the supported set */
+    M2RNN_ERR_MISALIGNED = -3,        /* a tensor pointer is not 16-byte aligned */
+    M2RNN_ERR_POINTER = -4,           /* a pointer is not device memory of the current device */
+    M2RNN_ERR_WORKSPACE = -5,         /* workspace missing or smaller than required */
+    M2RNN_ERR_CUDA = -6,              /* a CUDA runtime call or launch failed */
+    M2RNN_ERR_TIMEOUT = -7            /* a kernel wait exceeded its limit (device status) */
+} m2rnn_status;
+
+typedef enum {
+    M2RNN_F32 = 0,  /* q, k, v, f, W, w_r, y, dy are float32 */
+    M2RNN_BF16 = 1  /* q, k, v, f, W, w_r, y, dy are bfloat16 */
+} m2rnn_dtype;
+
+typedef struct {
+    int B, T, N, K, V;
+    int in_dtype;    /* m2rnn_dtype */
+    int ckpt_every;  /* checkpoint interval C in steps; 0 = no checkpoints */
+} m2rnn_shape;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int m2rnn_version(void);
+
+/* Human-readable text for a status code; never NULL. */
+const char *m2rnn_status_string(int status);
+
+/* Number of checkpoints per (b, n) for `s`: ceil(T / ckpt_every), 0 when
+ * ckpt_every == 0 or T == 0. */
+size_t m2rnn_num_checkpoints(const m2rnn_shape *s);
+
+/* Forward pass, Eqs. (10)-(12).
+ *   q, k, v, f, W, w_r : inputs (required), layouts above.
+ *   H0   : initial state, or NULL for H_0 = 0.
+ *   y    : output (required).
+ *   H_T  : final state output, or NULL.
+ *   ckpt : checkpoint output, or NULL; written only when s->ckpt_every > 0. */
+int m2rnn_fwd(const m2rnn_shape *s, const void *q, const void *k, const void *v,
+              const void *f, const void *W, const void *w_r, const float *H0,
+              void *y, float *H_T, float *ckpt, void *stream);
+
+/* Bytes of workspace m2rnn_bwd needs for shape `s`; ckpt_given = 1 when the
+ * caller will pass checkpoints from the forward pass, 0 when the backward
+ * must recompute them into the workspace. */
+size_t m2rnn_bwd_workspace_size(const m2rnn_shape *s, int ckpt_given);
+
+/* Backward pass (BPTT) for the loss L with dL/dy = dy and dL/dH_T = dH_T.
+ *   q, k, v, f, W, w_r, H0 : the forward inputs (H0 may be NULL = 0).
+ *   ckpt : checkpoints written by m2rnn_fwd with the same s->ckpt_every,
+ *          or NULL to have them recomputed into the workspace.
+ *          s->ckpt_every must be > 0 (it is the recomputation interval).
+ *   dy   : upstream gradient of y (required); dH_T may be NULL (= 0).
+ *   dq, dk, dv, df, dW, dw_r : gradient outputs (required, float32).
+ *   dH0  : gradient of H0, or NULL.
+ *   workspace, ws_bytes : at least m2rnn_bwd_workspace_size(s, ckpt != NULL)
+ *          bytes of device memory; its contents on entry are ignored. */
+int m2rnn_bwd(const m2rnn_shape *s, const void *q, const void *k, const void *v,
+              const void *f, const void *W, const void *w_r, const float *H0,
+              const float *ckpt, const void *dy, const float *dH_T,
+              float *dq, float *dk, float *dv, float *df, float *dW, float *dw_r,
+              float *dH0, void *workspace, size_t ws_bytes, void *stream);
+
+/* Reads (after synchronising `stream`) and optionally clears the device
+ * status word of the current device.  *status receives M2RNN_OK or the code
+ * a kernel recorded (M2RNN_ERR_TIMEOUT); *detail receives the location code
+ * of the wait that gave up (may be NULL).  Returns M2RNN_OK or
+ * M2RNN_ERR_CUDA. */
+int m2rnn_device_status(int *status, int *detail, int clear, void *stream);
+
+/* Sets the time limit, in nanoseconds, of every internal wait of kernels
+ * launched afterwards from this process (default 2e9 = 2 s; values <= 0
+ * restore the default).  Exposed so that the time-out path can be tested
+ * with a wait that cannot complete in time.  Returns M2RNN_OK. */
+int m2rnn_set_wait_limit_ns(long long limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* M2RNN_H_ */

@@ -1,0 +1,211 @@
+// m2rnn_api.cu -- the extern "C" entry points declared in include/m2rnn.h:
+// argument validation, kernel-variant dispatch, the device status word and
+// the wait time limit.  Kernels live in m2rnn_fwd.cu / m2rnn_bwd.cu.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "m2rnn.h"
+#include "m2rnn_internal.h"
+
+namespace m2rnn {
+int fwd_max_consumer_warps();
+}
+
+namespace {
+
+constexpr long long kDefaultWaitLimitNs = 2000000000LL;
+std::atomic<long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+// Device status word, one per device image of this library.
+__device__ int g_device_status[2];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+int* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+int status_from_cuda(cudaError_t e) { return e == cudaSuccess ? M2RNN_OK : M2RNN_ERR_CUDA; }
+
+// Per-device set-up: the device address of the status word and the SM count.
+int device_info(int* dev_out, int** status_out, int* sms_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return M2RNN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return M2RNN_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return M2RNN_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<int*>(ptr);
+    g_num_sms[dev] = sms;
+  }
+  *dev_out = dev;
+  *status_out = g_status_ptr[dev];
+  *sms_out = g_num_sms[dev];
+  return M2RNN_OK;
+}
+
+// A tensor pointer must be 16-byte aligned device (or managed) memory of the
+// current device.
+int check_ptr(const void* p, int dev, bool required) {
+  if (p == nullptr) return required ? M2RNN_ERR_INVALID_ARG : M2RNN_OK;
+  if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return M2RNN_ERR_MISALIGNED;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return M2RNN_ERR_POINTER;
+  }
+  if (a.type == cudaMemoryTypeManaged) return M2RNN_OK;
+  if (a.type != cudaMemoryTypeDevice || a.device != dev) return M2RNN_ERR_POINTER;
+  return M2RNN_OK;
+}
+
+int check_shape(const m2rnn_shape* s) {
+  if (s == nullptr) return M2RNN_ERR_INVALID_ARG;
+  if (s->B < 1 || s->N < 1 || s->T < 0 || s->ckpt_every < 0) return M2RNN_ERR_INVALID_ARG;
+  if (s->in_dtype != M2RNN_F32 && s->in_dtype != M2RNN_BF16) return M2RNN_ERR_INVALID_ARG;
+  if (!(s->K == 16 || s->K == 32 || s->K == 64 || s->K == 128)) return M2RNN_ERR_UNSUPPORTED_SHAPE;
+  if (!(s->V == 16 || s->V == 32)) return M2RNN_ERR_UNSUPPORTED_SHAPE;
+  const double elems = static_cast<double>(s->B) * s->T * s->N * s->V;
+  if (elems >= 1099511627776.0) return M2RNN_ERR_UNSUPPORTED_SHAPE;  // 2^40
+  if (static_cast<long long>(s->B) * s->N >= (1LL << 31)) return M2RNN_ERR_UNSUPPORTED_SHAPE;
+  return M2RNN_OK;
+}
+
+struct FwdConfig {
+  int MT, WPH, G;
+};
+
+// Picks rows-per-warp (MT 16-row slices) and heads per CTA.  At least ~16
+// consumer warps per SM are needed to keep the SFU busy; beyond that larger
+// slices amortise per-step overhead.  Heads per CTA are chosen so that the
+// grid covers the SMs.
+FwdConfig choose_fwd(const m2rnn_shape* s, int sms) {
+  const bool f32 = s->in_dtype == M2RNN_F32;
+  const int mtiles = s->K / 16;
+  const long long heads = static_cast<long long>(s->B) * s->N;
+  int MT = 1;
+  if (!f32) {
+    for (int cand : {4, 2}) {
+      if (mtiles % cand != 0) continue;
+      if (s->V == 32 && cand > 2) continue;
+      if (heads * (mtiles / cand) >= 16LL * sms) {
+        MT = cand;
+        break;
+      }
+    }
+  }
+  const int WPH = mtiles / MT;
+  const int maxw = m2rnn::fwd_max_consumer_warps();
+  int best = 1;
+  for (int G = 1; G <= s->N && G * WPH <= maxw; ++G) {
+    if (s->N % G != 0) continue;
+    if (m2rnn::fwd_smem_bytes(s->K, s->V, G, WPH, f32) > 200 * 1024) continue;
+    const long long ctas = static_cast<long long>(s->B) * (s->N / G);
+    if (G == 1 || ctas >= sms) best = G;
+  }
+  return {MT, WPH, best};
+}
+
+}  // namespace
+
+extern "C" {
+
+int m2rnn_version(void) { return 100; }
+
+const char* m2rnn_status_string(int status) {
+  switch (status) {
+    case M2RNN_OK: return "ok";
+    case M2RNN_ERR_INVALID_ARG: return "invalid argument (null required pointer, negative size or bad dtype)";
+    case M2RNN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K must be 16/32/64/128, V 16/32)";
+    case M2RNN_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case M2RNN_ERR_POINTER: return "pointer is not device memory of the current device";
+    case M2RNN_ERR_WORKSPACE: return "workspace missing or too small";
+    case M2RNN_ERR_CUDA: return "CUDA runtime error";
+    case M2RNN_ERR_TIMEOUT: return "a kernel wait exceeded its time limit";
+    default: return "unknown status";
+  }
+}
+
+size_t m2rnn_num_checkpoints(const m2rnn_shape* s) {
+  if (s == nullptr || s->ckpt_every <= 0 || s->T <= 0) return 0;
+  return static_cast<size_t>((s->T + s->ckpt_every - 1) / s->ckpt_every);
+}
+
+int m2rnn_set_wait_limit_ns(long long limit_ns) {
+  g_wait_limit_ns.store(limit_ns > 0 ? limit_ns : kDefaultWaitLimitNs);
+  return M2RNN_OK;
+}
+
+int m2rnn_device_status(int* status, int* detail, int clear, void* stream) {
+  if (status == nullptr) return M2RNN_ERR_INVALID_ARG;
+  int dev, sms;
+  int* sp;
+  int rc = device_info(&dev, &sp, &sms);
+  if (rc != M2RNN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return M2RNN_ERR_CUDA;
+  int h[2] = {0, 0};
+  if (cudaMemcpy(h, sp, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return M2RNN_ERR_CUDA;
+  *status = h[0];
+  if (detail) *detail = h[1];
+  if (clear && cudaMemset(sp, 0, sizeof(h)) != cudaSuccess) return M2RNN_ERR_CUDA;
+  return M2RNN_OK;
+}
+
+int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
+              const void* W, const void* w_r, const float* H0, void* y, float* H_T, float* ckpt,
+              void* stream) {
+  int rc = check_shape(s);
+  if (rc != M2RNN_OK) return rc;
+  int dev, sms;
+  int* status;
+  rc = device_info(&dev, &status, &sms);
+  if (rc != M2RNN_OK) return rc;
+  const bool want_ckpt = s->ckpt_every > 0 && s->T > 0;
+  const void* req[] = {q, k, v, f, W, w_r, y};
+  for (const void* p : req)
+    if ((rc = check_ptr(p, dev, true)) != M2RNN_OK) return rc;
+  if ((rc = check_ptr(H0, dev, false)) != M2RNN_OK) return rc;
+  if ((rc = check_ptr(H_T, dev, false)) != M2RNN_OK) return rc;
+  if ((rc = check_ptr(ckpt, dev, want_ckpt)) != M2RNN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t state_bytes = static_cast<size_t>(s->B) * s->N * s->K * s->V * sizeof(float);
+  if (s->T == 0) {
+    if (H_T == nullptr) return M2RNN_OK;
+    return status_from_cuda(H0 ? cudaMemcpyAsync(H_T, H0, state_bytes, cudaMemcpyDeviceToDevice, st)
+                               : cudaMemsetAsync(H_T, 0, state_bytes, st));
+  }
+  const FwdConfig cfg = choose_fwd(s, sms);
+  m2rnn::FwdParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.f = f;
+  p.W = W;
+  p.w_r = w_r;
+  p.H0 = H0;
+  p.y = y;
+  p.HT = H_T;
+  p.ckpt = want_ckpt ? ckpt : nullptr;
+  p.B = s->B;
+  p.T = s->T;
+  p.N = s->N;
+  p.K = s->K;
+  p.C = want_ckpt ? s->ckpt_every : 0;
+  p.nck = static_cast<int>(m2rnn_num_checkpoints(s));
+  p.G = cfg.G;
+  p.WPH = cfg.WPH;
+  p.ngroups = (s->N + cfg.G - 1) / cfg.G;
+  p.status = status;
+  p.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
+  return status_from_cuda(m2rnn::launch_fwd(p, s->V, s->in_dtype == M2RNN_F32, cfg.MT, st));
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// m2rnn_internal.h -- launch parameters shared by the C-ABI layer and the
+// kernel translation units (host + device).  Not part of the public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace m2rnn {
+
+// Device status word: [0] = first recorded m2rnn_status (0 = OK),
+// [1] = location code of the wait that gave up.
+enum WaitSite : int {
+  SITE_FWD_PRODUCER = 1,
+  SITE_FWD_EPILOGUE = 2,
+  SITE_FWD_CONSUMER = 3,
+  SITE_FWD_DRAIN = 4,
+  SITE_BWD_PRODUCER = 11,
+  SITE_BWD_CONSUMER = 12,
+  SITE_BWD_DRAIN = 13,
+};
+
+constexpr int kStatusTimeout = -7;  // == M2RNN_ERR_TIMEOUT
+
+struct FwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* f;
+  const void* W;
+  const void* w_r;
+  const float* H0;  // nullable
+  void* y;
+  float* HT;    // nullable
+  float* ckpt;  // nullable
+  int B, T, N, K;
+  int C;        // checkpoint interval (0 = none)
+  int nck;      // checkpoints per (b, n)
+  int G;        // heads per CTA
+  int WPH;      // consumer warps per head
+  int ngroups;  // ceil(N / G)
+  int* status;
+  unsigned long long wait_limit_ns;
+};
+
+// Launches the forward kernel variant for (V, input dtype, MT m-tiles/warp).
+cudaError_t launch_fwd(const FwdParams& p, int V, bool f32_inputs, int MT, cudaStream_t stream);
+
+// Dynamic shared memory bytes the forward kernel needs.
+size_t fwd_smem_bytes(int K, int V, int G, int WPH, bool f32_inputs);
+
+}  // namespace m2rnn

@@ -1,0 +1,189 @@
+"""Thin ctypes binding of libm2rnn.so (include/m2rnn.h).
+
+Argument marshalling only: it checks tensor placement and dtypes, allocates
+output tensors with torch, passes raw device pointers and the current CUDA
+stream to the C ABI and turns non-zero status codes into exceptions.  Every
+step of the recurrence runs in the library's CUDA kernels; if the library is
+not built this module raises instead of computing anything itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libm2rnn.so")
+
+M2RNN_F32, M2RNN_BF16 = 0, 1
+STATUS = {
+    0: "M2RNN_OK", -1: "M2RNN_ERR_INVALID_ARG", -2: "M2RNN_ERR_UNSUPPORTED_SHAPE",
+    -3: "M2RNN_ERR_MISALIGNED", -4: "M2RNN_ERR_POINTER", -5: "M2RNN_ERR_WORKSPACE",
+    -6: "M2RNN_ERR_CUDA", -7: "M2RNN_ERR_TIMEOUT",
+}
+
+_lock = threading.Lock()
+_lib = None
+
+_VP = ctypes.c_void_p
+_EXPORTS = {
+    "m2rnn_version": (ctypes.c_int, []),
+    "m2rnn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "m2rnn_num_checkpoints": (ctypes.c_size_t, [_VP]),
+    "m2rnn_fwd": (ctypes.c_int, [_VP] * 12),
+    "m2rnn_bwd_workspace_size": (ctypes.c_size_t, [_VP, ctypes.c_int]),
+    "m2rnn_bwd": (ctypes.c_int, [_VP] * 19 + [ctypes.c_size_t, _VP]),
+    "m2rnn_device_status": (ctypes.c_int, [_VP, _VP, ctypes.c_int, _VP]),
+    "m2rnn_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_longlong]),
+}
+
+
+class M2RNNError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({status_string(code)})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("N", ctypes.c_int),
+                ("K", ctypes.c_int), ("V", ctypes.c_int), ("in_dtype", ctypes.c_int),
+                ("ckpt_every", ctypes.c_int)]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded native library (raises if it was never built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m non_linear_matrix_gb300.build` (there is no fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _EXPORTS.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().m2rnn_status_string(int(code)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise M2RNNError(rc, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return M2RNN_BF16
+    if t.dtype == torch.float32:
+        return M2RNN_F32
+    raise TypeError(f"unsupported input dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libm2rnn must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libm2rnn must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_shape(q, v, ckpt_every: int = 0) -> Shape:
+    B, T, K = q.shape
+    N, V = v.shape[2], v.shape[3]
+    return Shape(B, T, N, K, V, _dtype_code(q), int(ckpt_every))
+
+
+def num_checkpoints(shape: Shape) -> int:
+    return int(lib().m2rnn_num_checkpoints(ctypes.byref(shape)))
+
+
+def fwd(q, k, v, f, W, w_r, H0=None, *, ckpt_every: int = 0, want_HT: bool = True,
+        out=None, stream=None):
+    """Forward pass.  Returns (y, H_T or None, ckpt or None).
+
+    q, k [B,T,K]; v [B,T,N,V]; f [B,T,N]; W [N,V,V]; w_r [N,V], all of one
+    dtype (bf16 or f32); H0 [B,N,K,V] fp32 or None.  ``out`` may supply a
+    dict of preallocated outputs (y, HT, ckpt)."""
+    s = make_shape(q, v, ckpt_every)
+    for t in (k, v, f, W, w_r):
+        if t.dtype != q.dtype:
+            raise TypeError("q, k, v, f, W, w_r must share one dtype")
+    out = dict(out or {})
+    y = out.get("y")
+    if y is None:
+        y = torch.empty_like(v)
+    HT = out.get("HT")
+    if HT is None and want_HT:
+        HT = torch.empty(s.B, s.N, s.K, s.V, device=q.device, dtype=torch.float32)
+    ck = out.get("ckpt")
+    nck = num_checkpoints(s)
+    if ck is None and nck > 0:
+        ck = torch.empty(s.B, s.N, nck, s.K, s.V, device=q.device, dtype=torch.float32)
+    rc = lib().m2rnn_fwd(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r),
+                         _ptr(H0), _ptr(y), _ptr(HT), _ptr(ck), _stream(stream))
+    _check(rc, "m2rnn_fwd")
+    return y, HT, ck
+
+
+def bwd_workspace_size(shape: Shape, ckpt_given: bool) -> int:
+    return int(lib().m2rnn_bwd_workspace_size(ctypes.byref(shape), int(bool(ckpt_given))))
+
+
+def bwd(q, k, v, f, W, w_r, dy, H0=None, ckpt=None, dHT=None, *, ckpt_every: int = 64,
+        want_dH0: bool = False, workspace=None, out=None, stream=None):
+    """BPTT backward.  Returns dict(dq, dk, dv, df, dW, dw_r[, dH0]) (fp32)."""
+    s = make_shape(q, v, ckpt_every)
+    dev = q.device
+    f32 = dict(device=dev, dtype=torch.float32)
+    out = dict(out or {})
+    g = {
+        "dq": out.get("dq"), "dk": out.get("dk"), "dv": out.get("dv"), "df": out.get("df"),
+        "dW": out.get("dW"), "dw_r": out.get("dw_r"),
+    }
+    shapes = {"dq": (s.B, s.T, s.K), "dk": (s.B, s.T, s.K), "dv": (s.B, s.T, s.N, s.V),
+              "df": (s.B, s.T, s.N), "dW": (s.N, s.V, s.V), "dw_r": (s.N, s.V)}
+    for name, shp in shapes.items():
+        if g[name] is None:
+            g[name] = torch.empty(shp, **f32)
+    dH0 = out.get("dH0")
+    if dH0 is None and want_dH0:
+        dH0 = torch.empty(s.B, s.N, s.K, s.V, **f32)
+    need = bwd_workspace_size(s, ckpt is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+    rc = lib().m2rnn_bwd(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r),
+                         _ptr(H0), _ptr(ckpt), _ptr(dy), _ptr(dHT),
+                         _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["df"]),
+                         _ptr(g["dW"]), _ptr(g["dw_r"]), _ptr(dH0), _ptr(workspace),
+                         ctypes.c_size_t(workspace.numel()), _stream(stream))
+    _check(rc, "m2rnn_bwd")
+    if dH0 is not None:
+        g["dH0"] = dH0
+    return g
+
+
+def device_status(clear: bool = True, stream=None):
+    """(status, detail) of the device status word; synchronises the stream."""
+    st, de = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().m2rnn_device_status(ctypes.byref(st), ctypes.byref(de), int(clear),
+                                     _stream(stream)), "m2rnn_device_status")
+    return st.value, de.value
+
+
+def set_wait_limit_ns(limit_ns: int):
+    _check(lib().m2rnn_set_wait_limit_ns(int(limit_ns)), "m2rnn_set_wait_limit_ns")

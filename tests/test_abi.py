@@ -1,0 +1,79 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/m2rnn.h declares, and rejects bad arguments on the host before any
+device work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from non_linear_matrix_gb300 import build as nb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nb.build()
+    from non_linear_matrix_gb300 import m2rnn
+    return m2rnn.lib()
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(m2rnn_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert "m2rnn_fwd" in names and "m2rnn_bwd" in names
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    from non_linear_matrix_gb300 import m2rnn
+    assert lib.m2rnn_version() >= 100
+    for code in range(-7, 1):
+        assert len(m2rnn.status_string(code)) > 0
+    assert m2rnn.status_string(12345) == "unknown status"
+
+
+def test_num_checkpoints(lib):
+    from non_linear_matrix_gb300.m2rnn import Shape, num_checkpoints
+    assert num_checkpoints(Shape(8, 4096, 32, 64, 16, 1, 64)) == 64
+    assert num_checkpoints(Shape(1, 100, 4, 64, 16, 1, 64)) == 2
+    assert num_checkpoints(Shape(1, 64, 4, 64, 16, 1, 64)) == 1
+    assert num_checkpoints(Shape(1, 0, 4, 64, 16, 1, 64)) == 0
+    assert num_checkpoints(Shape(1, 64, 4, 64, 16, 1, 0)) == 0
+
+
+@pytest.mark.parametrize("shape,code", [
+    (None, -1),
+    ((1, 8, 2, 48, 16, 1, 0), -2),   # K not supported
+    ((1, 8, 2, 64, 24, 1, 0), -2),   # V not supported
+    ((1, 8, 2, 64, 16, 7, 0), -1),   # bad dtype
+    ((0, 8, 2, 64, 16, 1, 0), -1),   # B < 1
+    ((1, -1, 2, 64, 16, 1, 0), -1),  # T < 0
+    ((1, 8, 2, 64, 16, 1, -4), -1),  # negative checkpoint interval
+])
+def test_fwd_rejects_bad_shapes_before_launch(lib, shape, code):
+    from non_linear_matrix_gb300.m2rnn import Shape
+    s = None if shape is None else ctypes.byref(Shape(*shape))
+    p = ctypes.c_void_p(16)
+    rc = lib.m2rnn_fwd(s, p, p, p, p, p, p, None, p, None, None, None)
+    assert rc == code
+
+
+def test_bwd_rejects_bad_shapes_before_launch(lib):
+    from non_linear_matrix_gb300.m2rnn import Shape
+    p = ctypes.c_void_p(16)
+    s = ctypes.byref(Shape(1, 8, 2, 48, 16, 1, 4))
+    rc = lib.m2rnn_bwd(s, *([p] * 6), None, None, p, None, *([p] * 6), None, p,
+                       ctypes.c_size_t(1 << 20), None)
+    assert rc in (-1, -2)
