@@ -1,0 +1,358 @@
+"""Throughput benchmark of the M2RNN recurrence on GB300 (one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one forward pass of the recurrence over the workload's whole batch
+(default: B=64, T=4096, N=32, K=64, V=16, bf16 inputs, fp32 state: the
+throughput shape), through the C ABI, with inputs resident in HBM.  The
+inputs (~0.32 GB) exceed the 129 MB L2, so no flush is needed between steps.
+Metric: tokens x heads per second (B*T*N / step time).
+
+Extra keys on the JSON line:
+  roofline      the dominant kernel against the SFU tanh rate (the bound of
+                this path: K*V tanh per token x head at 16 tanh/clk/SM);
+  roofline_hbm_tensor_serial
+                the same time against max(tensor, HBM) + serial-chain bound;
+  cpu_baseline  the fp64 oracle (test infrastructure) on a bounded sample of
+                the same workload on the host cores;
+  e2e           the same metric with host (pinned) inputs: host->device
+                copies, the C-ABI call and the device->host copy of y inside
+                the timed region;
+  clocks        nvidia-smi SM clock samples taken during the timed region.
+For N > 1 (torchrun) every rank runs its own batch on its own GPU (weak
+scaling, no collective on the data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from non_linear_matrix_gb300.inputs import WORKLOADS, workload_inputs  # noqa: E402
+
+METRIC = "M2RNN fwd tokens x heads/s on 1 GB300"
+UNIT = "tokens*heads/s"
+DEFAULT_WORKLOAD = "fwd_bf16_b64_t4096_n32"
+
+# Rates measured on this machine's GB300 by non_linear_matrix_gb300/csrc/m2rnn_microbench.cu
+# (profiles/microbench_gb300.txt): tanh.approx results per clock per SM (f32,
+# bf16x2 and f16x2 alike) and the dependent latency of one recurrence step of
+# a 16x16 state tile (mma -> tanh -> blend -> bf16 repack) on one warp.
+SFU_TANH_PER_CLK_PER_SM = 16.0
+STEP_LATENCY_CLK = 82.5
+NUM_SMS = 152
+SM_MAX_MHZ = 2070.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "sm_max_mhz": float(d.get("sm_max_mhz", SM_MAX_MHZ)), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, sm_max_mhz=SM_MAX_MHZ, source="fallback")
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _roofline(w, kernel_ms, peaks, traffic):
+    th = w.th
+    tanh_per_launch = th * w.K * w.V
+    peak_tanh = NUM_SMS * SFU_TANH_PER_CLK_PER_SM * peaks["sm_max_mhz"] * 1e6
+    achieved = tanh_per_launch / (kernel_ms * 1e-3)
+    es = 2 if w.dtype == "bf16" else 4
+    # algorithmic bytes: v, f, y per token x head; q, k per token; W, w_r per head
+    bytes_per_launch = th * (2 * w.V * es + es) + w.B * w.T * 2 * w.K * es + \
+        w.N * (w.V * w.V + w.V) * es + w.B * w.N * w.K * w.V * 4
+    flops_per_launch = th * (2 * w.K * w.V * w.V + 4 * w.K * w.V)
+    t_hbm = bytes_per_launch / (peaks["hbm_gbs"] * 1e9) * 1e3
+    t_tensor = flops_per_launch / (peaks["bf16_tflops"] * 1e12) * 1e3
+    t_serial = w.T * STEP_LATENCY_CLK / (peaks["sm_max_mhz"] * 1e6) * 1e3
+    t_roof = max(t_hbm, t_tensor) + t_serial
+    return (
+        {"bound": "alu", "achieved": achieved / 1e12, "peak": peak_tanh / 1e12,
+         "unit": "Ttanh/s", "frac": achieved / peak_tanh, "traffic": traffic,
+         "units_per_launch": tanh_per_launch,
+         "peak_basis": f"SFU tanh {SFU_TANH_PER_CLK_PER_SM:g}/clk/SM (measured) x {NUM_SMS} SMs x "
+                       f"{peaks['sm_max_mhz']:g} MHz"},
+        {"t_tensor_ms": t_tensor, "t_hbm_ms": t_hbm, "t_serial_ms": t_serial,
+         "t_roof_ms": t_roof, "frac": t_roof / kernel_ms,
+         "frac_max_form": max(t_hbm, t_tensor, t_serial) / kernel_ms,
+         "algorithmic_bytes": bytes_per_launch, "algorithmic_flops": flops_per_launch,
+         "peaks": peaks["source"] + " (MEASURED_PEAKS.json)"
+         if peaks["source"] == "measured" else "fallback 6.8 TB/s, 1.9 PFLOP/s"},
+    )
+
+
+def _traffic(w):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since it was captured."""
+    path = os.path.join(ROOT, "profiles", "fwd_dram_traffic.json")
+    src = os.path.join(ROOT, "non_linear_matrix_gb300", "csrc", "m2rnn_fwd.cu")
+    try:
+        rec = json.load(open(path))
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if rec.get("kernel_source_sha256") == sha and rec.get("workload") == w.name:
+            return rec.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def _oracle_rate(w, budget_s: float, seed_offset: int = 0):
+    """fp64 oracle on a bounded sample: (th/s, description, threads, seconds)."""
+    import oracle
+    from non_linear_matrix_gb300.inputs import make_inputs
+    oracle.build()
+    threads = oracle.threads()
+    heads = max(1, min(w.N, threads))
+    T_probe = min(w.T, 256)
+    x = make_inputs(1, T_probe, heads, w.K, w.V, w.dtype, w.seed + seed_offset, w.f_mean)
+    t0 = time.perf_counter()
+    oracle.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"])
+    rate = heads * T_probe / max(time.perf_counter() - t0, 1e-6)
+    T_s = int(max(16, min(w.T, budget_s * rate / heads)))
+    x = make_inputs(1, T_s, heads, w.K, w.V, w.dtype, w.seed + seed_offset, w.f_mean)
+    t0 = time.perf_counter()
+    oracle.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"])
+    dt = time.perf_counter() - t0
+    desc = f"1 batch item x {heads} heads x {T_s} steps of {w.name} (K={w.K}, V={w.V})"
+    return heads * T_s / dt, desc, threads, dt
+
+
+def run_reference(args, w):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    per_step_budget = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        _oracle_rate(w, per_step_budget / 4)
+    times, th = [], 0.0
+    desc, threads = "", 0
+    for _ in range(args.steps):
+        rate, desc, threads, dt = _oracle_rate(w, per_step_budget)
+        times.append(dt)
+        th += rate * dt
+    value = th / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "N": w.N, "K": w.K, "V": w.V,
+                       "inputs": w.dtype, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from non_linear_matrix_gb300 import m2rnn
+    m2rnn.lib()
+
+    x = workload_inputs(w, with_dy=False)
+    if rank > 0:  # each rank its own batch (weak scaling)
+        from non_linear_matrix_gb300.inputs import make_inputs
+        x = make_inputs(w.B, w.T, w.N, w.K, w.V, w.dtype, w.seed + 1000 * rank, w.f_mean)
+    g = {n: t.cuda() for n, t in x.items()}
+    y = torch.empty_like(g["v"])
+    HT = torch.empty(w.B, w.N, w.K, w.V, device="cuda", dtype=torch.float32)
+    out = {"y": y, "HT": HT}
+    stream = torch.cuda.current_stream()
+
+    def step():
+        m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, detail = m2rnn.device_status(clear=True)
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail}) after warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    st, detail = m2rnn.device_status(clear=True)
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail}) in the timed region")
+    t_max = torch.tensor([ms], device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t_max.item())
+    value = world * w.th / (ms_max * 1e-3)
+
+    # End to end through the public API with host inputs.
+    e2e = None
+    if not args.no_e2e:
+        hx = {n: t.pin_memory() for n, t in x.items()}
+        hy = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in hx.values())
+        d2h = hy.numel() * hy.element_size()
+
+        def e2e_step():
+            for n in hx:
+                g[n].copy_(hx[n], non_blocking=True)
+            step()
+            hy.copy_(y, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_steps = max(3, min(args.steps, 50))
+        if world > 1:
+            torch.distributed.barrier()
+        ev0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = torch.tensor([ev0.elapsed_time(ev1) / e_steps], device="cuda")
+        if world > 1:
+            torch.distributed.all_reduce(e_ms, op=torch.distributed.ReduceOp.MAX)
+        e2e = {"value": world * w.th / (float(e_ms.item()) * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+               "ms_per_step": float(e_ms.item())}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peaks = _peaks()
+    roof, roof_json = _roofline(w, ms, peaks, _traffic(w))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "N": w.N, "K": w.K, "V": w.V,
+                   "inputs": w.dtype, "state": "f32", "global_batch": w.B * world,
+                   "seq_len": w.T, "parallelism": f"replicas{world}" if world > 1 else "1 GPU",
+                   "l2": "inputs (~0.32 GB) larger than L2; no flush"},
+        "roofline": roof, "roofline_hbm_tensor_serial": roof_json,
+        "e2e": e2e, "clocks": clocks, "gpu_launches": args.steps,
+    }
+    if not args.no_cpu:
+        rate, desc, threads, _ = _oracle_rate(w, 12.0)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,10 +1,21 @@
 """Forward parity: libm2rnn (through the C ABI) against the fp64 oracle on the
 same seeded inputs.
 
-Tolerances (max |.| elementwise on y and H_T): 2e-3 for fp32 operands, 2e-2
-for bf16 operands.  Sizes the oracle finishes in seconds are compared in
-full; the largest workloads are compared on sampled (batch, head) pairs,
-which the oracle computes independently from sliced inputs.
+Tolerances (max |.| elementwise on y, H_T and checkpoints): 2e-3 for fp32
+operands, 2e-2 for bf16 operands.
+
+Short sequences are compared along the whole trajectory.  Long sequences are
+compared per checkpoint interval: the oracle restarts from the GPU's own
+checkpoint at the start of every interval of C steps, and y over the
+interval plus the state at its end (the next checkpoint, or H_T) must match.
+This checks every step of the GPU path while bounding the amplification of
+rounding differences to C steps: at these input distributions the
+recurrence has transient unstable windows (the oracle alone, fed inputs
+perturbed by 1e-7, departs from itself by more than 1e-3 around step 540 of
+the B=8, T=2048 workload), so no finite-precision implementation follows the
+fp64 trajectory elementwise through them.
+The largest workloads are compared on sampled (batch, head) pairs, which the
+oracle computes from sliced inputs.
 """
 import numpy as np
 import pytest
@@ -59,18 +70,64 @@ def _compare(m2rnn, oracle_mod, x, dtype, H0=None, ckpt_every=0, label=""):
     return ey, eh
 
 
+def _restart_parity(oracle_mod, x, y, HT, ck, C, tol, label, H0=None):
+    """Oracle restarted from the GPU checkpoint of every interval of C steps
+    (inputs given for all heads of the batch items in x)."""
+    q, k, v, f = (x[n] for n in ("q", "k", "v", "f"))
+    B, T, K = q.shape
+    N, V = v.shape[2], v.shape[3]
+    ckn = _np(ck)                      # [B,N,nck,K,V]
+    yn, HTn = _np(y), _np(HT)
+    nck = ckn.shape[2]
+    assert nck == -(-T // C)
+    h0 = np.zeros((B, N, K, V)) if H0 is None else H0.double().numpy()
+    assert np.abs(ckn[:, :, 0] - h0).max() <= 1e-6, (label, "ckpt[0] != H0")
+    worst = {"y": 0.0, "state": 0.0}
+    for c0, c1 in ((0, T // C), (T // C, nck)):  # full intervals, then the ragged tail
+        if c1 <= c0:
+            continue
+        L = C if c0 == 0 else T - (T // C) * C
+        t0, t1 = c0 * C, c0 * C + (c1 - c0) * L
+        nb = c1 - c0
+
+        def split(a):  # [B, t0:t1, ...] -> [B*nb, L, ...]
+            a = a[:, t0:t1]
+            return a.reshape(B * nb, L, *a.shape[2:])
+        Hs = np.ascontiguousarray(np.moveaxis(ckn[:, :, c0:c1], 2, 1)).reshape(B * nb, N, K, V)
+        r = oracle_mod.fwd(split(q), split(k), split(v), split(f), x["W"], x["w_r"], H0=Hs)
+        ey = np.abs(split(yn) - r["y"]).max()
+        nxt = np.concatenate([ckn[:, :, 1:], HTn[:, :, None]], axis=2)[:, :, c0:c1]
+        nxt = np.ascontiguousarray(np.moveaxis(nxt, 2, 1)).reshape(B * nb, N, K, V)
+        es = np.abs(nxt - r["HT"]).max()
+        worst["y"] = max(worst["y"], ey)
+        worst["state"] = max(worst["state"], es)
+    assert worst["y"] <= tol and worst["state"] <= tol, (label, worst)
+    return worst
+
+
 @pytest.mark.parametrize("name", ["fwd_f32_b1_t64_n4", "fwd_bf16_b8_t2048_n32"])
-def test_small_workloads_full(m2rnn, oracle_mod, name):
+def test_small_workloads(m2rnn, oracle_mod, name):
     w = WORKLOADS[name]
     x = workload_inputs(w, with_dy=False)
-    _compare(m2rnn, oracle_mod, x, w.dtype, ckpt_every=64, label=name)
+    if w.T <= 256:
+        _compare(m2rnn, oracle_mod, x, w.dtype, ckpt_every=32, label=name)
+    g = _dev(x)
+    y, HT, ck = m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], ckpt_every=64)
+    torch.cuda.synchronize()
+    _check_status(m2rnn)
+    _restart_parity(oracle_mod, x, y, HT, ck, 64, TOL[w.dtype], name)
 
 
-def test_long_sequence_full(m2rnn, oracle_mod):
-    """B=1, T=65536, N=64: the serial chain; compared on every output."""
+def test_long_sequence(m2rnn, oracle_mod):
+    """B=1, T=65536, N=64: the serial chain, every output checked per
+    64-step interval."""
     w = WORKLOADS["fwd_bf16_b1_t65536_n64"]
     x = workload_inputs(w, with_dy=False)
-    _compare(m2rnn, oracle_mod, x, w.dtype, label=w.name)
+    g = _dev(x)
+    y, HT, ck = m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], ckpt_every=64)
+    torch.cuda.synchronize()
+    _check_status(m2rnn)
+    _restart_parity(oracle_mod, x, y, HT, ck, 64, TOL[w.dtype], w.name)
 
 
 def _sampled(m2rnn, oracle_mod, w, pairs):
@@ -80,13 +137,11 @@ def _sampled(m2rnn, oracle_mod, w, pairs):
     torch.cuda.synchronize()
     _check_status(m2rnn)
     for b, n in pairs:
-        ref = oracle_mod.fwd(x["q"][b:b + 1], x["k"][b:b + 1], x["v"][b:b + 1, :, n:n + 1],
-                             x["f"][b:b + 1, :, n:n + 1], x["W"][n:n + 1], x["w_r"][n:n + 1],
-                             want_states=True)
-        ey = np.abs(_np(y[b, :, n]) - ref["y"][0, :, 0]).max()
-        eh = np.abs(_np(HT[b, n]) - ref["HT"][0, 0]).max()
-        ec = np.abs(_np(ck[b, n]) - ref["states"][0, 0, ::64]).max()
-        assert max(ey, eh, ec) <= TOL[w.dtype], (w.name, b, n, ey, eh, ec)
+        xs = {"q": x["q"][b:b + 1], "k": x["k"][b:b + 1], "v": x["v"][b:b + 1, :, n:n + 1],
+              "f": x["f"][b:b + 1, :, n:n + 1], "W": x["W"][n:n + 1], "w_r": x["w_r"][n:n + 1]}
+        _restart_parity(oracle_mod, xs, y[b:b + 1, :, n:n + 1].contiguous(),
+                        HT[b:b + 1, n:n + 1].contiguous(), ck[b:b + 1, n:n + 1].contiguous(),
+                        64, TOL[w.dtype], (w.name, b, n))
 
 
 @pytest.mark.parametrize("name", ["fwd_bf16_b64_t4096_n32", "fwd_bf16_b64_t4096_n32_k128",
@@ -108,6 +163,19 @@ def test_shapes_ragged(m2rnn, oracle_mod, dtype, K, V, T):
     x = make_inputs(B, T, N, K, V, dtype, 1000 + K + V + T)
     H0 = torch.rand(B, N, K, V, generator=torch.Generator().manual_seed(T)) - 0.5
     _compare(m2rnn, oracle_mod, x, dtype, H0=H0, ckpt_every=16, label=f"{dtype} {K} {V} {T}")
+
+
+def test_restart_parity_ragged_tail_and_H0(m2rnn, oracle_mod):
+    """Checkpoint-interval parity with a ragged last interval and a given H0."""
+    B, T, N = 3, 1000, 6
+    x = make_inputs(B, T, N, 64, 16, "bf16", 31)
+    H0 = torch.rand(B, N, 64, 16, generator=torch.Generator().manual_seed(3)) - 0.5
+    g = _dev(x)
+    y, HT, ck = m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], H0.cuda(),
+                          ckpt_every=48)
+    torch.cuda.synchronize()
+    _check_status(m2rnn)
+    _restart_parity(oracle_mod, x, y, HT, ck, 48, TOL["bf16"], "ragged", H0=H0)
 
 
 def test_many_heads_per_cta_groups(m2rnn, oracle_mod):
