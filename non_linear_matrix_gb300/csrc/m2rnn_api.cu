@@ -13,7 +13,7 @@
 #include "m2rnn_internal.h"
 
 namespace m2rnn {
-int fwd_max_consumer_warps();
+int fwd_max_consumer_warps(int V, int MT, bool f32_inputs);
 }
 
 namespace {
@@ -102,7 +102,7 @@ FwdConfig choose_fwd(const m2rnn_shape* s, int sms) {
     }
   }
   const int WPH = mtiles / MT;
-  const int maxw = m2rnn::fwd_max_consumer_warps();
+  const int maxw = m2rnn::fwd_max_consumer_warps(s->V, MT, f32);
   int best = 1;
   for (int G = 1; G <= s->N && G * WPH <= maxw; ++G) {
     if (s->N % G != 0) continue;
@@ -169,19 +169,19 @@ int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   rc = device_info(&dev, &status, &sms);
   if (rc != M2RNN_OK) return rc;
   const bool want_ckpt = s->ckpt_every > 0 && s->T > 0;
-  const void* req[] = {q, k, v, f, W, w_r, y};
-  for (const void* p : req)
-    if ((rc = check_ptr(p, dev, true)) != M2RNN_OK) return rc;
   if ((rc = check_ptr(H0, dev, false)) != M2RNN_OK) return rc;
   if ((rc = check_ptr(H_T, dev, false)) != M2RNN_OK) return rc;
-  if ((rc = check_ptr(ckpt, dev, want_ckpt)) != M2RNN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t state_bytes = static_cast<size_t>(s->B) * s->N * s->K * s->V * sizeof(float);
-  if (s->T == 0) {
+  if (s->T == 0) {  // empty sequences: the [B,0,...] tensors may have no storage
     if (H_T == nullptr) return M2RNN_OK;
     return status_from_cuda(H0 ? cudaMemcpyAsync(H_T, H0, state_bytes, cudaMemcpyDeviceToDevice, st)
                                : cudaMemsetAsync(H_T, 0, state_bytes, st));
   }
+  const void* req[] = {q, k, v, f, W, w_r, y};
+  for (const void* p : req)
+    if ((rc = check_ptr(p, dev, true)) != M2RNN_OK) return rc;
+  if ((rc = check_ptr(ckpt, dev, false)) != M2RNN_OK) return rc;
   const FwdConfig cfg = choose_fwd(s, sms);
   m2rnn::FwdParams p;
   p.q = q;
@@ -193,7 +193,7 @@ int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   p.H0 = H0;
   p.y = y;
   p.HT = H_T;
-  p.ckpt = want_ckpt ? ckpt : nullptr;
+  p.ckpt = want_ckpt ? ckpt : nullptr;  // NULL: no checkpoints written
   p.B = s->B;
   p.T = s->T;
   p.N = s->N;

@@ -20,15 +20,16 @@
 //   warps 2+ consumers: WPH warps per head, each holding MT 16-row slices of
 //            the fp32 state in registers for all T steps, in the accumulator
 //            layout of mma.sync m16n8k16.  Per step and slice:
-//              acc  = k v^T           (bf16 path: one MMA whose B operand has
-//                                      v_t in row 0 and zeros elsewhere)
+//              acc  = k v^T           (packed fp32 multiplies, exact for
+//                                      bf16 inputs)
 //              acc += bf16(H) * W     (mma.sync, W in registers)
 //              H    = Z + f (H - Z),  Z = tanh(acc)   (SFU tanh, fp32)
 //              A    = bf16(H)         (the next step's A operand)
 //              ypart += q^T H         (MMA on movmatrix-transposed A)
+// Inputs of step t+1 are read from shared memory while step t computes.
 // The fp32-input path keeps the same structure but splits H and W into
-// bf16 hi + lo parts (three MMAs), forms k v^T in fp32, uses the accurate
-// tanhf and an fp32 readout.
+// bf16 hi + lo parts (three MMAs), uses the accurate tanhf and an fp32
+// readout.
 // Every mbarrier wait has a time limit; a wait that gives up records
 // M2RNN_ERR_TIMEOUT in the device status word and the warp leaves its loop.
 #include <cuda_bf16.h>
@@ -46,8 +47,12 @@ namespace {
 constexpr int TC = 32;                   // time steps per ring chunk
 constexpr int NSTAGE = 3;                // depth of the input ring
 constexpr int NYSTAGE = 2;               // depth of the readout-partial ring
-constexpr int kMaxConsumerWarps = 16;    // per CTA
-constexpr int kMaxThreads = 32 * (2 + kMaxConsumerWarps);
+// Consumer warps per CTA: 16 where the register budget of an 18-warp CTA
+// (96 per thread) holds the variant without spills, 8 otherwise.
+template <int V, int MT, bool F32>
+constexpr int max_consumer_warps() {
+  return (V == 16 && MT <= 2 && !F32) || (V == 16 && MT == 1) ? 16 : 8;
+}
 // Limit of the producer's final wait for its own bulk copies; independent of
 // the caller's wait limit so that a tiny limit never lets a CTA exit while a
 // copy into its shared memory is still in flight.
@@ -104,8 +109,6 @@ struct InType<false> {
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
-__device__ __forceinline__ void store_as(float* d, float x) { *d = x; }
-__device__ __forceinline__ void store_as(__nv_bfloat16* d, float x) { *d = __float2bfloat16_rn(x); }
 
 __device__ __forceinline__ void record_timeout(int* status, int site) {
   if (atomicCAS(&status[0], 0, kStatusTimeout) == 0) atomicExch(&status[1], site);
@@ -122,8 +125,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
 // producer warp
 // ---------------------------------------------------------------------------
 template <int V, bool F32>
-__device__ void fwd_producer(const FwdParams& p, const FwdLayout& L, unsigned char* smem,
-                             uint32_t sbase, int b, int n0, int Geff) {
+__device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout& L, uint32_t sbase,
+                                             int b, int n0, int Geff) {
   using TIn = typename InType<F32>::T;
   constexpr int es = sizeof(TIn);
   const int lane = threadIdx.x & 31;
@@ -157,10 +160,22 @@ __device__ void fwd_producer(const FwdParams& p, const FwdLayout& L, unsigned ch
     for (int tl = lane; tl < Tc; tl += 32)
       ptx::bulk_g2s(st + L.v + static_cast<uint32_t>(tl * G * V * es),
                     v + ((bt0 + tl) * N + n0) * V, v_bytes, full);
-    float* fs = reinterpret_cast<float*>(smem + static_cast<size_t>(s) * L.stage + L.f);
-    for (int e = lane; e < Tc * Geff; e += 32) {
-      const int tl = e / Geff, h = e - tl * Geff;
-      fs[tl * G + h] = to_f(f[(bt0 + tl) * N + n0 + h]);
+    // f[b, t0:t0+Tc, n0:n0+Geff] -> fp32 [TC][G]; loads batched for ILP.
+    const int nf = Tc * Geff;
+    for (int base = 0; base < nf; base += 256) {
+      float fv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = base + lane + 32 * i;
+        const int tl = e / Geff, h = e - tl * Geff;
+        fv[i] = e < nf ? to_f(f[(bt0 + tl) * N + n0 + h]) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = base + lane + 32 * i;
+        const int tl = e / Geff, h = e - tl * Geff;
+        if (e < nf) ptx::sts_f32(st + L.f + static_cast<uint32_t>((tl * G + h) * 4), fv[i]);
+      }
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(full);
@@ -179,19 +194,51 @@ __device__ void fwd_producer(const FwdParams& p, const FwdLayout& L, unsigned ch
 // ---------------------------------------------------------------------------
 // epilogue warp
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void store8(float* y, const float (&o)[8]) {
+  float4* d = reinterpret_cast<float4*>(y);
+  d[0] = make_float4(o[0], o[1], o[2], o[3]);
+  d[1] = make_float4(o[4], o[5], o[6], o[7]);
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* y, const float (&o)[8]) {
+  uint4 u;
+  u.x = ptx::pack_bf16x2(o[0], o[1]);
+  u.y = ptx::pack_bf16x2(o[2], o[3]);
+  u.z = ptx::pack_bf16x2(o[4], o[5]);
+  u.w = ptx::pack_bf16x2(o[6], o[7]);
+  *reinterpret_cast<uint4*>(y) = u;
+}
+// Eight consecutive v values from shared memory, as floats.
+template <bool F32>
+__device__ __forceinline__ void load8_v(uint32_t addr, float (&o)[8]) {
+  if (F32) {
+    const float4 a = ptx::lds_f32x4(addr), c = ptx::lds_f32x4(addr + 16);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = c.x; o[5] = c.y; o[6] = c.z; o[7] = c.w;
+  } else {
+    const uint4 u = ptx::lds_u32x4(addr);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = ptx::bf16x2_lo(w[i]);
+      o[2 * i + 1] = ptx::bf16x2_hi(w[i]);
+    }
+  }
+}
+
 template <int V, bool F32>
-__device__ void fwd_epilogue(const FwdParams& p, const FwdLayout& L, unsigned char* smem,
-                             uint32_t sbase, int b, int n0, int Geff) {
+__device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout& L, uint32_t sbase,
+                                             int b, int n0, int Geff) {
   using TIn = typename InType<F32>::T;
+  constexpr int es = sizeof(TIn);
   const int lane = threadIdx.x & 31;
   const int T = p.T, N = p.N, G = p.G, WPH = p.WPH;
   const uint32_t bars = sbase + L.bars;
   const int nchunks = (T + TC - 1) / TC;
-  float* wr_s = reinterpret_cast<float*>(smem + L.wr);
   const TIn* w_r = static_cast<const TIn*>(p.w_r) + static_cast<size_t>(n0) * V;
   const int GV = Geff * V;
-  for (int e = lane; e < GV; e += 32) wr_s[e] = to_f(w_r[e]);
+  for (int e = lane; e < GV; e += 32) ptx::sts_f32(sbase + L.wr + 4 * e, to_f(w_r[e]));
   __syncwarp();
+  const int R8 = GV / 8;  // 8-element groups per time step
   for (int ch = 0; ch < nchunks; ++ch) {
     const int s = ch % NSTAGE, ys = ch % NYSTAGE;
     if (!warp_wait(bar_in_full(bars, s), (ch / NSTAGE) & 1, p.wait_limit_ns) ||
@@ -201,18 +248,32 @@ __device__ void fwd_epilogue(const FwdParams& p, const FwdLayout& L, unsigned ch
     }
     const int t0 = ch * TC;
     const int Tc = min(TC, T - t0);
-    const TIn* vs = reinterpret_cast<const TIn*>(smem + static_cast<size_t>(s) * L.stage + L.v);
-    const float* yp = reinterpret_cast<const float*>(smem + L.yp_base + static_cast<size_t>(ys) * L.yp_stage);
+    const uint32_t vs = sbase + static_cast<uint32_t>(s) * L.stage + L.v;
+    const uint32_t yp = sbase + L.yp_base + static_cast<uint32_t>(ys) * L.yp_stage;
     TIn* y = static_cast<TIn*>(p.y) + ((static_cast<size_t>(b) * T + t0) * N + n0) * V;
-    for (int tl = 0; tl < Tc; ++tl) {
-      for (int r = lane; r < GV; r += 32) {
-        const int hl = r / V, j = r - hl * V;
-        const float* pp = yp + ((tl * G + hl) * WPH) * V + j;
-        float acc = 0.f;
-        for (int w = 0; w < WPH; ++w) acc += pp[w * V];
-        acc = fmaf(wr_s[r], to_f(vs[tl * G * V + r]), acc);
-        store_as(y + static_cast<size_t>(tl) * N * V + r, acc);
+    for (int idx = lane; idx < Tc * R8; idx += 32) {
+      const int tl = idx / R8;
+      const int r = (idx - tl * R8) * 8;
+      const int hl = r / V, j = r - hl * V;
+      float o[8], vv[8];
+      const uint32_t pa = yp + static_cast<uint32_t>((((tl * G + hl) * WPH) * V + j) * 4);
+      {
+        const float4 a = ptx::lds_f32x4(pa), c = ptx::lds_f32x4(pa + 16);
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+        o[4] = c.x; o[5] = c.y; o[6] = c.z; o[7] = c.w;
       }
+      for (int w = 1; w < WPH; ++w) {
+        const float4 a = ptx::lds_f32x4(pa + w * V * 4), c = ptx::lds_f32x4(pa + w * V * 4 + 16);
+        o[0] += a.x; o[1] += a.y; o[2] += a.z; o[3] += a.w;
+        o[4] += c.x; o[5] += c.y; o[6] += c.z; o[7] += c.w;
+      }
+      load8_v<F32>(vs + static_cast<uint32_t>((tl * G * V + r) * es), vv);
+      const float4 w0 = ptx::lds_f32x4(sbase + L.wr + 4 * r);
+      const float4 w1 = ptx::lds_f32x4(sbase + L.wr + 4 * r + 16);
+      const float wr[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = fmaf(wr[i], vv[i], o[i]);
+      store8(y + static_cast<size_t>(tl) * N * V + r, o);
     }
     __syncwarp();
     if (lane == 0) {
@@ -269,10 +330,171 @@ __device__ __forceinline__ void pack_a_lo(const float (&H)[V / 8][4], const uint
     }
 }
 
+// Per-step inputs one lane needs, loaded one step ahead of their use.
+// bf16 path: k (rows 16mt+g, 16mt+8+g) and v (columns 8nt+2c, +1) stay
+// packed as bf16x2 and are widened when used; q pairs feed the readout MMA.
+template <int MT, int NT, bool F32>
+struct StepIn;
+template <int MT, int NT>
+struct StepIn<MT, NT, false> {
+  uint32_t k[MT];     // lo: k[16mt+g], hi: k[16mt+8+g]
+  uint32_t q[MT][2];  // (q[16mt+2c], q[16mt+2c+1]), (q[16mt+8+2c], q[16mt+9+2c])
+  uint32_t v[NT];     // (v[8nt+2c], v[8nt+2c+1])
+  float f;
+};
+template <int MT, int NT>
+struct StepIn<MT, NT, true> {
+  float k0[MT], k1[MT];    // k at rows 16mt+g and 16mt+8+g
+  float qf0[MT], qf1[MT];  // q at rows 16mt+g and 16mt+8+g
+  float2 v[NT];            // v at columns 8nt+2c, 8nt+2c+1
+  float f;
+};
+
+template <int V, int MT>
+__device__ __forceinline__ void load_step(StepIn<MT, V / 8, true>& in, uint32_t qb, uint32_t kb,
+                                          uint32_t vb, uint32_t fb, int g, int c) {
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    in.k0[mt] = ptx::lds_f32(kb + 4 * (16 * mt + g));
+    in.k1[mt] = ptx::lds_f32(kb + 4 * (16 * mt + 8 + g));
+    in.qf0[mt] = ptx::lds_f32(qb + 4 * (16 * mt + g));
+    in.qf1[mt] = ptx::lds_f32(qb + 4 * (16 * mt + 8 + g));
+  }
+#pragma unroll
+  for (int nt = 0; nt < V / 8; ++nt) in.v[nt] = ptx::lds_f32x2(vb + 4 * (8 * nt + 2 * c));
+  in.f = ptx::lds_f32(fb);
+}
+
+template <int V, int MT>
+__device__ __forceinline__ void load_step(StepIn<MT, V / 8, false>& in, uint32_t qb, uint32_t kb,
+                                          uint32_t vb, uint32_t fb, int g, int c) {
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    in.k[mt] = ptx::lds_u16(kb + 2 * (16 * mt + g)) | (ptx::lds_u16(kb + 2 * (16 * mt + 8 + g)) << 16);
+    in.q[mt][0] = ptx::lds_u32(qb + 2 * (16 * mt + 2 * c));
+    in.q[mt][1] = ptx::lds_u32(qb + 2 * (16 * mt + 8 + 2 * c));
+  }
+#pragma unroll
+  for (int nt = 0; nt < V / 8; ++nt) in.v[nt] = ptx::lds_u32(vb + 2 * (8 * nt + 2 * c));
+  in.f = ptx::lds_f32(fb);
+}
+
+// Per-warp constant operands and the running state.
+template <int V, int MT>
+struct WarpState {
+  uint32_t Bw[V / 16][V / 8][2];   // W, bf16 hi
+  uint32_t Bwl[V / 16][V / 8][2];  // W, bf16 lo residual (fp32-input path)
+  float H[MT][V / 8][4];           // state, fp32
+  uint32_t A[MT][V / 16][4];       // bf16(H) as A operand
+  uint32_t Al[MT][V / 16][4];      // residual of bf16(H) (fp32-input path)
+};
+
+// One recurrence step for this warp's MT slices; writes the slices' readout
+// partial (columns 8nt+2c, +1 on lanes with g == 0) to ypaddr.
 template <int V, int MT, bool F32>
-__device__ void fwd_consumer(const FwdParams& p, const FwdLayout& L, unsigned char* smem,
-                             uint32_t sbase, int b, int n0, int ci) {
+__device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V / 8, F32>& in,
+                                         uint32_t ypaddr, int g, int c) {
+  constexpr int NT = V / 8, KS = V / 16;
+  const float2 f2 = make_float2(in.f, in.f);
+  const float2 m1 = make_float2(-1.f, -1.f);
+  float ya[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) ya[nt][0] = ya[nt][1] = ya[nt][2] = ya[nt][3] = 0.f;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    // acc = k v^T (exact fp32 products), then acc += bf16(H) W on the tensor core.
+    float acc[NT][4];
+    float2 k0, k1;
+    if constexpr (F32) {
+      k0 = make_float2(in.k0[mt], in.k0[mt]);
+      k1 = make_float2(in.k1[mt], in.k1[mt]);
+    } else {
+      const float a = ptx::bf16x2_lo(in.k[mt]), bb = ptx::bf16x2_hi(in.k[mt]);
+      k0 = make_float2(a, a);
+      k1 = make_float2(bb, bb);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float2 vv;
+      if constexpr (F32) {
+        vv = in.v[nt];
+      } else {
+        vv = make_float2(ptx::bf16x2_lo(in.v[nt]), ptx::bf16x2_hi(in.v[nt]));
+      }
+      const float2 lo = __fmul2_rn(k0, vv), hi = __fmul2_rn(k1, vv);
+      acc[nt][0] = lo.x;
+      acc[nt][1] = lo.y;
+      acc[nt][2] = hi.x;
+      acc[nt][3] = hi.y;
+    }
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        ptx::mma_bf16_16816(acc[nt], S.A[mt][ks], S.Bw[ks][nt][0], S.Bw[ks][nt][1]);
+        if (F32) {
+          ptx::mma_bf16_16816(acc[nt], S.A[mt][ks], S.Bwl[ks][nt][0], S.Bwl[ks][nt][1]);
+          ptx::mma_bf16_16816(acc[nt], S.Al[mt][ks], S.Bw[ks][nt][0], S.Bw[ks][nt][1]);
+        }
+      }
+    // Z = tanh(acc); H = Z + f (H - Z)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float2 z;
+        z.x = F32 ? tanhf(acc[nt][2 * h]) : ptx::tanh_approx(acc[nt][2 * h]);
+        z.y = F32 ? tanhf(acc[nt][2 * h + 1]) : ptx::tanh_approx(acc[nt][2 * h + 1]);
+        const float2 hp = make_float2(S.H[mt][nt][2 * h], S.H[mt][nt][2 * h + 1]);
+        const float2 d = __ffma2_rn(m1, z, hp);
+        const float2 hn = __ffma2_rn(f2, d, z);
+        S.H[mt][nt][2 * h] = hn.x;
+        S.H[mt][nt][2 * h + 1] = hn.y;
+      }
+    pack_a<V>(S.H[mt], S.A[mt]);
+    if constexpr (F32) {
+      pack_a_lo<V>(S.H[mt], S.A[mt], S.Al[mt]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        ya[nt][0] = fmaf(in.qf0[mt], S.H[mt][nt][0], fmaf(in.qf1[mt], S.H[mt][nt][2], ya[nt][0]));
+        ya[nt][1] = fmaf(in.qf0[mt], S.H[mt][nt][1], fmaf(in.qf1[mt], S.H[mt][nt][3], ya[nt][1]));
+      }
+    } else {
+      // Readout y^T += q^T H on the tensor core: A = q in every row,
+      // B = this slice of bf16(H_t) transposed 8x8-blockwise.
+      const uint32_t Aq[4] = {in.q[mt][0], in.q[mt][0], in.q[mt][1], in.q[mt][1]};
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+          ptx::mma_bf16_16816(ya[2 * ks + h2], Aq, ptx::movmatrix_trans(S.A[mt][ks][2 * h2]),
+                              ptx::movmatrix_trans(S.A[mt][ks][2 * h2 + 1]));
+    }
+  }
+  if (F32) {
+    // Sum the fp32 partials over the 8 lanes of each column group.
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float x = ya[nt][e];
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        x += __shfl_xor_sync(0xffffffffu, x, 8);
+        x += __shfl_xor_sync(0xffffffffu, x, 16);
+        ya[nt][e] = x;
+      }
+  }
+  if (g == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) ptx::sts_f32x2(ypaddr + 4 * (8 * nt + 2 * c), ya[nt][0], ya[nt][1]);
+  }
+}
+
+template <int V, int MT, bool F32>
+__device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout& L, uint32_t sbase,
+                                             int b, int n0, int ci) {
   using TIn = typename InType<F32>::T;
+  constexpr int es = sizeof(TIn);
   constexpr int NT = V / 8, KS = V / 16;
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int K = p.K, T = p.T, N = p.N, G = p.G, WPH = p.WPH;
@@ -281,10 +503,9 @@ __device__ void fwd_consumer(const FwdParams& p, const FwdLayout& L, unsigned ch
   const int row0 = w * 16 * MT;
   const uint32_t bars = sbase + L.bars;
 
+  WarpState<V, MT> S;
   // W as B operands (k = row l of W, n = column j), bf16 hi (+ lo residual).
   const TIn* Wn = static_cast<const TIn*>(p.W) + static_cast<size_t>(n) * V * V;
-  uint32_t Bw[KS][NT][2];
-  uint32_t Bwl[KS][NT][2];
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
@@ -293,14 +514,11 @@ __device__ void fwd_consumer(const FwdParams& p, const FwdLayout& L, unsigned ch
       for (int h = 0; h < 2; ++h) {
         const int r0 = 16 * ks + 8 * h + 2 * c, col = 8 * nt + g;
         const float w0 = to_f(Wn[r0 * V + col]), w1 = to_f(Wn[(r0 + 1) * V + col]);
-        Bw[ks][nt][h] = ptx::pack_bf16x2(w0, w1);
-        Bwl[ks][nt][h] = F32 ? ptx::pack_bf16x2(w0 - ptx::bf16x2_lo(Bw[ks][nt][h]),
-                                                w1 - ptx::bf16x2_hi(Bw[ks][nt][h]))
-                             : 0u;
+        S.Bw[ks][nt][h] = ptx::pack_bf16x2(w0, w1);
+        S.Bwl[ks][nt][h] = F32 ? ptx::pack_bf16x2(w0 - ptx::bf16x2_lo(S.Bw[ks][nt][h]),
+                                                  w1 - ptx::bf16x2_hi(S.Bw[ks][nt][h]))
+                               : 0u;
       }
-
-  // State in registers, fp32.
-  float H[MT][NT][4];
   const size_t hoff = (static_cast<size_t>(b) * N + n) * K * V;
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
@@ -309,18 +527,24 @@ __device__ void fwd_consumer(const FwdParams& p, const FwdLayout& L, unsigned ch
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int row = row0 + 16 * mt + g + 8 * (r >> 1), col = 8 * nt + 2 * c + (r & 1);
-        H[mt][nt][r] = p.H0 ? p.H0[hoff + row * V + col] : 0.f;
+        S.H[mt][nt][r] = p.H0 ? p.H0[hoff + row * V + col] : 0.f;
       }
-  uint32_t A[MT][KS][4];
-  uint32_t Al[MT][KS][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
-    pack_a<V>(H[mt], A[mt]);
-    if (F32) pack_a_lo<V>(H[mt], A[mt], Al[mt]);
+    pack_a<V>(S.H[mt], S.A[mt]);
+    if (F32) pack_a_lo<V>(S.H[mt], S.A[mt], S.Al[mt]);
   }
 
+  float* ckpt = p.ckpt ? p.ckpt + (static_cast<size_t>(b) * N + n) * p.nck * K * V : nullptr;
+  int ck_left = 0;  // steps until the next checkpoint store
   const int nchunks = (T + TC - 1) / TC;
+  // Per-time-step strides of this lane's shared-memory reads.
+  const uint32_t qk_stride = static_cast<uint32_t>(K * es);
+  const uint32_t v_stride = static_cast<uint32_t>(G * V * es);
+  const uint32_t f_stride = static_cast<uint32_t>(G * 4);
+  const uint32_t yp_stride = static_cast<uint32_t>(G * WPH * V * 4);
   bool ok = true;
+  StepIn<MT, NT, F32> in0, in1;
   for (int ch = 0; ch < nchunks; ++ch) {
     const int s = ch % NSTAGE, ys = ch % NYSTAGE;
     if (!warp_wait(bar_in_full(bars, s), (ch / NSTAGE) & 1, p.wait_limit_ns) ||
@@ -328,124 +552,46 @@ __device__ void fwd_consumer(const FwdParams& p, const FwdLayout& L, unsigned ch
       ok = false;
       break;
     }
-    const int t0 = ch * TC;
-    const int Tc = min(TC, T - t0);
-    const unsigned char* st = smem + static_cast<size_t>(s) * L.stage;
-    const TIn* qs = reinterpret_cast<const TIn*>(st + L.q);
-    const TIn* kst = reinterpret_cast<const TIn*>(st + L.k);
-    const TIn* vs = reinterpret_cast<const TIn*>(st + L.v);
-    const float* fs = reinterpret_cast<const float*>(st + L.f);
-    float* yp = reinterpret_cast<float*>(smem + L.yp_base + static_cast<size_t>(ys) * L.yp_stage);
+    const int Tc = min(TC, T - ch * TC);
+    const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
+    const uint32_t qb = st + L.q + static_cast<uint32_t>(row0 * es);
+    const uint32_t kb = st + L.k + static_cast<uint32_t>(row0 * es);
+    const uint32_t vb = st + L.v + static_cast<uint32_t>(hl * V * es);
+    const uint32_t fb = st + L.f + static_cast<uint32_t>(hl * 4);
+    const uint32_t yb = sbase + L.yp_base + static_cast<uint32_t>(ys) * L.yp_stage +
+                        static_cast<uint32_t>(((hl * WPH) + w) * V * 4);
+    load_step<V, MT>(in0, qb, kb, vb, fb, g, c);
 #pragma unroll 1
-    for (int tl = 0; tl < Tc; ++tl) {
-      const int t = t0 + tl;
-      if (p.ckpt != nullptr && t % p.C == 0)
-        store_state<V, MT>(p.ckpt + ((static_cast<size_t>(b) * N + n) * p.nck + t / p.C) * K * V, H,
-                           row0, g, c);
-      const float fg = fs[tl * G + hl];
-      const TIn* vrow = vs + (tl * G + hl) * V;
-      const TIn* krow = kst + tl * K + row0;
-      const TIn* qrow = qs + tl * K + row0;
-      float ya[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) ya[nt][0] = ya[nt][1] = ya[nt][2] = ya[nt][3] = 0.f;
-      // B operand of the rank-1 write: v_t in row 0, zeros elsewhere.
-      uint32_t Bv[NT];
-      float vv[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (F32) {
-          vv[nt][0] = to_f(vrow[8 * nt + 2 * c]);
-          vv[nt][1] = to_f(vrow[8 * nt + 2 * c + 1]);
-          Bv[nt] = 0u;
-        } else {
-          const uint32_t raw = reinterpret_cast<const uint16_t*>(vrow)[8 * nt + g];
-          Bv[nt] = (c == 0) ? raw : 0u;
-          vv[nt][0] = vv[nt][1] = 0.f;
+    for (int tl = 0; tl < Tc; tl += 2) {
+      // even step: inputs in in0, prefetch tl+1 into in1
+      const uint32_t u1 = static_cast<uint32_t>(tl + 1);
+      if (tl + 1 < Tc)
+        load_step<V, MT>(in1, qb + u1 * qk_stride, kb + u1 * qk_stride, vb + u1 * v_stride,
+                              fb + u1 * f_stride, g, c);
+      if (ckpt != nullptr) {
+        if (ck_left == 0) {
+          store_state<V, MT>(ckpt, S.H, row0, g, c);
+          ckpt += K * V;
+          ck_left = p.C;
         }
+        --ck_left;
       }
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        float acc[NT][4];
-        if (F32) {
-          const float k0 = to_f(krow[16 * mt + g]), k1 = to_f(krow[16 * mt + 8 + g]);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            acc[nt][0] = k0 * vv[nt][0];
-            acc[nt][1] = k0 * vv[nt][1];
-            acc[nt][2] = k1 * vv[nt][0];
-            acc[nt][3] = k1 * vv[nt][1];
-          }
-        } else {
-          // A operand with k_i in every column of row i: A * Bv = k v^T.
-          const uint32_t k0 = reinterpret_cast<const uint16_t*>(krow)[16 * mt + g];
-          const uint32_t k1 = reinterpret_cast<const uint16_t*>(krow)[16 * mt + 8 + g];
-          const uint32_t Ak[4] = {k0 | (k0 << 16), k1 | (k1 << 16), k0 | (k0 << 16), k1 | (k1 << 16)};
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-            ptx::mma_bf16_16816(acc[nt], Ak, Bv[nt], 0u);
-          }
+      fwd_step<V, MT, F32>(S, in0, yb + static_cast<uint32_t>(tl) * yp_stride, g, c);
+      if (tl + 1 >= Tc) break;
+      // odd step: inputs in in1, prefetch tl+2 into in0
+      const uint32_t u2 = static_cast<uint32_t>(tl + 2);
+      if (tl + 2 < Tc)
+        load_step<V, MT>(in0, qb + u2 * qk_stride, kb + u2 * qk_stride, vb + u2 * v_stride,
+                              fb + u2 * f_stride, g, c);
+      if (ckpt != nullptr) {
+        if (ck_left == 0) {
+          store_state<V, MT>(ckpt, S.H, row0, g, c);
+          ckpt += K * V;
+          ck_left = p.C;
         }
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            ptx::mma_bf16_16816(acc[nt], A[mt][ks], Bw[ks][nt][0], Bw[ks][nt][1]);
-            if (F32) {
-              ptx::mma_bf16_16816(acc[nt], A[mt][ks], Bwl[ks][nt][0], Bwl[ks][nt][1]);
-              ptx::mma_bf16_16816(acc[nt], Al[mt][ks], Bw[ks][nt][0], Bw[ks][nt][1]);
-            }
-          }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const float z = F32 ? tanhf(acc[nt][r]) : ptx::tanh_approx(acc[nt][r]);
-            H[mt][nt][r] = fmaf(fg, H[mt][nt][r] - z, z);
-          }
-        pack_a<V>(H[mt], A[mt]);
-        if (F32) {
-          pack_a_lo<V>(H[mt], A[mt], Al[mt]);
-          const float q0 = to_f(qrow[16 * mt + g]), q1 = to_f(qrow[16 * mt + 8 + g]);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            ya[nt][0] = fmaf(q0, H[mt][nt][0], fmaf(q1, H[mt][nt][2], ya[nt][0]));
-            ya[nt][1] = fmaf(q0, H[mt][nt][1], fmaf(q1, H[mt][nt][3], ya[nt][1]));
-          }
-        } else {
-          // Readout y^T += q^T H on the tensor core: A = q in every row,
-          // B = this slice of bf16(H_t) transposed 8x8-blockwise.
-          const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow);
-          const uint32_t qa0 = q32[8 * mt + c], qa1 = q32[8 * mt + 4 + c];
-          const uint32_t Aq[4] = {qa0, qa0, qa1, qa1};
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
-              ptx::mma_bf16_16816(ya[2 * ks + h2], Aq, ptx::movmatrix_trans(A[mt][ks][2 * h2]),
-                                  ptx::movmatrix_trans(A[mt][ks][2 * h2 + 1]));
-        }
+        --ck_left;
       }
-      if (F32) {
-        // Sum the fp32 partials over the 8 lanes of each column group.
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float x = ya[nt][e];
-            x += __shfl_xor_sync(0xffffffffu, x, 4);
-            x += __shfl_xor_sync(0xffffffffu, x, 8);
-            x += __shfl_xor_sync(0xffffffffu, x, 16);
-            ya[nt][e] = x;
-          }
-      }
-      if (g == 0) {
-        float* dst = yp + ((tl * G + hl) * WPH + w) * V;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          *reinterpret_cast<float2*>(dst + 8 * nt + 2 * c) = make_float2(ya[nt][0], ya[nt][1]);
-      }
+      fwd_step<V, MT, F32>(S, in1, yb + u1 * yp_stride, g, c);
     }
     __syncwarp();
     if (lane == 0) {
@@ -457,11 +603,12 @@ __device__ void fwd_consumer(const FwdParams& p, const FwdLayout& L, unsigned ch
     if (lane == 0) record_timeout(p.status, SITE_FWD_CONSUMER);
     return;
   }
-  if (p.HT != nullptr) store_state<V, MT>(p.HT + hoff, H, row0, g, c);
+  if (p.HT != nullptr) store_state<V, MT>(p.HT + hoff, S.H, row0, g, c);
 }
 
 template <int V, int MT, bool F32>
-__global__ void __launch_bounds__(kMaxThreads, 1) fwd_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1)
+    fwd_kernel(const FwdParams p) {
   using TIn = typename InType<F32>::T;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
@@ -485,11 +632,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) fwd_kernel(const FwdParams p) 
   }
   __syncthreads();
   if (warp == 0)
-    fwd_producer<V, F32>(p, L, smem, sbase, b, n0, Geff);
+    fwd_producer<V, F32>(p, L, sbase, b, n0, Geff);
   else if (warp == 1)
-    fwd_epilogue<V, F32>(p, L, smem, sbase, b, n0, Geff);
+    fwd_epilogue<V, F32>(p, L, sbase, b, n0, Geff);
   else if (warp - 2 < ncons)
-    fwd_consumer<V, MT, F32>(p, L, smem, sbase, b, n0, warp - 2);
+    fwd_consumer<V, MT, F32>(p, L, sbase, b, n0, warp - 2);
 }
 
 template <int V, int MT, bool F32>
@@ -510,7 +657,12 @@ size_t fwd_smem_bytes(int K, int V, int G, int WPH, bool f32_inputs) {
   return fwd_layout(K, V, G, WPH, f32_inputs ? 4 : 2).total;
 }
 
-int fwd_max_consumer_warps() { return kMaxConsumerWarps; }
+int fwd_max_consumer_warps(int V, int MT, bool f32_inputs) {
+  if (f32_inputs) return V == 16 ? max_consumer_warps<16, 1, true>() : max_consumer_warps<32, 1, true>();
+  if (V == 16) return MT == 1 ? max_consumer_warps<16, 1, false>()
+                     : MT == 2 ? max_consumer_warps<16, 2, false>() : max_consumer_warps<16, 4, false>();
+  return MT == 1 ? max_consumer_warps<32, 1, false>() : max_consumer_warps<32, 2, false>();
+}
 
 cudaError_t launch_fwd(const FwdParams& p, int V, bool f32_inputs, int MT, cudaStream_t stream) {
   if (f32_inputs) {
