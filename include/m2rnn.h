@@ -139,6 +139,14 @@ int m2rnn_device_status(int *status, int *detail, int clear, void *stream);
  * with a wait that cannot complete in time.  Returns M2RNN_OK. */
 int m2rnn_set_wait_limit_ns(long long limit_ns);
 
+/* Test hook for the time-out path.  mode 1: kernels launched afterwards
+ * from this process start no input transfers, so every internal wait runs
+ * into the wait limit, the kernel stops early (outputs unspecified) and
+ * M2RNN_ERR_TIMEOUT is recorded in the device status word.  mode 0 (the
+ * default) turns it off.  Returns M2RNN_OK, or M2RNN_ERR_INVALID_ARG for an
+ * unknown mode. */
+int m2rnn_set_fault_injection(int mode);
+
 #ifdef __cplusplus
 }
 #endif

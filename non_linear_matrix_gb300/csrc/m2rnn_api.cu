@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -20,6 +21,7 @@ namespace {
 
 constexpr long long kDefaultWaitLimitNs = 2000000000LL;
 std::atomic<long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int> g_fault_injection{0};
 
 // Device status word, one per device image of this library.
 __device__ int g_device_status[2];
@@ -79,8 +81,10 @@ int check_shape(const m2rnn_shape* s) {
 }
 
 struct FwdConfig {
-  int MT, WPH, G;
+  int MT, WPH, G, tc;
 };
+
+constexpr size_t kSmemBudget = 220 * 1024;  // per CTA, below the 227 KB limit
 
 // Picks rows-per-warp (MT 16-row slices) and heads per CTA.  At least ~16
 // consumer warps per SM are needed to keep the SFU busy; beyond that larger
@@ -101,16 +105,24 @@ FwdConfig choose_fwd(const m2rnn_shape* s, int sms) {
       }
     }
   }
+  // Tuning override: M2RNN_FWD_MT=1|2|4 forces the rows-per-warp variant.
+  if (const char* e = std::getenv("M2RNN_FWD_MT")) {
+    const int m = std::atoi(e);
+    if ((m == 1 || m == 2 || m == 4) && mtiles % m == 0 && !(f32 && m != 1) && !(s->V == 32 && m == 4))
+      MT = m;
+  }
   const int WPH = mtiles / MT;
   const int maxw = m2rnn::fwd_max_consumer_warps(s->V, MT, f32);
   int best = 1;
   for (int G = 1; G <= s->N && G * WPH <= maxw; ++G) {
     if (s->N % G != 0) continue;
-    if (m2rnn::fwd_smem_bytes(s->K, s->V, G, WPH, f32) > 200 * 1024) continue;
+    if (m2rnn::fwd_smem_bytes(s->K, s->V, G, WPH, f32, 32) > 200 * 1024) continue;
     const long long ctas = static_cast<long long>(s->B) * (s->N / G);
     if (G == 1 || ctas >= sms) best = G;
   }
-  return {MT, WPH, best};
+  int tc = 32;  // shorter ring chunks where the layout would not fit
+  while (tc > 8 && m2rnn::fwd_smem_bytes(s->K, s->V, best, WPH, f32, tc) > kSmemBudget) tc /= 2;
+  return {MT, WPH, best, tc};
 }
 
 }  // namespace
@@ -140,6 +152,12 @@ size_t m2rnn_num_checkpoints(const m2rnn_shape* s) {
 
 int m2rnn_set_wait_limit_ns(long long limit_ns) {
   g_wait_limit_ns.store(limit_ns > 0 ? limit_ns : kDefaultWaitLimitNs);
+  return M2RNN_OK;
+}
+
+int m2rnn_set_fault_injection(int mode) {
+  if (mode != 0 && mode != 1) return M2RNN_ERR_INVALID_ARG;
+  g_fault_injection.store(mode);
   return M2RNN_OK;
 }
 
@@ -203,8 +221,10 @@ int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   p.G = cfg.G;
   p.WPH = cfg.WPH;
   p.ngroups = (s->N + cfg.G - 1) / cfg.G;
+  p.tc = cfg.tc;
   p.status = status;
   p.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
+  p.inject_stall = g_fault_injection.load();
   return status_from_cuda(m2rnn::launch_fwd(p, s->V, s->in_dtype == M2RNN_F32, cfg.MT, st));
 }
 

@@ -13,20 +13,22 @@
 //
 // CTA = one batch item b and G consecutive heads.  Warp roles:
 //   warp 0   producer: bulk copies (cp.async.bulk, no multicast) of q, k, v
-//            for TC-step chunks into an NSTAGE-deep shared-memory ring, and
-//            f converted to fp32; completion on mbarriers.
+//            for TC-step chunks into an NSTAGE-deep shared-memory ring; once
+//            a chunk has landed it writes k as duplicated fp32 pairs (k_i,
+//            k_i) and f as (f, f), the operand form of the packed fp32
+//            multiplies below, then releases the chunk to the consumers.
 //   warp 1   epilogue: sums the per-warp readout partials, adds w_r (.) v_t,
-//            converts and stores y (coalesced rows of G*V elements).
+//            converts and stores y (16-byte vector stores).
 //   warps 2+ consumers: WPH warps per head, each holding MT 16-row slices of
 //            the fp32 state in registers for all T steps, in the accumulator
 //            layout of mma.sync m16n8k16.  Per step and slice:
 //              acc  = k v^T           (packed fp32 multiplies, exact for
 //                                      bf16 inputs)
 //              acc += bf16(H) * W     (mma.sync, W in registers)
-//              H    = Z + f (H - Z),  Z = tanh(acc)   (SFU tanh, fp32)
+//              H    = Z + f (H - Z),  Z = tanh(acc)   (SFU tanh; fma.f32x2)
 //              A    = bf16(H)         (the next step's A operand)
-//              ypart += q^T H         (MMA on movmatrix-transposed A)
-// Inputs of step t+1 are read from shared memory while step t computes.
+//              ypart = q^T H          (MMA on movmatrix-transposed A)
+//            The rank-1 inputs of step t+1 are read while step t computes.
 // The fp32-input path keeps the same structure but splits H and W into
 // bf16 hi + lo parts (three MMAs), uses the accurate tanhf and an fp32
 // readout.
@@ -36,7 +38,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <type_traits>
 
 #include "m2rnn_internal.h"
 #include "ptx.cuh"
@@ -44,31 +45,34 @@
 namespace m2rnn {
 namespace {
 
-constexpr int TC = 32;                   // time steps per ring chunk
-constexpr int NSTAGE = 3;                // depth of the input ring
-constexpr int NYSTAGE = 2;               // depth of the readout-partial ring
-// Consumer warps per CTA: 16 where the register budget of an 18-warp CTA
-// (96 per thread) holds the variant without spills, 8 otherwise.
-template <int V, int MT, bool F32>
-constexpr int max_consumer_warps() {
-  return (V == 16 && MT <= 2 && !F32) || (V == 16 && MT == 1) ? 16 : 8;
-}
+constexpr int NSTAGE = 3;   // depth of the input ring
+constexpr int NYSTAGE = 2;  // depth of the readout-partial ring
 // Limit of the producer's final wait for its own bulk copies; independent of
 // the caller's wait limit so that a tiny limit never lets a CTA exit while a
 // copy into its shared memory is still in flight.
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
+// Consumer warps per CTA: 16 where an 18-warp CTA's register budget (96 per
+// thread) holds the variant without spills, 8 otherwise.
+template <int V, int MT, bool F32>
+constexpr int max_consumer_warps() {
+  return (V == 16 && MT <= 2 && !F32) || (V == 16 && MT == 1) ? 16 : 8;
+}
+
 struct FwdLayout {
-  uint32_t q, k, v, f, stage;  // offsets inside one ring stage, stage size
+  uint32_t q, k, v;    // raw bulk-copied inputs (input dtype)
+  uint32_t kd, fd;     // k as fp32 pairs [TC][K][2], f as fp32 pairs [TC][G][2]
+  uint32_t stage;      // bytes per ring stage
   uint32_t yp_base, yp_stage;  // readout partials [TC][G][WPH][V] fp32
-  uint32_t wr;                 // w_r as fp32 [G][V]
-  uint32_t bars;               // mbarriers
+  uint32_t wr;         // w_r as fp32 [G][V]
+  uint32_t bars;       // mbarriers
   uint32_t total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline FwdLayout fwd_layout(int K, int V, int G, int WPH, int es) {
+// TC: time steps per ring chunk (<= 32).
+__host__ __device__ inline FwdLayout fwd_layout(int K, int V, int G, int WPH, int es, int TC) {
   FwdLayout L;
   uint32_t o = 0;
   L.q = o;
@@ -77,23 +81,28 @@ __host__ __device__ inline FwdLayout fwd_layout(int K, int V, int G, int WPH, in
   o = align_up(o + TC * K * es, 128);
   L.v = o;
   o = align_up(o + TC * G * V * es, 128);
-  L.f = o;
-  o = align_up(o + TC * G * 4, 128);
+  L.kd = o;
+  o = align_up(o + TC * K * 8, 128);
+  L.fd = o;
+  o = align_up(o + TC * G * 8, 128);
   L.stage = o;
   L.yp_base = NSTAGE * L.stage;
   L.yp_stage = align_up(TC * G * WPH * V * 4, 128);
   L.wr = L.yp_base + NYSTAGE * L.yp_stage;
   L.bars = align_up(L.wr + G * V * 4, 128);
-  L.total = L.bars + 8 * (2 * NSTAGE + 2 * NYSTAGE);
+  L.total = L.bars + 8 * (3 * NSTAGE + 2 * NYSTAGE);
   return L;
 }
 
 // mbarrier addresses
-__device__ __forceinline__ uint32_t bar_in_full(uint32_t bars, int s) { return bars + 8 * s; }
-__device__ __forceinline__ uint32_t bar_in_empty(uint32_t bars, int s) { return bars + 8 * (NSTAGE + s); }
-__device__ __forceinline__ uint32_t bar_yp_full(uint32_t bars, int s) { return bars + 8 * (2 * NSTAGE + s); }
+__device__ __forceinline__ uint32_t bar_raw_full(uint32_t bars, int s) { return bars + 8 * s; }
+__device__ __forceinline__ uint32_t bar_in_full(uint32_t bars, int s) { return bars + 8 * (NSTAGE + s); }
+__device__ __forceinline__ uint32_t bar_in_empty(uint32_t bars, int s) {
+  return bars + 8 * (2 * NSTAGE + s);
+}
+__device__ __forceinline__ uint32_t bar_yp_full(uint32_t bars, int s) { return bars + 8 * (3 * NSTAGE + s); }
 __device__ __forceinline__ uint32_t bar_yp_empty(uint32_t bars, int s) {
-  return bars + 8 * (2 * NSTAGE + NYSTAGE + s);
+  return bars + 8 * (3 * NSTAGE + NYSTAGE + s);
 }
 
 template <bool F32>
@@ -132,35 +141,35 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
   const int lane = threadIdx.x & 31;
   const int K = p.K, T = p.T, N = p.N, G = p.G;
   const uint32_t bars = sbase + L.bars;
+  const int TC = p.tc;
   const int nchunks = (T + TC - 1) / TC;
   const TIn* q = static_cast<const TIn*>(p.q);
   const TIn* k = static_cast<const TIn*>(p.k);
   const TIn* v = static_cast<const TIn*>(p.v);
   const TIn* f = static_cast<const TIn*>(p.f);
-  int armed = 0;
-  for (int ch = 0; ch < nchunks; ++ch) {
+
+  // Waits for a free stage, starts the bulk copies of chunk ch and writes
+  // its f as fp32 pairs.
+  auto issue = [&](int ch) -> bool {
     const int s = ch % NSTAGE;
-    if (!warp_wait(bar_in_empty(bars, s), ((ch / NSTAGE) & 1) ^ 1, p.wait_limit_ns)) {
-      if (lane == 0) record_timeout(p.status, SITE_FWD_PRODUCER);
-      break;
-    }
+    if (!warp_wait(bar_in_empty(bars, s), ((ch / NSTAGE) & 1) ^ 1, p.wait_limit_ns)) return false;
     const int t0 = ch * TC;
     const int Tc = min(TC, T - t0);
     const uint32_t qk_bytes = static_cast<uint32_t>(Tc * K * es);
     const uint32_t v_bytes = static_cast<uint32_t>(Geff * V * es);
-    const uint32_t full = bar_in_full(bars, s);
-    if (lane == 0) ptx::mbar_expect_tx(full, 2 * qk_bytes + static_cast<uint32_t>(Tc) * v_bytes);
+    const uint32_t raw = bar_raw_full(bars, s);
+    if (lane == 0) ptx::mbar_expect_tx(raw, 2 * qk_bytes + static_cast<uint32_t>(Tc) * v_bytes);
     __syncwarp();
     const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
     const size_t bt0 = static_cast<size_t>(b) * T + t0;
     if (lane == 0) {
-      ptx::bulk_g2s(st + L.q, q + bt0 * K, qk_bytes, full);
-      ptx::bulk_g2s(st + L.k, k + bt0 * K, qk_bytes, full);
+      ptx::bulk_g2s(st + L.q, q + bt0 * K, qk_bytes, raw);
+      ptx::bulk_g2s(st + L.k, k + bt0 * K, qk_bytes, raw);
     }
     for (int tl = lane; tl < Tc; tl += 32)
       ptx::bulk_g2s(st + L.v + static_cast<uint32_t>(tl * G * V * es),
-                    v + ((bt0 + tl) * N + n0) * V, v_bytes, full);
-    // f[b, t0:t0+Tc, n0:n0+Geff] -> fp32 [TC][G]; loads batched for ILP.
+                    v + ((bt0 + tl) * N + n0) * V, v_bytes, raw);
+    // f[b, t0:t0+Tc, n0:n0+Geff] -> fp32 pairs [TC][G][2]; loads batched.
     const int nf = Tc * Geff;
     for (int base = 0; base < nf; base += 256) {
       float fv[8];
@@ -174,17 +183,65 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
       for (int i = 0; i < 8; ++i) {
         const int e = base + lane + 32 * i;
         const int tl = e / Geff, h = e - tl * Geff;
-        if (e < nf) ptx::sts_f32(st + L.f + static_cast<uint32_t>((tl * G + h) * 4), fv[i]);
+        if (e < nf) ptx::sts_f32x2(st + L.fd + static_cast<uint32_t>((tl * G + h) * 8), fv[i], fv[i]);
       }
     }
+    // The copies' bytes were announced above; this arrival is the barrier's
+    // single expected one, so its phase completes once all bytes have landed.
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(full);
-    armed = ch + 1;
+    if (lane == 0) ptx::mbar_arrive(raw);
+    return true;
+  };
+
+  // Waits for chunk ch's copies, writes k as fp32 pairs, releases the chunk.
+  auto convert = [&](int ch) -> bool {
+    const int s = ch % NSTAGE;
+    if (!warp_wait(bar_raw_full(bars, s), (ch / NSTAGE) & 1, p.wait_limit_ns)) return false;
+    const int Tc = min(TC, T - ch * TC);
+    const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
+    const int n8 = Tc * K / 8;
+    for (int i = lane; i < n8; i += 32) {
+      float x[8];
+      if (F32) {
+        const float4 a = ptx::lds_f32x4(st + L.k + 32 * i), c = ptx::lds_f32x4(st + L.k + 32 * i + 16);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
+      } else {
+        const uint4 u = ptx::lds_u32x4(st + L.k + 16 * i);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          x[2 * j] = ptx::bf16x2_lo(w[j]);
+          x[2 * j + 1] = ptx::bf16x2_hi(w[j]);
+        }
+      }
+      const uint32_t d = st + L.kd + 64 * i;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ptx::sts_f32x4(d + 16 * j, x[2 * j], x[2 * j], x[2 * j + 1], x[2 * j + 1]);
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar_in_full(bars, s));
+    return true;
+  };
+
+  int issued = 0, converted = 0;
+  bool ok = true;
+  for (int ch = 0; ch < nchunks; ++ch) {
+    if (!(ok = issue(ch))) break;
+    issued = ch + 1;
+    if (ch >= 1) {
+      if (!(ok = convert(ch - 1))) break;
+      converted = ch;
+    }
   }
+  if (ok && nchunks > 0) {
+    if ((ok = convert(nchunks - 1))) converted = nchunks;
+  }
+  if (!ok && lane == 0) record_timeout(p.status, SITE_FWD_PRODUCER);
   // Bulk copies complete on their own; before this warp (possibly the last
   // one alive after a time-out) leaves, wait until none is in flight.
-  for (int ch = max(0, armed - NSTAGE); ch < armed; ++ch) {
-    if (!warp_wait(bar_in_full(bars, ch % NSTAGE), (ch / NSTAGE) & 1, kDrainLimitNs)) {
+  for (int ch = max(converted, issued - NSTAGE); ch < issued; ++ch) {
+    if (!warp_wait(bar_raw_full(bars, ch % NSTAGE), (ch / NSTAGE) & 1, kDrainLimitNs)) {
       if (lane == 0) record_timeout(p.status, SITE_FWD_DRAIN);
       break;
     }
@@ -207,9 +264,9 @@ __device__ __forceinline__ void store8(__nv_bfloat16* y, const float (&o)[8]) {
   u.w = ptx::pack_bf16x2(o[6], o[7]);
   *reinterpret_cast<uint4*>(y) = u;
 }
-// Eight consecutive v values from shared memory, as floats.
+// Eight consecutive input-dtype values from shared memory, as floats.
 template <bool F32>
-__device__ __forceinline__ void load8_v(uint32_t addr, float (&o)[8]) {
+__device__ __forceinline__ void load8(uint32_t addr, float (&o)[8]) {
   if (F32) {
     const float4 a = ptx::lds_f32x4(addr), c = ptx::lds_f32x4(addr + 16);
     o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
@@ -233,6 +290,7 @@ __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout
   const int lane = threadIdx.x & 31;
   const int T = p.T, N = p.N, G = p.G, WPH = p.WPH;
   const uint32_t bars = sbase + L.bars;
+  const int TC = p.tc;
   const int nchunks = (T + TC - 1) / TC;
   const TIn* w_r = static_cast<const TIn*>(p.w_r) + static_cast<size_t>(n0) * V;
   const int GV = Geff * V;
@@ -267,7 +325,7 @@ __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout
         o[0] += a.x; o[1] += a.y; o[2] += a.z; o[3] += a.w;
         o[4] += c.x; o[5] += c.y; o[6] += c.z; o[7] += c.w;
       }
-      load8_v<F32>(vs + static_cast<uint32_t>((tl * G * V + r) * es), vv);
+      load8<F32>(vs + static_cast<uint32_t>((tl * G * V + r) * es), vv);
       const float4 w0 = ptx::lds_f32x4(sbase + L.wr + 4 * r);
       const float4 w1 = ptx::lds_f32x4(sbase + L.wr + 4 * r + 16);
       const float wr[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -330,53 +388,31 @@ __device__ __forceinline__ void pack_a_lo(const float (&H)[V / 8][4], const uint
     }
 }
 
-// Per-step inputs one lane needs, loaded one step ahead of their use.
-// bf16 path: k (rows 16mt+g, 16mt+8+g) and v (columns 8nt+2c, +1) stay
-// packed as bf16x2 and are widened when used; q pairs feed the readout MMA.
+// Rank-1 inputs of one step, read one step ahead of their use:
+// k as fp32 pairs (k_i, k_i) at rows 16mt+g and 16mt+8+g, and v at columns
+// 8nt+2c, 8nt+2c+1 (bf16x2 in the bf16 path, fp32 pair in the fp32 path).
 template <int MT, int NT, bool F32>
-struct StepIn;
-template <int MT, int NT>
-struct StepIn<MT, NT, false> {
-  uint32_t k[MT];     // lo: k[16mt+g], hi: k[16mt+8+g]
-  uint32_t q[MT][2];  // (q[16mt+2c], q[16mt+2c+1]), (q[16mt+8+2c], q[16mt+9+2c])
-  uint32_t v[NT];     // (v[8nt+2c], v[8nt+2c+1])
-  float f;
-};
-template <int MT, int NT>
-struct StepIn<MT, NT, true> {
-  float k0[MT], k1[MT];    // k at rows 16mt+g and 16mt+8+g
-  float qf0[MT], qf1[MT];  // q at rows 16mt+g and 16mt+8+g
-  float2 v[NT];            // v at columns 8nt+2c, 8nt+2c+1
-  float f;
+struct StepIn {
+  float2 k0[MT], k1[MT];
+  uint32_t vb[NT];
+  float2 vf[NT];
 };
 
-template <int V, int MT>
-__device__ __forceinline__ void load_step(StepIn<MT, V / 8, true>& in, uint32_t qb, uint32_t kb,
-                                          uint32_t vb, uint32_t fb, int g, int c) {
+template <int V, int MT, bool F32>
+__device__ __forceinline__ void load_step(StepIn<MT, V / 8, F32>& in, uint32_t kdb, uint32_t vb,
+                                          int g, int c) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
-    in.k0[mt] = ptx::lds_f32(kb + 4 * (16 * mt + g));
-    in.k1[mt] = ptx::lds_f32(kb + 4 * (16 * mt + 8 + g));
-    in.qf0[mt] = ptx::lds_f32(qb + 4 * (16 * mt + g));
-    in.qf1[mt] = ptx::lds_f32(qb + 4 * (16 * mt + 8 + g));
+    in.k0[mt] = ptx::lds_f32x2(kdb + 8 * (16 * mt + g));
+    in.k1[mt] = ptx::lds_f32x2(kdb + 8 * (16 * mt + 8 + g));
   }
 #pragma unroll
-  for (int nt = 0; nt < V / 8; ++nt) in.v[nt] = ptx::lds_f32x2(vb + 4 * (8 * nt + 2 * c));
-  in.f = ptx::lds_f32(fb);
-}
-
-template <int V, int MT>
-__device__ __forceinline__ void load_step(StepIn<MT, V / 8, false>& in, uint32_t qb, uint32_t kb,
-                                          uint32_t vb, uint32_t fb, int g, int c) {
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    in.k[mt] = ptx::lds_u16(kb + 2 * (16 * mt + g)) | (ptx::lds_u16(kb + 2 * (16 * mt + 8 + g)) << 16);
-    in.q[mt][0] = ptx::lds_u32(qb + 2 * (16 * mt + 2 * c));
-    in.q[mt][1] = ptx::lds_u32(qb + 2 * (16 * mt + 8 + 2 * c));
+  for (int nt = 0; nt < V / 8; ++nt) {
+    if (F32)
+      in.vf[nt] = ptx::lds_f32x2(vb + 4 * (8 * nt + 2 * c));
+    else
+      in.vb[nt] = ptx::lds_u32(vb + 2 * (8 * nt + 2 * c));
   }
-#pragma unroll
-  for (int nt = 0; nt < V / 8; ++nt) in.v[nt] = ptx::lds_u32(vb + 2 * (8 * nt + 2 * c));
-  in.f = ptx::lds_f32(fb);
 }
 
 // Per-warp constant operands and the running state.
@@ -390,38 +426,39 @@ struct WarpState {
 };
 
 // One recurrence step for this warp's MT slices; writes the slices' readout
-// partial (columns 8nt+2c, +1 on lanes with g == 0) to ypaddr.
+// partial (columns 8nt+2c, +1, on lanes with g == 0) to ypaddr.
 template <int V, int MT, bool F32>
 __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V / 8, F32>& in,
-                                         uint32_t ypaddr, int g, int c) {
+                                         uint32_t qb, uint32_t fdaddr, uint32_t ypaddr, int g,
+                                         int c) {
   constexpr int NT = V / 8, KS = V / 16;
-  const float2 f2 = make_float2(in.f, in.f);
-  const float2 m1 = make_float2(-1.f, -1.f);
-  float ya[NT][4];
+  // q (for the readout) and f are read here; their use is tens of cycles on.
+  uint32_t qa[MT][2];
+  float qf[MT][2];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) ya[nt][0] = ya[nt][1] = ya[nt][2] = ya[nt][3] = 0.f;
+  for (int mt = 0; mt < MT; ++mt) {
+    if (F32) {
+      qf[mt][0] = ptx::lds_f32(qb + 4 * (16 * mt + g));
+      qf[mt][1] = ptx::lds_f32(qb + 4 * (16 * mt + 8 + g));
+    } else {
+      qa[mt][0] = ptx::lds_u32(qb + 2 * (16 * mt + 2 * c));
+      qa[mt][1] = ptx::lds_u32(qb + 2 * (16 * mt + 8 + 2 * c));
+    }
+  }
+  const float2 f2 = ptx::lds_f32x2(fdaddr);
+  const float2 m1 = make_float2(-1.f, -1.f);
+  float2 vv[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+    vv[nt] = F32 ? in.vf[nt] : make_float2(ptx::bf16x2_lo(in.vb[nt]), ptx::bf16x2_hi(in.vb[nt]));
+  float ya[NT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     // acc = k v^T (exact fp32 products), then acc += bf16(H) W on the tensor core.
     float acc[NT][4];
-    float2 k0, k1;
-    if constexpr (F32) {
-      k0 = make_float2(in.k0[mt], in.k0[mt]);
-      k1 = make_float2(in.k1[mt], in.k1[mt]);
-    } else {
-      const float a = ptx::bf16x2_lo(in.k[mt]), bb = ptx::bf16x2_hi(in.k[mt]);
-      k0 = make_float2(a, a);
-      k1 = make_float2(bb, bb);
-    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float2 vv;
-      if constexpr (F32) {
-        vv = in.v[nt];
-      } else {
-        vv = make_float2(ptx::bf16x2_lo(in.v[nt]), ptx::bf16x2_hi(in.v[nt]));
-      }
-      const float2 lo = __fmul2_rn(k0, vv), hi = __fmul2_rn(k1, vv);
+      const float2 lo = __fmul2_rn(in.k0[mt], vv[nt]), hi = __fmul2_rn(in.k1[mt], vv[nt]);
       acc[nt][0] = lo.x;
       acc[nt][1] = lo.y;
       acc[nt][2] = hi.x;
@@ -456,22 +493,29 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
       pack_a_lo<V>(S.H[mt], S.A[mt], S.Al[mt]);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        ya[nt][0] = fmaf(in.qf0[mt], S.H[mt][nt][0], fmaf(in.qf1[mt], S.H[mt][nt][2], ya[nt][0]));
-        ya[nt][1] = fmaf(in.qf0[mt], S.H[mt][nt][1], fmaf(in.qf1[mt], S.H[mt][nt][3], ya[nt][1]));
+        const float p0 = fmaf(qf[mt][0], S.H[mt][nt][0], qf[mt][1] * S.H[mt][nt][2]);
+        const float p1 = fmaf(qf[mt][0], S.H[mt][nt][1], qf[mt][1] * S.H[mt][nt][3]);
+        ya[nt][0] = mt == 0 ? p0 : ya[nt][0] + p0;
+        ya[nt][1] = mt == 0 ? p1 : ya[nt][1] + p1;
       }
     } else {
       // Readout y^T += q^T H on the tensor core: A = q in every row,
       // B = this slice of bf16(H_t) transposed 8x8-blockwise.
-      const uint32_t Aq[4] = {in.q[mt][0], in.q[mt][0], in.q[mt][1], in.q[mt][1]};
+      const uint32_t Aq[4] = {qa[mt][0], qa[mt][0], qa[mt][1], qa[mt][1]};
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2)
-          ptx::mma_bf16_16816(ya[2 * ks + h2], Aq, ptx::movmatrix_trans(S.A[mt][ks][2 * h2]),
-                              ptx::movmatrix_trans(S.A[mt][ks][2 * h2 + 1]));
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint32_t b0 = ptx::movmatrix_trans(S.A[mt][ks][2 * h2]);
+          const uint32_t b1 = ptx::movmatrix_trans(S.A[mt][ks][2 * h2 + 1]);
+          if (mt == 0)
+            ptx::mma_bf16_16816_zero(ya[2 * ks + h2], Aq, b0, b1);
+          else
+            ptx::mma_bf16_16816(ya[2 * ks + h2], Aq, b0, b1);
+        }
     }
   }
-  if (F32) {
+  if constexpr (F32) {
     // Sum the fp32 partials over the 8 lanes of each column group.
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -536,12 +580,16 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
   }
 
   float* ckpt = p.ckpt ? p.ckpt + (static_cast<size_t>(b) * N + n) * p.nck * K * V : nullptr;
-  int ck_left = 0;  // steps until the next checkpoint store
+  // Absolute step before which the next checkpoint is stored (the state
+  // after next_ck steps); beyond T when no checkpoints are written.
+  int next_ck = ckpt != nullptr ? 0 : T + 1;
+  const int TC = p.tc;
   const int nchunks = (T + TC - 1) / TC;
   // Per-time-step strides of this lane's shared-memory reads.
-  const uint32_t qk_stride = static_cast<uint32_t>(K * es);
+  const uint32_t q_stride = static_cast<uint32_t>(K * es);
+  const uint32_t kd_stride = static_cast<uint32_t>(K * 8);
   const uint32_t v_stride = static_cast<uint32_t>(G * V * es);
-  const uint32_t f_stride = static_cast<uint32_t>(G * 4);
+  const uint32_t fd_stride = static_cast<uint32_t>(G * 8);
   const uint32_t yp_stride = static_cast<uint32_t>(G * WPH * V * 4);
   bool ok = true;
   StepIn<MT, NT, F32> in0, in1;
@@ -552,46 +600,45 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
       ok = false;
       break;
     }
-    const int Tc = min(TC, T - ch * TC);
+    const int t0 = ch * TC;
+    const int Tc = min(TC, T - t0);
     const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
     const uint32_t qb = st + L.q + static_cast<uint32_t>(row0 * es);
-    const uint32_t kb = st + L.k + static_cast<uint32_t>(row0 * es);
+    const uint32_t kdb = st + L.kd + static_cast<uint32_t>(row0 * 8);
     const uint32_t vb = st + L.v + static_cast<uint32_t>(hl * V * es);
-    const uint32_t fb = st + L.f + static_cast<uint32_t>(hl * 4);
+    const uint32_t fdb = st + L.fd + static_cast<uint32_t>(hl * 8);
     const uint32_t yb = sbase + L.yp_base + static_cast<uint32_t>(ys) * L.yp_stage +
                         static_cast<uint32_t>(((hl * WPH) + w) * V * 4);
-    load_step<V, MT>(in0, qb, kb, vb, fb, g, c);
+    // The rank-1 inputs of step tl+1 are read while step tl computes.  The
+    // read past the chunk's last step (slot Tc <= TC) stays inside this
+    // stage's shared memory and its values are never used.
+    load_step<V, MT, F32>(in0, kdb, vb, g, c);
+    int tl = 0;
+    while (tl < Tc) {
+      if (t0 + tl == next_ck) {
+        store_state<V, MT>(ckpt, S.H, row0, g, c);
+        ckpt += K * V;
+        next_ck += p.C;
+      }
+      const int seg_end = min(Tc, next_ck - t0);  // no checkpoint inside [tl, seg_end)
 #pragma unroll 1
-    for (int tl = 0; tl < Tc; tl += 2) {
-      // even step: inputs in in0, prefetch tl+1 into in1
-      const uint32_t u1 = static_cast<uint32_t>(tl + 1);
-      if (tl + 1 < Tc)
-        load_step<V, MT>(in1, qb + u1 * qk_stride, kb + u1 * qk_stride, vb + u1 * v_stride,
-                              fb + u1 * f_stride, g, c);
-      if (ckpt != nullptr) {
-        if (ck_left == 0) {
-          store_state<V, MT>(ckpt, S.H, row0, g, c);
-          ckpt += K * V;
-          ck_left = p.C;
-        }
-        --ck_left;
+      for (; tl + 1 < seg_end; tl += 2) {
+        const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1, u2 = u0 + 2;
+        load_step<V, MT, F32>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
+        fwd_step<V, MT, F32>(S, in0, qb + u0 * q_stride, fdb + u0 * fd_stride,
+                             yb + u0 * yp_stride, g, c);
+        load_step<V, MT, F32>(in0, kdb + u2 * kd_stride, vb + u2 * v_stride, g, c);
+        fwd_step<V, MT, F32>(S, in1, qb + u1 * q_stride, fdb + u1 * fd_stride,
+                             yb + u1 * yp_stride, g, c);
       }
-      fwd_step<V, MT, F32>(S, in0, yb + static_cast<uint32_t>(tl) * yp_stride, g, c);
-      if (tl + 1 >= Tc) break;
-      // odd step: inputs in in1, prefetch tl+2 into in0
-      const uint32_t u2 = static_cast<uint32_t>(tl + 2);
-      if (tl + 2 < Tc)
-        load_step<V, MT>(in0, qb + u2 * qk_stride, kb + u2 * qk_stride, vb + u2 * v_stride,
-                              fb + u2 * f_stride, g, c);
-      if (ckpt != nullptr) {
-        if (ck_left == 0) {
-          store_state<V, MT>(ckpt, S.H, row0, g, c);
-          ckpt += K * V;
-          ck_left = p.C;
-        }
-        --ck_left;
+      if (tl < seg_end) {  // odd remainder of the segment
+        const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1;
+        load_step<V, MT, F32>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
+        fwd_step<V, MT, F32>(S, in0, qb + u0 * q_stride, fdb + u0 * fd_stride,
+                             yb + u0 * yp_stride, g, c);
+        in0 = in1;
+        ++tl;
       }
-      fwd_step<V, MT, F32>(S, in1, yb + u1 * yp_stride, g, c);
     }
     __syncwarp();
     if (lane == 0) {
@@ -616,11 +663,12 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
   const int n0 = (blockIdx.x % p.ngroups) * p.G;
   const int Geff = min(p.G, p.N - n0);
   const int ncons = Geff * p.WPH;
-  const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, sizeof(TIn));
+  const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, sizeof(TIn), p.tc);
   const uint32_t sbase = ptx::smem_addr(smem);
   const uint32_t bars = sbase + L.bars;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
+      ptx::mbar_init(bar_raw_full(bars, s), 1);
       ptx::mbar_init(bar_in_full(bars, s), 1);
       ptx::mbar_init(bar_in_empty(bars, s), ncons + 1);
     }
@@ -631,17 +679,22 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
     ptx::mbar_init_fence();
   }
   __syncthreads();
-  if (warp == 0)
-    fwd_producer<V, F32>(p, L, sbase, b, n0, Geff);
-  else if (warp == 1)
+  if (warp == 0) {
+    // With fault injection on, the producer issues nothing, so every wait of
+    // the other warps runs into its time limit (tests of the time-out path).
+    if (p.inject_stall == 0) fwd_producer<V, F32>(p, L, sbase, b, n0, Geff);
+  } else if (warp == 1) {
     fwd_epilogue<V, F32>(p, L, sbase, b, n0, Geff);
-  else if (warp - 2 < ncons)
+  } else if (warp - 2 < ncons) {
     fwd_consumer<V, MT, F32>(p, L, sbase, b, n0, warp - 2);
+  }
 }
 
 template <int V, int MT, bool F32>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
-  const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2);
+  const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc);
+  if (p.tc < 2 || p.tc > 32) return cudaErrorInvalidValue;
+  if (p.G * p.WPH > max_consumer_warps<V, MT, F32>()) return cudaErrorInvalidConfiguration;
   auto kern = fwd_kernel<V, MT, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L.total));
@@ -653,14 +706,16 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-size_t fwd_smem_bytes(int K, int V, int G, int WPH, bool f32_inputs) {
-  return fwd_layout(K, V, G, WPH, f32_inputs ? 4 : 2).total;
+size_t fwd_smem_bytes(int K, int V, int G, int WPH, bool f32_inputs, int tc) {
+  return fwd_layout(K, V, G, WPH, f32_inputs ? 4 : 2, tc).total;
 }
 
 int fwd_max_consumer_warps(int V, int MT, bool f32_inputs) {
   if (f32_inputs) return V == 16 ? max_consumer_warps<16, 1, true>() : max_consumer_warps<32, 1, true>();
-  if (V == 16) return MT == 1 ? max_consumer_warps<16, 1, false>()
-                     : MT == 2 ? max_consumer_warps<16, 2, false>() : max_consumer_warps<16, 4, false>();
+  if (V == 16)
+    return MT == 1   ? max_consumer_warps<16, 1, false>()
+           : MT == 2 ? max_consumer_warps<16, 2, false>()
+                     : max_consumer_warps<16, 4, false>();
   return MT == 1 ? max_consumer_warps<32, 1, false>() : max_consumer_warps<32, 2, false>();
 }
 

@@ -38,14 +38,16 @@ struct FwdParams {
   int G;        // heads per CTA
   int WPH;      // consumer warps per head
   int ngroups;  // ceil(N / G)
+  int tc;       // time steps per shared-memory ring chunk (2..32)
   int* status;
   unsigned long long wait_limit_ns;
+  int inject_stall;  // test hook: 1 = the producer issues nothing
 };
 
 // Launches the forward kernel variant for (V, input dtype, MT m-tiles/warp).
 cudaError_t launch_fwd(const FwdParams& p, int V, bool f32_inputs, int MT, cudaStream_t stream);
 
 // Dynamic shared memory bytes the forward kernel needs.
-size_t fwd_smem_bytes(int K, int V, int G, int WPH, bool f32_inputs);
+size_t fwd_smem_bytes(int K, int V, int G, int WPH, bool f32_inputs, int tc);
 
 }  // namespace m2rnn

@@ -37,6 +37,7 @@ _EXPORTS = {
     "m2rnn_bwd": (ctypes.c_int, [_VP] * 19 + [ctypes.c_size_t, _VP]),
     "m2rnn_device_status": (ctypes.c_int, [_VP, _VP, ctypes.c_int, _VP]),
     "m2rnn_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_longlong]),
+    "m2rnn_set_fault_injection": (ctypes.c_int, [ctypes.c_int]),
 }
 
 
@@ -187,3 +188,8 @@ def device_status(clear: bool = True, stream=None):
 
 def set_wait_limit_ns(limit_ns: int):
     _check(lib().m2rnn_set_wait_limit_ns(int(limit_ns)), "m2rnn_set_wait_limit_ns")
+
+
+def set_fault_injection(mode: int):
+    """Test hook: 1 makes kernels start no input transfers (time-out path)."""
+    _check(lib().m2rnn_set_fault_injection(int(mode)), "m2rnn_set_fault_injection")

@@ -44,6 +44,11 @@ def test_status_strings_and_version(lib):
     assert m2rnn.status_string(12345) == "unknown status"
 
 
+def test_fault_injection_modes(lib):
+    assert lib.m2rnn_set_fault_injection(2) == -1
+    assert lib.m2rnn_set_fault_injection(0) == 0
+
+
 def test_num_checkpoints(lib):
     from non_linear_matrix_gb300.m2rnn import Shape, num_checkpoints
     assert num_checkpoints(Shape(8, 4096, 32, 64, 16, 1, 64)) == 64
