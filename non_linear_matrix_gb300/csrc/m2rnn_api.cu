@@ -125,6 +125,75 @@ FwdConfig choose_fwd(const m2rnn_shape* s, int sms) {
   return {MT, WPH, best, tc};
 }
 
+struct WavePlan {
+  int B1;       // leading batch items run with the main configuration (0 = one launch)
+  int tail_G;   // heads per CTA of the launch covering the remaining batch items
+  int tail_tc;  // its ring chunk length
+};
+
+// Decides whether the batch items beyond whole waves of the main
+// configuration should get a launch of their own with fewer heads per CTA,
+// spread over all SMs, because that shortens the run.
+WavePlan plan_full_waves(const m2rnn_shape* s, int sms, const FwdConfig& cfg,
+                         const m2rnn::FwdParams& p, bool f32) {
+  const WavePlan none{0, cfg.G, cfg.tc};
+  const int R = m2rnn::fwd_ctas_per_sm(p, s->V, f32, cfg.MT);
+  if (R <= 0 || s->N % cfg.G != 0) return none;
+  const long long wave_heads = static_cast<long long>(sms) * R * cfg.G;
+  if (wave_heads % s->N != 0) return none;
+  const long long wave_b = wave_heads / s->N;
+  const long long heads = static_cast<long long>(s->B) * s->N;
+  if (heads <= wave_heads) return none;
+  const long long B1 = (s->B / wave_b) * wave_b;
+  const long long rem_heads = (s->B - B1) * s->N;
+  if (rem_heads == 0) return none;
+  // Cost of the remainder in "heads per SM" (time of the slowest SM).
+  auto cost = [&](int G, int R_) -> long long {
+    const long long ctas = rem_heads / G;
+    const long long per_sm = (ctas + sms - 1) / sms;
+    return per_sm <= R_ ? per_sm * G : -1;
+  };
+  long long best = cost(cfg.G, R);
+  if (best < 0) best = ((rem_heads / cfg.G + static_cast<long long>(sms) * R - 1) /
+                        (static_cast<long long>(sms) * R)) * R * cfg.G;
+  int bestG = 0, bestTc = cfg.tc;
+  for (int G = cfg.G - 1; G >= 1; --G) {
+    if (s->N % G != 0) continue;
+    // Shorter ring chunks shrink the per-CTA shared memory so that more of
+    // the small CTAs fit on an SM.
+    for (int tc = 32; tc >= 8; tc /= 2) {
+      if (m2rnn::fwd_smem_bytes(s->K, s->V, G, p.WPH, f32, tc) > kSmemBudget) continue;
+      m2rnn::FwdParams q = p;
+      q.G = G;
+      q.tc = tc;
+      const int RG = m2rnn::fwd_ctas_per_sm(q, s->V, f32, cfg.MT);
+      const long long c = RG > 0 ? cost(G, RG) : -1;
+      if (c > 0 && c < best) {
+        best = c;
+        bestG = G;
+        bestTc = tc;
+      }
+    }
+  }
+  if (bestG == 0) return none;
+  return {static_cast<int>(B1), bestG, bestTc};
+}
+
+// Parameters with every per-batch pointer advanced by b0 batch items.
+m2rnn::FwdParams offset_batch(const m2rnn::FwdParams& p, int b0, const m2rnn_shape* s, int es) {
+  m2rnn::FwdParams r = p;
+  const size_t B0 = static_cast<size_t>(b0), T = s->T, N = s->N, K = s->K, V = s->V;
+  r.q = static_cast<const char*>(p.q) + B0 * T * K * es;
+  r.k = static_cast<const char*>(p.k) + B0 * T * K * es;
+  r.v = static_cast<const char*>(p.v) + B0 * T * N * V * es;
+  r.f = static_cast<const char*>(p.f) + B0 * T * N * es;
+  r.y = static_cast<char*>(p.y) + B0 * T * N * V * es;
+  if (p.H0) r.H0 = p.H0 + B0 * N * K * V;
+  if (p.HT) r.HT = p.HT + B0 * N * K * V;
+  if (p.ckpt) r.ckpt = p.ckpt + B0 * N * static_cast<size_t>(p.nck) * K * V;
+  return r;
+}
+
 }  // namespace
 
 extern "C" {
@@ -200,6 +269,7 @@ int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   for (const void* p : req)
     if ((rc = check_ptr(p, dev, true)) != M2RNN_OK) return rc;
   if ((rc = check_ptr(ckpt, dev, false)) != M2RNN_OK) return rc;
+  const bool f32 = s->in_dtype == M2RNN_F32;
   const FwdConfig cfg = choose_fwd(s, sms);
   m2rnn::FwdParams p;
   p.q = q;
@@ -225,7 +295,27 @@ int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   p.status = status;
   p.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
   p.inject_stall = g_fault_injection.load();
-  return status_from_cuda(m2rnn::launch_fwd(p, s->V, s->in_dtype == M2RNN_F32, cfg.MT, st));
+
+  // Wave planning.  All CTAs of a launch run equally long, so when the heads
+  // fill some whole waves plus a remainder, the remainder's batch items get a
+  // second launch with fewer heads per CTA, spread over all SMs.
+  // M2RNN_FWD_ONE_LAUNCH=1 disables the split (A/B measurement).
+  const char* one = std::getenv("M2RNN_FWD_ONE_LAUNCH");
+  const WavePlan plan = (one && one[0] == '1') ? WavePlan{0, cfg.G, cfg.tc}
+                                               : plan_full_waves(s, sms, cfg, p, f32);
+  const int B1 = plan.B1;
+  if (B1 <= 0 || B1 >= s->B)
+    return status_from_cuda(m2rnn::launch_fwd(p, s->V, f32, cfg.MT, st));
+  m2rnn::FwdParams p1 = p;
+  p1.B = B1;
+  cudaError_t e = m2rnn::launch_fwd(p1, s->V, f32, cfg.MT, st);
+  if (e != cudaSuccess) return M2RNN_ERR_CUDA;
+  m2rnn::FwdParams p2 = offset_batch(p, B1, s, f32 ? 4 : 2);
+  p2.B = s->B - B1;
+  p2.G = plan.tail_G;
+  p2.ngroups = (s->N + p2.G - 1) / p2.G;
+  p2.tc = plan.tail_tc;
+  return status_from_cuda(m2rnn::launch_fwd(p2, s->V, f32, cfg.MT, st));
 }
 
 }  // extern "C"

@@ -691,6 +691,20 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
 }
 
 template <int V, int MT, bool F32>
+int ctas_per_sm_t(const FwdParams& p) {
+  const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc);
+  auto kern = fwd_kernel<V, MT, F32>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(L.total)) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * (2 + p.G * p.WPH), L.total) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <int V, int MT, bool F32>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
   const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc);
   if (p.tc < 2 || p.tc > 32) return cudaErrorInvalidValue;
@@ -717,6 +731,14 @@ int fwd_max_consumer_warps(int V, int MT, bool f32_inputs) {
            : MT == 2 ? max_consumer_warps<16, 2, false>()
                      : max_consumer_warps<16, 4, false>();
   return MT == 1 ? max_consumer_warps<32, 1, false>() : max_consumer_warps<32, 2, false>();
+}
+
+int fwd_ctas_per_sm(const FwdParams& p, int V, bool f32_inputs, int MT) {
+  if (f32_inputs) return V == 16 ? ctas_per_sm_t<16, 1, true>(p) : ctas_per_sm_t<32, 1, true>(p);
+  if (V == 16)
+    return MT == 1 ? ctas_per_sm_t<16, 1, false>(p)
+           : MT == 2 ? ctas_per_sm_t<16, 2, false>(p) : ctas_per_sm_t<16, 4, false>(p);
+  return MT == 1 ? ctas_per_sm_t<32, 1, false>(p) : ctas_per_sm_t<32, 2, false>(p);
 }
 
 cudaError_t launch_fwd(const FwdParams& p, int V, bool f32_inputs, int MT, cudaStream_t stream) {

@@ -47,6 +47,9 @@ struct FwdParams {
 // Launches the forward kernel variant for (V, input dtype, MT m-tiles/warp).
 cudaError_t launch_fwd(const FwdParams& p, int V, bool f32_inputs, int MT, cudaStream_t stream);
 
+// Resident CTAs per SM of the forward variant for p's G, WPH, K and tc.
+int fwd_ctas_per_sm(const FwdParams& p, int V, bool f32_inputs, int MT);
+
 // Dynamic shared memory bytes the forward kernel needs.
 size_t fwd_smem_bytes(int K, int V, int G, int WPH, bool f32_inputs, int tc);
 
