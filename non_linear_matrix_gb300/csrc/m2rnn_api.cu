@@ -194,6 +194,106 @@ m2rnn::FwdParams offset_batch(const m2rnn::FwdParams& p, int b0, const m2rnn_sha
   return r;
 }
 
+// Plans and launches the forward pass (pointers already validated).  y may
+// be NULL (checkpoint-only runs for the backward pass).
+int run_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
+            const void* W, const void* w_r, const float* H0, void* y, float* H_T, float* ckpt,
+            cudaStream_t st, int* status, int sms) {
+  const bool want_ckpt = ckpt != nullptr && s->ckpt_every > 0 && s->T > 0;
+  const bool f32 = s->in_dtype == M2RNN_F32;
+  const FwdConfig cfg = choose_fwd(s, sms);
+  m2rnn::FwdParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.f = f;
+  p.W = W;
+  p.w_r = w_r;
+  p.H0 = H0;
+  p.y = y;
+  p.HT = H_T;
+  p.ckpt = want_ckpt ? ckpt : nullptr;  // NULL: no checkpoints written
+  p.B = s->B;
+  p.T = s->T;
+  p.N = s->N;
+  p.K = s->K;
+  p.C = want_ckpt ? s->ckpt_every : 0;
+  p.nck = static_cast<int>(m2rnn_num_checkpoints(s));
+  p.G = cfg.G;
+  p.WPH = cfg.WPH;
+  p.ngroups = (s->N + cfg.G - 1) / cfg.G;
+  p.tc = cfg.tc;
+  p.status = status;
+  p.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
+  p.inject_stall = g_fault_injection.load();
+
+  // Wave planning.  All CTAs of a launch run equally long, so when the heads
+  // fill some whole waves plus a remainder, the remainder's batch items get a
+  // second launch with fewer heads per CTA, spread over all SMs.
+  // M2RNN_FWD_ONE_LAUNCH=1 disables the split (A/B measurement).
+  const char* one = std::getenv("M2RNN_FWD_ONE_LAUNCH");
+  const WavePlan plan = (one && one[0] == '1') ? WavePlan{0, cfg.G, cfg.tc}
+                                               : plan_full_waves(s, sms, cfg, p, f32);
+  const int B1 = plan.B1;
+  if (B1 <= 0 || B1 >= s->B)
+    return status_from_cuda(m2rnn::launch_fwd(p, s->V, f32, cfg.MT, st));
+  m2rnn::FwdParams p1 = p;
+  p1.B = B1;
+  cudaError_t e = m2rnn::launch_fwd(p1, s->V, f32, cfg.MT, st);
+  if (e != cudaSuccess) return M2RNN_ERR_CUDA;
+  m2rnn::FwdParams p2 = offset_batch(p, B1, s, f32 ? 4 : 2);
+  p2.B = s->B - B1;
+  p2.G = plan.tail_G;
+  p2.ngroups = (s->N + p2.G - 1) / p2.G;
+  p2.tc = plan.tail_tc;
+  return status_from_cuda(m2rnn::launch_fwd(p2, s->V, f32, cfg.MT, st));
+}
+
+// ---- backward planning ------------------------------------------------------
+
+// Longest checkpoint interval the backward kernel takes directly; longer ones
+// are re-checkpointed into the workspace at kBwdDefaultC.
+constexpr int kBwdMaxC = 128;
+constexpr int kBwdDefaultC = 64;
+
+// Interval the backward kernel works with, and whether it needs its own
+// checkpoints (in the workspace).
+int bwd_interval(const m2rnn_shape* s, bool ckpt_given, bool* own_ckpt) {
+  const int C = s->ckpt_every;
+  const bool direct = ckpt_given && C <= kBwdMaxC;
+  *own_ckpt = !direct;
+  return direct ? C : (C <= kBwdMaxC ? C : kBwdDefaultC);
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Picks warps per CTA (16 rows each) for the fewest waves; ties go to more
+// rows per CTA (fewer cross-CTA reductions).
+bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
+  const int mtiles = p.K / 16;
+  int best_w = 0;
+  long long best_waves = 0;
+  for (int w = mtiles < 8 ? mtiles : 8; w >= 1; w /= 2) {
+    if (mtiles % w != 0) continue;
+    if (m2rnn::bwd_smem_bytes(V, p.C, p.S2, w, f32) > kSmemBudget) continue;
+    m2rnn::BwdParams q = p;
+    q.WPC = w;
+    q.nslices = mtiles / w;
+    const int R = m2rnn::bwd_ctas_per_sm(q, V, f32);
+    if (R <= 0) continue;
+    const long long ctas = static_cast<long long>(p.B) * p.N * q.nslices;
+    const long long waves = (ctas + static_cast<long long>(sms) * R - 1) / (static_cast<long long>(sms) * R);
+    if (best_w == 0 || waves < best_waves) {
+      best_w = w;
+      best_waves = waves;
+    }
+  }
+  if (best_w == 0) return false;
+  p.WPC = best_w;
+  p.nslices = mtiles / best_w;
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -269,53 +369,104 @@ int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   for (const void* p : req)
     if ((rc = check_ptr(p, dev, true)) != M2RNN_OK) return rc;
   if ((rc = check_ptr(ckpt, dev, false)) != M2RNN_OK) return rc;
+  return run_fwd(s, q, k, v, f, W, w_r, H0, y, H_T, want_ckpt ? ckpt : nullptr, st, status, sms);
+}
+
+size_t m2rnn_bwd_workspace_size(const m2rnn_shape* s, int ckpt_given) {
+  if (check_shape(s) != M2RNN_OK || s->ckpt_every <= 0 || s->T == 0) return 0;
+  bool own = false;
+  const int C = bwd_interval(s, ckpt_given != 0, &own);
+  if (!own) return 0;
+  const size_t nck = static_cast<size_t>((s->T + C - 1) / C);
+  return align256(static_cast<size_t>(s->B) * s->N * nck * s->K * s->V * sizeof(float));
+}
+
+int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
+              const void* W, const void* w_r, const float* H0, const float* ckpt, const void* dy,
+              const float* dH_T, float* dq, float* dk, float* dv, float* df, float* dW, float* dw_r,
+              float* dH0, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_shape(s);
+  if (rc != M2RNN_OK) return rc;
+  if (s->ckpt_every <= 0) return M2RNN_ERR_INVALID_ARG;
+  int dev, sms;
+  int* status;
+  rc = device_info(&dev, &status, &sms);
+  if (rc != M2RNN_OK) return rc;
+  const void* always[] = {W, w_r, dW, dw_r};
+  for (const void* x : always)
+    if ((rc = check_ptr(x, dev, true)) != M2RNN_OK) return rc;
+  const void* optional[] = {H0, dH_T, dH0};
+  for (const void* x : optional)
+    if ((rc = check_ptr(x, dev, false)) != M2RNN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool f32 = s->in_dtype == M2RNN_F32;
-  const FwdConfig cfg = choose_fwd(s, sms);
-  m2rnn::FwdParams p;
+  const size_t es = f32 ? 4 : 2;
+  const size_t NV = static_cast<size_t>(s->N) * s->V;
+  const size_t state_bytes = static_cast<size_t>(s->B) * s->N * s->K * s->V * sizeof(float);
+  if (cudaMemsetAsync(dW, 0, NV * s->V * sizeof(float), st) != cudaSuccess ||
+      cudaMemsetAsync(dw_r, 0, NV * sizeof(float), st) != cudaSuccess)
+    return M2RNN_ERR_CUDA;
+  if (s->T == 0) {  // no steps: dH0 = dH_T
+    if (dH0 == nullptr) return M2RNN_OK;
+    return status_from_cuda(dH_T ? cudaMemcpyAsync(dH0, dH_T, state_bytes, cudaMemcpyDeviceToDevice, st)
+                                 : cudaMemsetAsync(dH0, 0, state_bytes, st));
+  }
+  const void* req[] = {q, k, v, f, dy, dq, dk, dv, df};
+  for (const void* x : req)
+    if ((rc = check_ptr(x, dev, true)) != M2RNN_OK) return rc;
+  if ((rc = check_ptr(ckpt, dev, false)) != M2RNN_OK) return rc;
+  bool own = false;
+  const int C = bwd_interval(s, ckpt != nullptr, &own);
+  const size_t need = m2rnn_bwd_workspace_size(s, ckpt != nullptr);
+  if (need > 0) {
+    if (workspace == nullptr || ws_bytes < need) return M2RNN_ERR_WORKSPACE;
+    if ((rc = check_ptr(workspace, dev, true)) != M2RNN_OK) return rc;
+  }
+  const float* ck = ckpt;
+  if (own) {  // checkpoints at interval C into the workspace (no y written)
+    m2rnn_shape sf = *s;
+    sf.ckpt_every = C;
+    rc = run_fwd(&sf, q, k, v, f, W, w_r, H0, nullptr, nullptr, static_cast<float*>(workspace), st,
+                 status, sms);
+    if (rc != M2RNN_OK) return rc;
+    ck = static_cast<const float*>(workspace);
+  }
+  m2rnn::BwdParams p;
   p.q = q;
   p.k = k;
   p.v = v;
   p.f = f;
   p.W = W;
   p.w_r = w_r;
-  p.H0 = H0;
-  p.y = y;
-  p.HT = H_T;
-  p.ckpt = want_ckpt ? ckpt : nullptr;  // NULL: no checkpoints written
+  p.ckpt = ck;
+  p.dy = dy;
+  p.dHT = dH_T;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.df = df;
+  p.dW = dW;
+  p.dw_r = dw_r;
+  p.dH0 = dH0;
   p.B = s->B;
   p.T = s->T;
   p.N = s->N;
   p.K = s->K;
-  p.C = want_ckpt ? s->ckpt_every : 0;
-  p.nck = static_cast<int>(m2rnn_num_checkpoints(s));
-  p.G = cfg.G;
-  p.WPH = cfg.WPH;
-  p.ngroups = (s->N + cfg.G - 1) / cfg.G;
-  p.tc = cfg.tc;
-  p.status = status;
-  p.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
-  p.inject_stall = g_fault_injection.load();
-
-  // Wave planning.  All CTAs of a launch run equally long, so when the heads
-  // fill some whole waves plus a remainder, the remainder's batch items get a
-  // second launch with fewer heads per CTA, spread over all SMs.
-  // M2RNN_FWD_ONE_LAUNCH=1 disables the split (A/B measurement).
-  const char* one = std::getenv("M2RNN_FWD_ONE_LAUNCH");
-  const WavePlan plan = (one && one[0] == '1') ? WavePlan{0, cfg.G, cfg.tc}
-                                               : plan_full_waves(s, sms, cfg, p, f32);
-  const int B1 = plan.B1;
-  if (B1 <= 0 || B1 >= s->B)
-    return status_from_cuda(m2rnn::launch_fwd(p, s->V, f32, cfg.MT, st));
-  m2rnn::FwdParams p1 = p;
-  p1.B = B1;
-  cudaError_t e = m2rnn::launch_fwd(p1, s->V, f32, cfg.MT, st);
-  if (e != cudaSuccess) return M2RNN_ERR_CUDA;
-  m2rnn::FwdParams p2 = offset_batch(p, B1, s, f32 ? 4 : 2);
-  p2.B = s->B - B1;
-  p2.G = plan.tail_G;
-  p2.ngroups = (s->N + p2.G - 1) / p2.G;
-  p2.tc = plan.tail_tc;
-  return status_from_cuda(m2rnn::launch_fwd(p2, s->V, f32, cfg.MT, st));
+  p.C = C;
+  p.nck = (s->T + C - 1) / C;
+  p.S2 = C < 8 ? C : 8;
+  p.WPC = 1;
+  p.nslices = s->K / 16;
+  if (!choose_bwd(p, s->V, f32, sms)) return M2RNN_ERR_UNSUPPORTED_SHAPE;
+  const size_t BT = static_cast<size_t>(s->B) * s->T;
+  if (cudaMemsetAsync(dq, 0, BT * s->K * sizeof(float), st) != cudaSuccess ||
+      cudaMemsetAsync(dk, 0, BT * s->K * sizeof(float), st) != cudaSuccess)
+    return M2RNN_ERR_CUDA;
+  if (p.nslices > 1 && (cudaMemsetAsync(dv, 0, BT * NV * sizeof(float), st) != cudaSuccess ||
+                        cudaMemsetAsync(df, 0, BT * s->N * sizeof(float), st) != cudaSuccess))
+    return M2RNN_ERR_CUDA;
+  (void)es;
+  return status_from_cuda(m2rnn::launch_bwd(p, s->V, f32, st));
 }
 
 }  // extern "C"

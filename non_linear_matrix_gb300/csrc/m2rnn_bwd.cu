@@ -1,21 +1,646 @@
-// m2rnn_bwd.cu -- backward entry points (kernel under construction).
-#include <cstddef>
+// m2rnn_bwd.cu -- BPTT backward kernel of the M2RNN recurrence.
+//
+// Chain rule of the backup frame "the recurrent gradient needs both paths"
+// in the discussion deck of "M2RNN: Non-Linear RNNs with Matrix-Valued
+// States": with u_t = dL/dy_t and C_t the gradient arriving from later steps,
+//     R_t = C_t + q_t u_t^T,   D_t = ((1 - f_t) R_t) (.) (1 - Z_t (.) Z_t),
+//     C_{t-1} = f_t R_t + D_t W^T,   dL/df_t = <R_t, H_{t-1} - Z_t>_F,
+//     dL/dW = sum_t H_{t-1}^T D_t,
+// plus the terms Eqs. (10)-(12) give for the other inputs:
+//     dk_t = sum_n D_t v_t,  dq_t = sum_n H_t u_t,  dv_t = D_t^T k_t + w_r (.) u_t,
+//     dw_r = sum_{b,t} u_t (.) v_t,  dH_0 = C_0.
+// (The paper's printed Algorithm 2 drops C_t; the deck's boxed recursion is
+// followed.)
+//
+// The deck's backward caches every state in HBM ("recompute the trajectory,
+// cache states in HBM, then run the reverse sweep"); here nothing but the
+// checkpoints H_{cC} (every C steps, written by the forward pass) leaves the
+// chip.  CTA = one (batch b, head n, slice of 16*WPC rows); warp w owns 16
+// rows in mma.sync m16n8k16 accumulator layout.  For each checkpoint interval,
+// last first:
+//   1. load the interval's inputs into shared memory;
+//   2. recompute the interval forward from its checkpoint, keeping a
+//      sub-checkpoint every S2 steps (fp32);
+//   3. for each sub-interval, last first: recompute its S2 steps keeping
+//      bf16(H) (as MMA operand fragments) and Z (fp32), then run the reverse
+//      steps over it; per-step partials go to shared memory and are flushed
+//      with vector reductions (head sums of dq, dk) or stores.
+// All per-thread state lives in thread-private shared-memory slots laid out
+// lane-contiguously (no bank conflicts).  The recomputation performs the
+// same operations as the forward kernel, so it reproduces its trajectory.
+// Synchronisation is __syncthreads only (no spin waits).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
 
 #include "m2rnn.h"
+#include "m2rnn_internal.h"
+#include "ptx.cuh"
 
-extern "C" {
+namespace m2rnn {
+namespace {
 
-size_t m2rnn_bwd_workspace_size(const m2rnn_shape* s, int ckpt_given) {
-  (void)s;
-  (void)ckpt_given;
-  return 0;
+template <bool F32>
+struct InT;
+template <>
+struct InT<true> {
+  using T = float;
+};
+template <>
+struct InT<false> {
+  using T = __nv_bfloat16;
+};
+
+__device__ __forceinline__ float tof(float x) { return x; }
+__device__ __forceinline__ float tof(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Shared-memory layout of one CTA (byte offsets).
+struct BwdLayout {
+  uint32_t in_q, in_k, in_v, in_dy, in_f;  // interval inputs
+  uint32_t subck;                          // [NS1][WPC][NT][32][4] fp32
+  uint32_t hs;                             // [S2+1][WPC][KS][32][4] u32 (bf16 frags)
+  uint32_t zs;                             // [S2][WPC][NT][32][4] fp32
+  uint32_t r_dq, r_dk;                     // [S2][RS] fp32
+  uint32_t r_dv;                           // [S2][WPC][V] fp32
+  uint32_t r_df;                           // [S2][WPC] fp32
+  uint32_t total;
+};
+
+__host__ __device__ inline uint32_t al(uint32_t x) { return (x + 127u) / 128u * 128u; }
+
+__host__ __device__ inline BwdLayout bwd_layout(int V, int C, int S2, int WPC, int es) {
+  const int RS = 16 * WPC, NT = V / 8, KS = V / 16, NS1 = (C + S2 - 1) / S2;
+  BwdLayout L;
+  uint32_t o = 0;
+  L.in_q = o;
+  o = al(o + C * RS * es);
+  L.in_k = o;
+  o = al(o + C * RS * es);
+  L.in_v = o;
+  o = al(o + C * V * es);
+  L.in_dy = o;
+  o = al(o + C * V * es);
+  L.in_f = o;
+  o = al(o + C * 4);
+  L.subck = o;
+  o = al(o + NS1 * WPC * NT * 512);
+  L.hs = o;
+  o = al(o + (S2 + 1) * WPC * KS * 512);
+  L.zs = o;
+  o = al(o + S2 * WPC * NT * 512);
+  L.r_dq = o;
+  o = al(o + S2 * RS * 4);
+  L.r_dk = o;
+  o = al(o + S2 * RS * 4);
+  L.r_dv = o;
+  o = al(o + S2 * WPC * V * 4);
+  L.r_df = o;
+  o = al(o + S2 * WPC * 4);
+  L.total = o;
+  return L;
 }
 
-int m2rnn_bwd(const m2rnn_shape* s, const void*, const void*, const void*, const void*,
-              const void*, const void*, const float*, const float*, const void*, const float*,
-              float*, float*, float*, float*, float*, float*, float*, void*, size_t, void*) {
-  (void)s;
-  return M2RNN_ERR_UNSUPPORTED_SHAPE;
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void red_add(float* p, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(a) : "memory");
+}
+__device__ __forceinline__ void sts_u32x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                          uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 
-}  // extern "C"
+// bf16x2 pair of two input values (rounding fp32 inputs to bf16).
+template <bool F32>
+__device__ __forceinline__ uint32_t pair_bf16(uint32_t addr) {
+  if (F32) {
+    const float2 x = ptx::lds_f32x2(addr);
+    return ptx::pack_bf16x2(x.x, x.y);
+  }
+  return ptx::lds_u32(addr);
+}
+// Two consecutive input values as floats.
+template <bool F32>
+__device__ __forceinline__ float2 pair_f32(uint32_t addr) {
+  if (F32) return ptx::lds_f32x2(addr);
+  const uint32_t w = ptx::lds_u32(addr);
+  return make_float2(ptx::bf16x2_lo(w), ptx::bf16x2_hi(w));
+}
+template <bool F32>
+__device__ __forceinline__ float one_f32(uint32_t addr) {
+  if (F32) return ptx::lds_f32(addr);
+  return __uint_as_float(ptx::lds_u16(addr) << 16);
+}
+
+template <int V>
+__device__ __forceinline__ void pack_frag(const float (&H)[V / 8][4], uint32_t (&A)[V / 16][4]) {
+#pragma unroll
+  for (int ks = 0; ks < V / 16; ++ks) {
+    A[ks][0] = ptx::pack_bf16x2(H[2 * ks][0], H[2 * ks][1]);
+    A[ks][1] = ptx::pack_bf16x2(H[2 * ks][2], H[2 * ks][3]);
+    A[ks][2] = ptx::pack_bf16x2(H[2 * ks + 1][0], H[2 * ks + 1][1]);
+    A[ks][3] = ptx::pack_bf16x2(H[2 * ks + 1][2], H[2 * ks + 1][3]);
+  }
+}
+template <int V>
+__device__ __forceinline__ void pack_frag_lo(const float (&H)[V / 8][4], const uint32_t (&A)[V / 16][4],
+                                             uint32_t (&Al)[V / 16][4]) {
+#pragma unroll
+  for (int ks = 0; ks < V / 16; ++ks)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int nt = 2 * ks + (i >> 1), r = 2 * (i & 1);
+      Al[ks][i] = ptx::pack_bf16x2(H[nt][r] - ptx::bf16x2_lo(A[ks][i]),
+                                   H[nt][r + 1] - ptx::bf16x2_hi(A[ks][i]));
+    }
+}
+
+// One forward step of Eqs. (10)-(11) for this warp's 16 rows, with exactly
+// the operations of the forward kernel (so trajectories agree bitwise).
+// Returns Z in Zo; updates H, A (and Al on the fp32-input path).
+template <int V, bool F32>
+__device__ __forceinline__ void recompute_step(float (&H)[V / 8][4], uint32_t (&A)[V / 16][4],
+                                               uint32_t (&Al)[V / 16][4],
+                                               const uint32_t (&Bw)[V / 16][V / 8][2],
+                                               const uint32_t (&Bwl)[V / 16][V / 8][2], float k0,
+                                               float k1, const float2 (&vv)[V / 8], float fg,
+                                               float (&Zo)[V / 8][4]) {
+  constexpr int NT = V / 8, KS = V / 16;
+  const float2 kk0 = make_float2(k0, k0), kk1 = make_float2(k1, k1);
+  const float2 f2 = make_float2(fg, fg), m1 = make_float2(-1.f, -1.f);
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float2 lo = __fmul2_rn(kk0, vv[nt]), hi = __fmul2_rn(kk1, vv[nt]);
+    acc[nt][0] = lo.x;
+    acc[nt][1] = lo.y;
+    acc[nt][2] = hi.x;
+    acc[nt][3] = hi.y;
+  }
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      ptx::mma_bf16_16816(acc[nt], A[ks], Bw[ks][nt][0], Bw[ks][nt][1]);
+      if (F32) {
+        ptx::mma_bf16_16816(acc[nt], A[ks], Bwl[ks][nt][0], Bwl[ks][nt][1]);
+        ptx::mma_bf16_16816(acc[nt], Al[ks], Bw[ks][nt][0], Bw[ks][nt][1]);
+      }
+    }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float2 z;
+      z.x = F32 ? tanhf(acc[nt][2 * h]) : ptx::tanh_approx(acc[nt][2 * h]);
+      z.y = F32 ? tanhf(acc[nt][2 * h + 1]) : ptx::tanh_approx(acc[nt][2 * h + 1]);
+      const float2 hp = make_float2(H[nt][2 * h], H[nt][2 * h + 1]);
+      const float2 d = __ffma2_rn(m1, z, hp);
+      const float2 hn = __ffma2_rn(f2, d, z);
+      H[nt][2 * h] = hn.x;
+      H[nt][2 * h + 1] = hn.y;
+      Zo[nt][2 * h] = z.x;
+      Zo[nt][2 * h + 1] = z.y;
+    }
+  pack_frag<V>(H, A);
+  if (F32) pack_frag_lo<V>(H, A, Al);
+}
+
+template <int V, bool F32>
+__global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
+  using TIn = typename InT<F32>::T;
+  constexpr int es = sizeof(TIn);
+  constexpr int NT = V / 8, KS = V / 16;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int WPC = p.WPC, RS = 16 * WPC, nthr = 32 * WPC;
+  const int K = p.K, T = p.T, N = p.N, C = p.C, S2 = p.S2;
+  const int slice = blockIdx.x % p.nslices;
+  const int bn = blockIdx.x / p.nslices;
+  const int b = bn / N, n = bn % N;
+  const int row0c = slice * RS;            // first row of this CTA
+  const int row0 = row0c + 16 * warp;      // first row of this warp
+  const BwdLayout L = bwd_layout(V, C, S2, WPC, es);
+  const uint32_t sb = ptx::smem_addr(smem);
+
+  const TIn* q = static_cast<const TIn*>(p.q);
+  const TIn* kin = static_cast<const TIn*>(p.k);
+  const TIn* vin = static_cast<const TIn*>(p.v);
+  const TIn* fin = static_cast<const TIn*>(p.f);
+  const TIn* dy = static_cast<const TIn*>(p.dy);
+  const TIn* Wn = static_cast<const TIn*>(p.W) + static_cast<size_t>(n) * V * V;
+  const TIn* wr = static_cast<const TIn*>(p.w_r) + static_cast<size_t>(n) * V;
+
+  // W as the B operand of H W (k = l, n = j) and of D W^T (k = j, n = l).
+  uint32_t Bw[KS][NT][2], Bwl[KS][NT][2], Bt[KS][NT][2], Btl[KS][NT][2];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int kk = 16 * ks + 8 * h + 2 * c, nn = 8 * nt + g;
+        const float w0 = tof(Wn[kk * V + nn]), w1 = tof(Wn[(kk + 1) * V + nn]);
+        Bw[ks][nt][h] = ptx::pack_bf16x2(w0, w1);
+        Bwl[ks][nt][h] = F32 ? ptx::pack_bf16x2(w0 - ptx::bf16x2_lo(Bw[ks][nt][h]),
+                                                w1 - ptx::bf16x2_hi(Bw[ks][nt][h]))
+                             : 0u;
+        const float t0 = tof(Wn[nn * V + kk]), t1 = tof(Wn[nn * V + kk + 1]);
+        Bt[ks][nt][h] = ptx::pack_bf16x2(t0, t1);
+        Btl[ks][nt][h] = F32 ? ptx::pack_bf16x2(t0 - ptx::bf16x2_lo(Bt[ks][nt][h]),
+                                                t1 - ptx::bf16x2_hi(Bt[ks][nt][h]))
+                             : 0u;
+      }
+
+  const size_t sidx = (static_cast<size_t>(b) * N + n) * K * V;  // [K][V] block of (b, n)
+  // C (state gradient) for this thread's elements, from dH_T or 0.
+  float Cg[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int row = row0 + g + 8 * (r >> 1), col = 8 * nt + 2 * c + (r & 1);
+      Cg[nt][r] = p.dHT ? p.dHT[sidx + row * V + col] : 0.f;
+    }
+  float dW[KS][NT][4];
+#pragma unroll
+  for (int a = 0; a < KS; ++a)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) dW[a][nt][0] = dW[a][nt][1] = dW[a][nt][2] = dW[a][nt][3] = 0.f;
+  float dwr_acc = 0.f;  // thread j < V of slice 0: sum_t u_j v_j
+
+  // thread-private slot addresses (lane-contiguous 16-byte groups)
+  const uint32_t lane16 = static_cast<uint32_t>(lane * 16);
+  auto slot_f = [&](uint32_t base, int idx, int nt) -> uint32_t {  // fp32 [idx][warp][nt]
+    return base + static_cast<uint32_t>(((idx * WPC + warp) * NT + nt) * 512) + lane16;
+  };
+  auto slot_h = [&](int idx, int ks) -> uint32_t {  // bf16 frags [idx][warp][ks]
+    return sb + L.hs + static_cast<uint32_t>(((idx * WPC + warp) * KS + ks) * 512) + lane16;
+  };
+
+  const int nck = p.nck;
+  for (int ci = nck - 1; ci >= 0; --ci) {
+    const int t0 = ci * C;
+    const int Lc = min(C, T - t0);
+    // ---- 1. interval inputs -> shared memory ----
+    __syncthreads();
+    {
+      const size_t bt0 = static_cast<size_t>(b) * T + t0;
+      const int qv = RS * es / 16;  // 16-byte vectors per step
+      for (int e = tid; e < Lc * qv; e += nthr) {
+        const int s = e / qv, x = e - s * qv;
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(q + (bt0 + s) * K + row0c) + x);
+        const uint4 d = __ldg(reinterpret_cast<const uint4*>(kin + (bt0 + s) * K + row0c) + x);
+        sts_u32x4(sb + L.in_q + static_cast<uint32_t>(s * RS * es + 16 * x), a.x, a.y, a.z, a.w);
+        sts_u32x4(sb + L.in_k + static_cast<uint32_t>(s * RS * es + 16 * x), d.x, d.y, d.z, d.w);
+      }
+      const int vvn = V * es / 16;
+      for (int e = tid; e < Lc * vvn; e += nthr) {
+        const int s = e / vvn, x = e - s * vvn;
+        const size_t off = ((bt0 + s) * N + n) * V;
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(vin + off) + x);
+        const uint4 d = __ldg(reinterpret_cast<const uint4*>(dy + off) + x);
+        sts_u32x4(sb + L.in_v + static_cast<uint32_t>(s * V * es + 16 * x), a.x, a.y, a.z, a.w);
+        sts_u32x4(sb + L.in_dy + static_cast<uint32_t>(s * V * es + 16 * x), d.x, d.y, d.z, d.w);
+      }
+      for (int s = tid; s < Lc; s += nthr)
+        ptx::sts_f32(sb + L.in_f + 4 * s, tof(fin[(bt0 + s) * N + n]));
+    }
+    // checkpoint H_{t0} of this thread's elements
+    float H[NT][4];
+    {
+      const float* ck = p.ckpt + ((static_cast<size_t>(b) * N + n) * nck + ci) * K * V;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float2 x = *reinterpret_cast<const float2*>(ck + (row0 + g + 8 * h) * V + 8 * nt + 2 * c);
+          H[nt][2 * h] = x.x;
+          H[nt][2 * h + 1] = x.y;
+        }
+    }
+    __syncthreads();
+
+    // per-step input addresses
+    const uint32_t kq_row = static_cast<uint32_t>((16 * warp) * es);
+    auto k_rows = [&](int s, float& k0, float& k1) {
+      const uint32_t a = sb + L.in_k + static_cast<uint32_t>(s * RS * es) + kq_row;
+      k0 = one_f32<F32>(a + g * es);
+      k1 = one_f32<F32>(a + (g + 8) * es);
+    };
+    auto v_pairs = [&](int s, float2 (&vv)[NT]) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        vv[nt] = pair_f32<F32>(sb + L.in_v + static_cast<uint32_t>((s * V + 8 * nt + 2 * c) * es));
+    };
+
+    // ---- 2. recompute the interval, sub-checkpoint every S2 steps ----
+    uint32_t A[KS][4], Al[KS][4];
+    pack_frag<V>(H, A);
+    if (F32) pack_frag_lo<V>(H, A, Al);
+#pragma unroll 1
+    for (int s = 0; s < Lc; ++s) {
+      if (s % S2 == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          ptx::sts_f32x4(slot_f(sb + L.subck, s / S2, nt), H[nt][0], H[nt][1], H[nt][2], H[nt][3]);
+      }
+      float k0, k1, Zd[NT][4];
+      float2 vv[NT];
+      k_rows(s, k0, k1);
+      v_pairs(s, vv);
+      recompute_step<V, F32>(H, A, Al, Bw, Bwl, k0, k1, vv, ptx::lds_f32(sb + L.in_f + 4 * s), Zd);
+    }
+
+    // ---- 3. sub-intervals, last first ----
+    const int nsub = (Lc + S2 - 1) / S2;
+#pragma unroll 1
+    for (int j = nsub - 1; j >= 0; --j) {
+      const int s0 = j * S2;
+      const int Ls = min(S2, Lc - s0);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float4 x = ptx::lds_f32x4(slot_f(sb + L.subck, j, nt));
+        H[nt][0] = x.x;
+        H[nt][1] = x.y;
+        H[nt][2] = x.z;
+        H[nt][3] = x.w;
+      }
+      pack_frag<V>(H, A);
+      if (F32) pack_frag_lo<V>(H, A, Al);
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) sts_u32x4(slot_h(0, ks), A[ks][0], A[ks][1], A[ks][2], A[ks][3]);
+#pragma unroll 1
+      for (int i = 0; i < Ls; ++i) {
+        float k0, k1, Zd[NT][4];
+        float2 vv[NT];
+        k_rows(s0 + i, k0, k1);
+        v_pairs(s0 + i, vv);
+        recompute_step<V, F32>(H, A, Al, Bw, Bwl, k0, k1, vv,
+                               ptx::lds_f32(sb + L.in_f + 4 * (s0 + i)), Zd);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          ptx::sts_f32x4(slot_f(sb + L.zs, i, nt), Zd[nt][0], Zd[nt][1], Zd[nt][2], Zd[nt][3]);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+          sts_u32x4(slot_h(i + 1, ks), A[ks][0], A[ks][1], A[ks][2], A[ks][3]);
+      }
+      // reverse steps
+#pragma unroll 1
+      for (int i = Ls - 1; i >= 0; --i) {
+        const int s = s0 + i;
+        uint32_t Hp[KS][4], Hc[KS][4];
+        float Z[NT][4];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint4 a = ptx::lds_u32x4(slot_h(i, ks));
+          const uint4 d = ptx::lds_u32x4(slot_h(i + 1, ks));
+          Hp[ks][0] = a.x; Hp[ks][1] = a.y; Hp[ks][2] = a.z; Hp[ks][3] = a.w;
+          Hc[ks][0] = d.x; Hc[ks][1] = d.y; Hc[ks][2] = d.z; Hc[ks][3] = d.w;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float4 x = ptx::lds_f32x4(slot_f(sb + L.zs, i, nt));
+          Z[nt][0] = x.x;
+          Z[nt][1] = x.y;
+          Z[nt][2] = x.z;
+          Z[nt][3] = x.w;
+        }
+        const uint32_t qrow = sb + L.in_q + static_cast<uint32_t>(s * RS * es) + kq_row;
+        const uint32_t krow = sb + L.in_k + static_cast<uint32_t>(s * RS * es) + kq_row;
+        const float qa = one_f32<F32>(qrow + g * es), qb = one_f32<F32>(qrow + (g + 8) * es);
+        const float fg = ptx::lds_f32(sb + L.in_f + 4 * s);
+        const float omf = 1.f - fg;
+        float2 u[NT];
+        uint32_t ub[KS][2], vb[KS][2], kb[2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          u[nt] = pair_f32<F32>(sb + L.in_dy + static_cast<uint32_t>((s * V + 8 * nt + 2 * c) * es));
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t off = static_cast<uint32_t>((s * V + 16 * ks + 8 * h + 2 * c) * es);
+            ub[ks][h] = pair_bf16<F32>(sb + L.in_dy + off);
+            vb[ks][h] = pair_bf16<F32>(sb + L.in_v + off);
+          }
+        kb[0] = pair_bf16<F32>(krow + 2 * c * es);
+        kb[1] = pair_bf16<F32>(krow + (8 + 2 * c) * es);
+
+        // R = C + q u^T;  D = (1 - f) R (.) (1 - Z^2);  df partial = <R, H_{t-1} - Z>
+        float R[NT][4], D[NT][4];
+        float dfp = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int ks = nt >> 1, hh = 2 * (nt & 1);
+          const float hp[4] = {ptx::bf16x2_lo(Hp[ks][hh]), ptx::bf16x2_hi(Hp[ks][hh]),
+                               ptx::bf16x2_lo(Hp[ks][hh + 1]), ptx::bf16x2_hi(Hp[ks][hh + 1])};
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const float qr = (r < 2) ? qa : qb;
+            const float ur = (r & 1) ? u[nt].y : u[nt].x;
+            R[nt][r] = fmaf(qr, ur, Cg[nt][r]);
+            const float z = Z[nt][r];
+            D[nt][r] = omf * R[nt][r] * fmaf(-z, z, 1.f);
+            dfp = fmaf(R[nt][r], hp[r] - z, dfp);
+          }
+        }
+        uint32_t Dh[KS][4], Dl[KS][4];
+        pack_frag<V>(D, Dh);
+        pack_frag_lo<V>(D, Dh, Dl);
+        // C_{t-1} = f R + D W^T   (D as hi + lo bf16 parts)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) Cg[nt][r] = fg * R[nt][r];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            ptx::mma_bf16_16816(Cg[nt], Dh[ks], Bt[ks][nt][0], Bt[ks][nt][1]);
+            ptx::mma_bf16_16816(Cg[nt], Dl[ks], Bt[ks][nt][0], Bt[ks][nt][1]);
+            if (F32) ptx::mma_bf16_16816(Cg[nt], Dh[ks], Btl[ks][nt][0], Btl[ks][nt][1]);
+          }
+        // dk rows = D v;  dq rows = H_t u  (columns of B all equal)
+        float dk4[4], dq4[4];
+        ptx::mma_bf16_16816_zero(dk4, Dh[0], vb[0][0], vb[0][1]);
+        ptx::mma_bf16_16816_zero(dq4, Hc[0], ub[0][0], ub[0][1]);
+#pragma unroll
+        for (int ks = 1; ks < KS; ++ks) {
+          ptx::mma_bf16_16816(dk4, Dh[ks], vb[ks][0], vb[ks][1]);
+          ptx::mma_bf16_16816(dq4, Hc[ks], ub[ks][0], ub[ks][1]);
+        }
+        // transposed fragments of D and H_{t-1}
+        uint32_t DT[KS][4], HT[KS][4];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            DT[ks][e] = ptx::movmatrix_trans(Dh[ks][e]);
+            HT[ks][e] = ptx::movmatrix_trans(Hp[ks][e]);
+          }
+        // dW += H_{t-1}^T D: m-tile over l (= k-step ml of H), n-tile over j
+#pragma unroll
+        for (int ml = 0; ml < KS; ++ml) {
+          const uint32_t Aa[4] = {HT[ml][0], HT[ml][2], HT[ml][1], HT[ml][3]};
+#pragma unroll
+          for (int nj = 0; nj < NT; ++nj)
+            ptx::mma_bf16_16816(dW[ml][nj], Aa, DT[nj >> 1][2 * (nj & 1)], DT[nj >> 1][2 * (nj & 1) + 1]);
+        }
+        // dv (this warp's rows) = D^T k: m-tile over j
+        float dv4[KS][4];
+#pragma unroll
+        for (int mj = 0; mj < KS; ++mj) {
+          const uint32_t Aa[4] = {DT[mj][0], DT[mj][2], DT[mj][1], DT[mj][3]};
+          ptx::mma_bf16_16816_zero(dv4[mj], Aa, kb[0], kb[1]);
+        }
+        // warp sum of the df partial
+        dfp += __shfl_xor_sync(0xffffffffu, dfp, 1);
+        dfp += __shfl_xor_sync(0xffffffffu, dfp, 2);
+        dfp += __shfl_xor_sync(0xffffffffu, dfp, 4);
+        dfp += __shfl_xor_sync(0xffffffffu, dfp, 8);
+        dfp += __shfl_xor_sync(0xffffffffu, dfp, 16);
+        if (c == 0) {
+          const uint32_t rq = sb + L.r_dq + static_cast<uint32_t>((i * RS + 16 * warp + g) * 4);
+          const uint32_t rk = sb + L.r_dk + static_cast<uint32_t>((i * RS + 16 * warp + g) * 4);
+          ptx::sts_f32(rq, dq4[0]);
+          ptx::sts_f32(rq + 32, dq4[2]);
+          ptx::sts_f32(rk, dk4[0]);
+          ptx::sts_f32(rk + 32, dk4[2]);
+#pragma unroll
+          for (int mj = 0; mj < KS; ++mj) {
+            const uint32_t rv = sb + L.r_dv + static_cast<uint32_t>(((i * WPC + warp) * V + 16 * mj + g) * 4);
+            ptx::sts_f32(rv, dv4[mj][0]);
+            ptx::sts_f32(rv + 32, dv4[mj][2]);
+          }
+        }
+        if (lane == 0) ptx::sts_f32(sb + L.r_df + static_cast<uint32_t>((i * WPC + warp) * 4), dfp);
+      }
+      __syncthreads();
+      // ---- flush the sub-interval's per-step results ----
+      {
+        const size_t bt = static_cast<size_t>(b) * T + t0 + s0;
+        const int r4 = RS / 4;
+        for (int e = tid; e < Ls * r4; e += nthr) {
+          const int i = e / r4, x = e - i * r4;
+          const float4 a = ptx::lds_f32x4(sb + L.r_dq + static_cast<uint32_t>((i * RS + 4 * x) * 4));
+          const float4 d = ptx::lds_f32x4(sb + L.r_dk + static_cast<uint32_t>((i * RS + 4 * x) * 4));
+          red_add_v4(p.dq + (bt + i) * K + row0c + 4 * x, a.x, a.y, a.z, a.w);
+          red_add_v4(p.dk + (bt + i) * K + row0c + 4 * x, d.x, d.y, d.z, d.w);
+        }
+        for (int e = tid; e < Ls * V; e += nthr) {
+          const int i = e / V, jj = e - i * V;
+          float acc = 0.f;
+          for (int w = 0; w < WPC; ++w)
+            acc += ptx::lds_f32(sb + L.r_dv + static_cast<uint32_t>(((i * WPC + w) * V + jj) * 4));
+          const int s = s0 + i;
+          const float uu = one_f32<F32>(sb + L.in_dy + static_cast<uint32_t>((s * V + jj) * es));
+          const float vv = one_f32<F32>(sb + L.in_v + static_cast<uint32_t>((s * V + jj) * es));
+          float* dst = p.dv + ((bt + i) * N + n) * V + jj;
+          if (p.nslices == 1) {
+            *dst = fmaf(tof(wr[jj]), uu, acc);
+          } else {
+            red_add(dst, slice == 0 ? fmaf(tof(wr[jj]), uu, acc) : acc);
+          }
+          if (slice == 0) dwr_acc = fmaf(uu, vv, dwr_acc);  // thread e % V == jj throughout
+        }
+        for (int i = tid; i < Ls; i += nthr) {
+          float acc = 0.f;
+          for (int w = 0; w < WPC; ++w)
+            acc += ptx::lds_f32(sb + L.r_df + static_cast<uint32_t>((i * WPC + w) * 4));
+          float* dst = p.df + (bt + i) * N + n;
+          if (p.nslices == 1)
+            *dst = acc;
+          else
+            red_add(dst, acc);
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // ---- end: dH0, dW, dw_r ----
+  if (p.dH0 != nullptr) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        *reinterpret_cast<float2*>(p.dH0 + sidx + (row0 + g + 8 * h) * V + 8 * nt + 2 * c) =
+            make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
+  }
+  // dW: this warp's [V][V] sum -> shared memory (reusing the Z slots) -> CTA sum -> global
+  __syncthreads();
+  {
+    const uint32_t base = sb + L.zs + static_cast<uint32_t>(warp * V * V * 4);
+#pragma unroll
+    for (int ml = 0; ml < KS; ++ml)
+#pragma unroll
+      for (int nj = 0; nj < NT; ++nj)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int l = 16 * ml + g + 8 * (r >> 1), jj = 8 * nj + 2 * c + (r & 1);
+          ptx::sts_f32(base + static_cast<uint32_t>((l * V + jj) * 4), dW[ml][nj][r]);
+        }
+  }
+  __syncthreads();
+  for (int e = tid; e < V * V; e += nthr) {
+    float acc = 0.f;
+    for (int w = 0; w < WPC; ++w)
+      acc += ptx::lds_f32(sb + L.zs + static_cast<uint32_t>((w * V * V + e) * 4));
+    red_add(p.dW + static_cast<size_t>(n) * V * V + e, acc);
+  }
+  // each thread holds the u (.) v sum of column tid % V over the steps it flushed
+  if (slice == 0) red_add(p.dw_r + static_cast<size_t>(n) * V + tid % V, dwr_acc);
+}
+
+template <int V, bool F32>
+cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
+  const BwdLayout L = bwd_layout(V, p.C, p.S2, p.WPC, F32 ? 4 : 2);
+  auto kern = bwd_kernel<V, F32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(L.total));
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(p.B) * p.N * p.nslices;
+  kern<<<grid, 32 * p.WPC, L.total, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int V, bool F32>
+int bwd_ctas_per_sm_t(const BwdParams& p) {
+  const BwdLayout L = bwd_layout(V, p.C, p.S2, p.WPC, F32 ? 4 : 2);
+  auto kern = bwd_kernel<V, F32>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(L.total)) != cudaSuccess)
+    return 0;
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, 32 * p.WPC, L.total) != cudaSuccess)
+    return 0;
+  return nb;
+}
+
+}  // namespace
+
+size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs) {
+  return bwd_layout(V, C, S2, WPC, f32_inputs ? 4 : 2).total;
+}
+
+int bwd_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs) {
+  if (V == 16) return f32_inputs ? bwd_ctas_per_sm_t<16, true>(p) : bwd_ctas_per_sm_t<16, false>(p);
+  return f32_inputs ? bwd_ctas_per_sm_t<32, true>(p) : bwd_ctas_per_sm_t<32, false>(p);
+}
+
+cudaError_t launch_bwd(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream) {
+  if (p.WPC < 1 || p.WPC > 8 || p.S2 < 1) return cudaErrorInvalidValue;
+  if (V == 16) return f32_inputs ? launch_bwd_t<16, true>(p, stream) : launch_bwd_t<16, false>(p, stream);
+  if (V == 32) return f32_inputs ? launch_bwd_t<32, true>(p, stream) : launch_bwd_t<32, false>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace m2rnn

@@ -309,7 +309,8 @@ __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout
     const uint32_t vs = sbase + static_cast<uint32_t>(s) * L.stage + L.v;
     const uint32_t yp = sbase + L.yp_base + static_cast<uint32_t>(ys) * L.yp_stage;
     TIn* y = static_cast<TIn*>(p.y) + ((static_cast<size_t>(b) * T + t0) * N + n0) * V;
-    for (int idx = lane; idx < Tc * R8; idx += 32) {
+    const int nidx = p.y != nullptr ? Tc * R8 : 0;  // no y in checkpoint-only runs
+    for (int idx = lane; idx < nidx; idx += 32) {
       const int tl = idx / R8;
       const int r = (idx - tl * R8) * 8;
       const int hl = r / V, j = r - hl * V;

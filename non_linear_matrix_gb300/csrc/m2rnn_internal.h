@@ -14,9 +14,6 @@ enum WaitSite : int {
   SITE_FWD_EPILOGUE = 2,
   SITE_FWD_CONSUMER = 3,
   SITE_FWD_DRAIN = 4,
-  SITE_BWD_PRODUCER = 11,
-  SITE_BWD_CONSUMER = 12,
-  SITE_BWD_DRAIN = 13,
 };
 
 constexpr int kStatusTimeout = -7;  // == M2RNN_ERR_TIMEOUT
@@ -29,7 +26,7 @@ struct FwdParams {
   const void* W;
   const void* w_r;
   const float* H0;  // nullable
-  void* y;
+  void* y;      // nullable inside the library (checkpoint-only runs)
   float* HT;    // nullable
   float* ckpt;  // nullable
   int B, T, N, K;
@@ -43,6 +40,35 @@ struct FwdParams {
   unsigned long long wait_limit_ns;
   int inject_stall;  // test hook: 1 = the producer issues nothing
 };
+
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* f;
+  const void* W;
+  const void* w_r;
+  const float* ckpt;  // [B,N,nck,K,V]
+  const void* dy;
+  const float* dHT;   // nullable
+  float* dq;          // accumulated with reductions: zeroed by the caller
+  float* dk;          //   "
+  float* dv;          // stored (nslices == 1) or accumulated (zeroed)
+  float* df;          //   "
+  float* dW;          // accumulated (zeroed)
+  float* dw_r;        // accumulated (zeroed)
+  float* dH0;         // nullable
+  int B, T, N, K;
+  int C;        // checkpoint interval
+  int nck;      // checkpoints per (b, n)
+  int WPC;      // warps per CTA (16 rows each)
+  int nslices;  // K / (16 * WPC)
+  int S2;       // sub-interval length of the recomputation
+};
+
+cudaError_t launch_bwd(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream);
+int bwd_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs);
+size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs);
 
 // Launches the forward kernel variant for (V, input dtype, MT m-tiles/warp).
 cudaError_t launch_fwd(const FwdParams& p, int V, bool f32_inputs, int MT, cudaStream_t stream);

@@ -1,0 +1,122 @@
+"""Backward parity: libm2rnn's BPTT gradients (through the C ABI) against the
+fp64 oracle on the same seeded inputs.
+
+Tolerance: relative L2 error <= 1e-2 per gradient tensor (dq, dk, dv, df,
+dW, dw_r, dH0).  The GPU differentiates its own (bf16-operand) trajectory,
+the oracle the fp64 one.
+"""
+import numpy as np
+import pytest
+import torch
+
+from non_linear_matrix_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+NAMES = ("dq", "dk", "dv", "df", "dW", "dw_r")
+
+
+@pytest.fixture(scope="module")
+def m2rnn():
+    import __graft_entry__
+    __graft_entry__.build()
+    from non_linear_matrix_gb300 import m2rnn as m
+    return m
+
+
+def _dev(x):
+    return {n: t.cuda() for n, t in x.items()}
+
+
+def _rel(a, r):
+    a = a.detach().cpu().double().numpy() if hasattr(a, "detach") else a
+    den = np.linalg.norm(r)
+    return np.linalg.norm(a - r) / den if den > 0 else np.linalg.norm(a)
+
+
+def _check_status(m2rnn):
+    st, de = m2rnn.device_status(clear=True)
+    assert st == 0, (st, de)
+
+
+def _run(m2rnn, x, C, H0=None, dHT=None, give_ckpt=True):
+    g = _dev(x)
+    H0g = None if H0 is None else H0.cuda()
+    dHTg = None if dHT is None else dHT.cuda()
+    ck = None
+    if give_ckpt:
+        _, _, ck = m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], H0g, ckpt_every=C)
+    gr = m2rnn.bwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], g["dy"], H0=H0g, ckpt=ck,
+                   dHT=dHTg, ckpt_every=C, want_dH0=True)
+    torch.cuda.synchronize()
+    _check_status(m2rnn)
+    return gr
+
+
+def _compare(m2rnn, oracle_mod, x, C, H0=None, dHT=None, give_ckpt=True, label=""):
+    gr = _run(m2rnn, x, C, H0, dHT, give_ckpt)
+    ref = oracle_mod.bwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], x["dy"], H0=H0,
+                         dHT=dHT)
+    errs = {n: _rel(gr[n], ref[n]) for n in NAMES + ("dH0",)}
+    assert max(errs.values()) <= TOL, (label, errs)
+    return errs
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("K,V", [(16, 16), (64, 16), (128, 16), (64, 32)])
+@pytest.mark.parametrize("T,C", [(1, 4), (7, 4), (50, 16), (130, 64)])
+def test_shapes(m2rnn, oracle_mod, dtype, K, V, T, C):
+    """Every K/V, both dtypes, ragged intervals and sub-intervals, H0 and
+    dH_T given."""
+    B, N = 2, 3
+    x = make_inputs(B, T, N, K, V, dtype, 2000 + K + V + T, with_dy=True)
+    gen = torch.Generator().manual_seed(T + K)
+    H0 = torch.rand(B, N, K, V, generator=gen) - 0.5
+    dHT = torch.randn(B, N, K, V, generator=gen)
+    _compare(m2rnn, oracle_mod, x, C, H0=H0, dHT=dHT, label=f"{dtype} K{K} V{V} T{T} C{C}")
+
+
+@pytest.mark.parametrize("C", [8, 64, 200])
+def test_checkpoints_recomputed(m2rnn, oracle_mod, C):
+    """ckpt = NULL: the library recomputes checkpoints into the workspace;
+    C = 200 exceeds the longest interval the kernel takes and is
+    re-checkpointed internally."""
+    x = make_inputs(3, 300, 4, 64, 16, "bf16", 77, with_dy=True)
+    _compare(m2rnn, oracle_mod, x, C, give_ckpt=False, label=f"recompute C{C}")
+    if C > 128:
+        _compare(m2rnn, oracle_mod, x, C, give_ckpt=True, label=f"given C{C}")
+
+
+def test_f_one_exact(m2rnn):
+    """f = 1: H stays 0 and the candidate path is closed, so dW, dk, dq are
+    exactly 0 and dv = w_r (.) dy (up to the fp32 product)."""
+    x = make_inputs(2, 40, 3, 64, 16, "bf16", 5, with_dy=True)
+    x["f"] = torch.ones_like(x["f"])
+    gr = _run(m2rnn, x, 16)
+    assert torch.count_nonzero(gr["dW"]) == 0
+    assert torch.count_nonzero(gr["dk"]) == 0
+    assert torch.count_nonzero(gr["dq"]) == 0
+    expect = x["w_r"].float()[None, None] * x["dy"].float()
+    assert torch.allclose(gr["dv"].cpu(), expect, rtol=1e-6, atol=0)
+
+
+def test_zero_steps(m2rnn):
+    x = _dev(make_inputs(2, 0, 3, 64, 16, "bf16", 0, with_dy=True))
+    dHT = torch.randn(2, 3, 64, 16, device="cuda")
+    gr = m2rnn.bwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], x["dy"], dHT=dHT,
+                   ckpt_every=8, want_dH0=True)
+    torch.cuda.synchronize()
+    assert torch.equal(gr["dH0"], dHT)
+    assert torch.count_nonzero(gr["dW"]) == 0 and torch.count_nonzero(gr["dw_r"]) == 0
+
+
+def test_workload_fwd_bwd(m2rnn, oracle_mod):
+    """B=8, T=4096, N=32 with checkpoints every 64 steps (the fwd+bwd
+    workload), every gradient compared with the oracle at full size."""
+    w = WORKLOADS["fwdbwd_bf16_b8_t4096_n32"]
+    x = workload_inputs(w)
+    gr = _run(m2rnn, x, w.ckpt_every)
+    ref = oracle_mod.bwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], x["dy"])
+    errs = {n: _rel(gr[n], ref[n]) for n in NAMES + ("dH0",)}
+    assert max(errs.values()) <= TOL, errs
