@@ -118,13 +118,16 @@ size_t m2rnn_bwd_workspace_size(const m2rnn_shape *s, int ckpt_given);
  *   dy   : upstream gradient of y (required); dH_T may be NULL (= 0).
  *   dq, dk, dv, df, dW, dw_r : gradient outputs (required, float32).
  *   dH0  : gradient of H0, or NULL.
+ *   dckpt: gradient of every checkpoint state, dL/dH_{c*ckpt_every}, laid
+ *          out like ckpt ([B,N,nck,K,V] float32; dckpt[..][0] = dH0), or
+ *          NULL.  It lets a caller split a sequence at checkpoints.
  *   workspace, ws_bytes : at least m2rnn_bwd_workspace_size(s, ckpt != NULL)
  *          bytes of device memory; its contents on entry are ignored. */
 int m2rnn_bwd(const m2rnn_shape *s, const void *q, const void *k, const void *v,
               const void *f, const void *W, const void *w_r, const float *H0,
               const float *ckpt, const void *dy, const float *dH_T,
               float *dq, float *dk, float *dv, float *df, float *dW, float *dw_r,
-              float *dH0, void *workspace, size_t ws_bytes, void *stream);
+              float *dH0, float *dckpt, void *workspace, size_t ws_bytes, void *stream);
 
 /* Reads (after synchronising `stream`) and optionally clears the device
  * status word of the current device.  *status receives M2RNN_OK or the code

@@ -254,15 +254,19 @@ int run_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, c
 // Longest checkpoint interval the backward kernel takes directly; longer ones
 // are re-checkpointed into the workspace at kBwdDefaultC.
 constexpr int kBwdMaxC = 128;
-constexpr int kBwdDefaultC = 64;
 
 // Interval the backward kernel works with, and whether it needs its own
-// checkpoints (in the workspace).
+// checkpoints (in the workspace).  Longer intervals are cut into the largest
+// divisor of the interval that the kernel takes, so every caller checkpoint
+// stays an interval boundary.
 int bwd_interval(const m2rnn_shape* s, bool ckpt_given, bool* own_ckpt) {
   const int C = s->ckpt_every;
   const bool direct = ckpt_given && C <= kBwdMaxC;
   *own_ckpt = !direct;
-  return direct ? C : (C <= kBwdMaxC ? C : kBwdDefaultC);
+  if (C <= kBwdMaxC) return C;
+  for (int d = kBwdMaxC; d > 1; --d)
+    if (C % d == 0) return d;
+  return 1;
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -384,7 +388,7 @@ size_t m2rnn_bwd_workspace_size(const m2rnn_shape* s, int ckpt_given) {
 int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
               const void* W, const void* w_r, const float* H0, const float* ckpt, const void* dy,
               const float* dH_T, float* dq, float* dk, float* dv, float* df, float* dW, float* dw_r,
-              float* dH0, void* workspace, size_t ws_bytes, void* stream) {
+              float* dH0, float* dckpt, void* workspace, size_t ws_bytes, void* stream) {
   int rc = check_shape(s);
   if (rc != M2RNN_OK) return rc;
   if (s->ckpt_every <= 0) return M2RNN_ERR_INVALID_ARG;
@@ -395,7 +399,7 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   const void* always[] = {W, w_r, dW, dw_r};
   for (const void* x : always)
     if ((rc = check_ptr(x, dev, true)) != M2RNN_OK) return rc;
-  const void* optional[] = {H0, dH_T, dH0};
+  const void* optional[] = {H0, dH_T, dH0, dckpt};
   for (const void* x : optional)
     if ((rc = check_ptr(x, dev, false)) != M2RNN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -448,6 +452,9 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   p.dW = dW;
   p.dw_r = dw_r;
   p.dH0 = dH0;
+  p.dckpt = dckpt;
+  p.dck_ratio = s->ckpt_every / C;
+  p.dck_n = static_cast<int>(m2rnn_num_checkpoints(s));
   p.B = s->B;
   p.T = s->T;
   p.N = s->N;

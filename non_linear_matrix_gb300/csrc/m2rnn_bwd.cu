@@ -60,7 +60,7 @@ struct BwdLayout {
   uint32_t in_q, in_k, in_v, in_dy, in_f;  // interval inputs
   uint32_t subck;                          // [NS1][WPC][NT][32][4] fp32
   uint32_t hs;                             // [S2+1][WPC][KS][32][4] u32 (bf16 frags)
-  uint32_t zs;                             // [S2][WPC][NT][32][4] fp32
+  uint32_t zs;                             // [S2][WPC][NT][32][4] fp32; dW sums at the end
   uint32_t r_dq, r_dk;                     // [S2][RS] fp32
   uint32_t r_dv;                           // [S2][WPC][V] fp32
   uint32_t r_df;                           // [S2][WPC] fp32
@@ -87,8 +87,9 @@ __host__ __device__ inline BwdLayout bwd_layout(int V, int C, int S2, int WPC, i
   o = al(o + NS1 * WPC * NT * 512);
   L.hs = o;
   o = al(o + (S2 + 1) * WPC * KS * 512);
-  L.zs = o;
-  o = al(o + S2 * WPC * NT * 512);
+  L.zs = o;  // also holds the per-warp dW sums ([WPC][V][V] fp32) at the end
+  const int zs_bytes = S2 * WPC * NT * 512, dw_bytes = WPC * V * V * 4;
+  o = al(o + (zs_bytes > dw_bytes ? zs_bytes : dw_bytes));
   L.r_dq = o;
   o = al(o + S2 * RS * 4);
   L.r_dk = o;
@@ -563,6 +564,16 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
         }
       }
       __syncthreads();
+    }
+    // C now holds dL/dH_{t0}: the gradient of this interval's checkpoint.
+    if (p.dckpt != nullptr && ci % p.dck_ratio == 0) {
+      float* dst = p.dckpt + ((static_cast<size_t>(b) * N + n) * p.dck_n + ci / p.dck_ratio) * K * V;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          *reinterpret_cast<float2*>(dst + (row0 + g + 8 * h) * V + 8 * nt + 2 * c) =
+              make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
     }
   }
 

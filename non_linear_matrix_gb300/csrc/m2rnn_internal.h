@@ -58,6 +58,9 @@ struct BwdParams {
   float* dW;          // accumulated (zeroed)
   float* dw_r;        // accumulated (zeroed)
   float* dH0;         // nullable
+  float* dckpt;       // nullable: dL/dH at every dck_ratio-th interval start
+  int dck_ratio;      // user checkpoint interval / C
+  int dck_n;          // user checkpoints per (b, n)
   int B, T, N, K;
   int C;        // checkpoint interval
   int nck;      // checkpoints per (b, n)

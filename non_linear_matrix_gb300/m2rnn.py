@@ -34,7 +34,7 @@ _EXPORTS = {
     "m2rnn_num_checkpoints": (ctypes.c_size_t, [_VP]),
     "m2rnn_fwd": (ctypes.c_int, [_VP] * 12),
     "m2rnn_bwd_workspace_size": (ctypes.c_size_t, [_VP, ctypes.c_int]),
-    "m2rnn_bwd": (ctypes.c_int, [_VP] * 19 + [ctypes.c_size_t, _VP]),
+    "m2rnn_bwd": (ctypes.c_int, [_VP] * 20 + [ctypes.c_size_t, _VP]),
     "m2rnn_device_status": (ctypes.c_int, [_VP, _VP, ctypes.c_int, _VP]),
     "m2rnn_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_longlong]),
     "m2rnn_set_fault_injection": (ctypes.c_int, [ctypes.c_int]),
@@ -146,8 +146,11 @@ def bwd_workspace_size(shape: Shape, ckpt_given: bool) -> int:
 
 
 def bwd(q, k, v, f, W, w_r, dy, H0=None, ckpt=None, dHT=None, *, ckpt_every: int = 64,
-        want_dH0: bool = False, workspace=None, out=None, stream=None):
-    """BPTT backward.  Returns dict(dq, dk, dv, df, dW, dw_r[, dH0]) (fp32)."""
+        want_dH0: bool = False, want_dckpt: bool = False, workspace=None, out=None,
+        stream=None):
+    """BPTT backward.  Returns dict(dq, dk, dv, df, dW, dw_r[, dH0][, dckpt]) (fp32).
+
+    ``dckpt`` is dL/dH at every checkpoint ([B,N,nck,K,V])."""
     s = make_shape(q, v, ckpt_every)
     dev = q.device
     f32 = dict(device=dev, dtype=torch.float32)
@@ -164,17 +167,22 @@ def bwd(q, k, v, f, W, w_r, dy, H0=None, ckpt=None, dHT=None, *, ckpt_every: int
     dH0 = out.get("dH0")
     if dH0 is None and want_dH0:
         dH0 = torch.empty(s.B, s.N, s.K, s.V, **f32)
+    dck = out.get("dckpt")
+    if dck is None and want_dckpt:
+        dck = torch.empty(s.B, s.N, num_checkpoints(s), s.K, s.V, **f32)
     need = bwd_workspace_size(s, ckpt is not None)
     if workspace is None:
         workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
     rc = lib().m2rnn_bwd(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W), _ptr(w_r),
                          _ptr(H0), _ptr(ckpt), _ptr(dy), _ptr(dHT),
                          _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["df"]),
-                         _ptr(g["dW"]), _ptr(g["dw_r"]), _ptr(dH0), _ptr(workspace),
+                         _ptr(g["dW"]), _ptr(g["dw_r"]), _ptr(dH0), _ptr(dck), _ptr(workspace),
                          ctypes.c_size_t(workspace.numel()), _stream(stream))
     _check(rc, "m2rnn_bwd")
     if dH0 is not None:
         g["dH0"] = dH0
+    if dck is not None:
+        g["dckpt"] = dck
     return g
 
 

@@ -79,6 +79,6 @@ def test_bwd_rejects_bad_shapes_before_launch(lib):
     from non_linear_matrix_gb300.m2rnn import Shape
     p = ctypes.c_void_p(16)
     s = ctypes.byref(Shape(1, 8, 2, 48, 16, 1, 4))
-    rc = lib.m2rnn_bwd(s, *([p] * 6), None, None, p, None, *([p] * 6), None, p,
+    rc = lib.m2rnn_bwd(s, *([p] * 6), None, None, p, None, *([p] * 6), None, None, p,
                        ctypes.c_size_t(1 << 20), None)
     assert rc in (-1, -2)
