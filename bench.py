@@ -50,7 +50,7 @@ DEFAULT_WORKLOAD = "fwd_bf16_b64_t4096_n32"
 # bf16x2 and f16x2 alike) and the dependent latency of one recurrence step of
 # a 16x16 state tile (mma -> tanh -> blend -> bf16 repack) on one warp.
 SFU_TANH_PER_CLK_PER_SM = 16.0
-STEP_LATENCY_CLK = 82.5
+STEP_LATENCY_CLK = 113.3
 NUM_SMS = 152
 SM_MAX_MHZ = 2070.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
