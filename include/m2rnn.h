@@ -142,6 +142,40 @@ int m2rnn_device_status(int *status, int *detail, int clear, void *stream);
  * with a wait that cannot complete in time.  Returns M2RNN_OK. */
 int m2rnn_set_wait_limit_ns(long long limit_ns);
 
+/* Size of the checkpoint buffer built into the library for
+ * m2rnn_bwd_noalloc (bytes, per GPU). */
+#define M2RNN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* Backward pass for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that must not call cudaMalloc (or any allocating routine) at the point
+ * where they run the backward pass -- for example code running while a
+ * memory pool is frozen or exhausted, code inside a framework whose
+ * allocator must not be re-entered, or a runtime that only hands out
+ * pre-registered buffers.  It computes the same gradients as m2rnn_bwd
+ * with ckpt = NULL and dckpt = NULL, but recomputes the checkpoints into a
+ * buffer compiled into the library instead of a caller workspace, and
+ * allocates nothing.  The caller still passes every input and output.
+ *
+ *   - The buffer holds M2RNN_NOALLOC_SCRATCH_BYTES (64 MiB); problems whose
+ *     checkpoints need more (m2rnn_bwd_workspace_size(s, 0) bytes) are
+ *     refused with M2RNN_ERR_WORKSPACE before any device work.
+ *   - Every GPU that loads this part of the library holds the buffer until
+ *     the process exits.
+ *   - The first call on a device looks up the buffer's device address on
+ *     that device (which must be current); make that first call before any
+ *     stream capture.
+ *   - All calls share the buffer and it keeps the last call's contents;
+ *     nothing in it needs to start at zero (the forward recomputation writes
+ *     every checkpoint the backward reads).  Calls that overlap on the GPU
+ *     (different streams, or threads sharing a device) race on it: the
+ *     caller must serialise them. */
+int m2rnn_bwd_noalloc(const m2rnn_shape *s, const void *q, const void *k, const void *v,
+                      const void *f, const void *W, const void *w_r, const float *H0,
+                      const void *dy, const float *dH_T, float *dq, float *dk, float *dv,
+                      float *df, float *dW, float *dw_r, float *dH0, void *stream);
+
 /* Test hook for the time-out path.  mode 1: kernels launched afterwards
  * from this process start no input transfers, so every internal wait runs
  * into the wait limit, the kernel stops early (outputs unspecified) and

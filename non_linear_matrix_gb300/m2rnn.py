@@ -38,6 +38,7 @@ _EXPORTS = {
     "m2rnn_device_status": (ctypes.c_int, [_VP, _VP, ctypes.c_int, _VP]),
     "m2rnn_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_longlong]),
     "m2rnn_set_fault_injection": (ctypes.c_int, [ctypes.c_int]),
+    "m2rnn_bwd_noalloc": (ctypes.c_int, [_VP] * 18),
 }
 
 
@@ -183,6 +184,32 @@ def bwd(q, k, v, f, W, w_r, dy, H0=None, ckpt=None, dHT=None, *, ckpt_every: int
         g["dH0"] = dH0
     if dck is not None:
         g["dckpt"] = dck
+    return g
+
+
+def bwd_noalloc(q, k, v, f, W, w_r, dy, H0=None, dHT=None, *, ckpt_every: int = 64,
+                want_dH0: bool = False, out=None, stream=None):
+    """Backward pass that allocates nothing inside the library (checkpoints
+    are recomputed into a buffer built into it).  Same outputs as
+    ``bwd(..., ckpt=None)``; output tensors come from ``out`` or are created
+    here by the caller side."""
+    s = make_shape(q, v, ckpt_every)
+    f32 = dict(device=q.device, dtype=torch.float32)
+    out = dict(out or {})
+    shapes = {"dq": (s.B, s.T, s.K), "dk": (s.B, s.T, s.K), "dv": (s.B, s.T, s.N, s.V),
+              "df": (s.B, s.T, s.N), "dW": (s.N, s.V, s.V), "dw_r": (s.N, s.V)}
+    g = {n: out.get(n) if out.get(n) is not None else torch.empty(shp, **f32)
+         for n, shp in shapes.items()}
+    dH0 = out.get("dH0")
+    if dH0 is None and want_dH0:
+        dH0 = torch.empty(s.B, s.N, s.K, s.V, **f32)
+    rc = lib().m2rnn_bwd_noalloc(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W),
+                                 _ptr(w_r), _ptr(H0), _ptr(dy), _ptr(dHT), _ptr(g["dq"]),
+                                 _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["df"]), _ptr(g["dW"]),
+                                 _ptr(g["dw_r"]), _ptr(dH0), _stream(stream))
+    _check(rc, "m2rnn_bwd_noalloc")
+    if dH0 is not None:
+        g["dH0"] = dH0
     return g
 
 
