@@ -178,17 +178,24 @@ def _oracle_rate(w, budget_s: float, seed_offset: int = 0):
     oracle.build()
     threads = oracle.threads()
     heads = max(1, min(w.N, threads))
+
+    def run(T_):
+        x = make_inputs(1, T_, heads, w.K, w.V, w.dtype, w.seed + seed_offset, w.f_mean,
+                        with_dy=w.backward)
+        t0 = time.perf_counter()
+        if w.backward:  # forward + BPTT backward (the oracle's backward reruns the forward)
+            oracle.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"])
+            oracle.bwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], x["dy"])
+        else:
+            oracle.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"])
+        return time.perf_counter() - t0
+
     T_probe = min(w.T, 256)
-    x = make_inputs(1, T_probe, heads, w.K, w.V, w.dtype, w.seed + seed_offset, w.f_mean)
-    t0 = time.perf_counter()
-    oracle.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"])
-    rate = heads * T_probe / max(time.perf_counter() - t0, 1e-6)
+    rate = heads * T_probe / max(run(T_probe), 1e-6)
     T_s = int(max(16, min(w.T, budget_s * rate / heads)))
-    x = make_inputs(1, T_s, heads, w.K, w.V, w.dtype, w.seed + seed_offset, w.f_mean)
-    t0 = time.perf_counter()
-    oracle.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"])
-    dt = time.perf_counter() - t0
-    desc = f"1 batch item x {heads} heads x {T_s} steps of {w.name} (K={w.K}, V={w.V})"
+    dt = run(T_s)
+    what = "fwd+bwd" if w.backward else "fwd"
+    desc = f"{what} of 1 batch item x {heads} heads x {T_s} steps of {w.name} (K={w.K}, V={w.V})"
     return heads * T_s / dt, desc, threads, dt
 
 
@@ -220,6 +227,92 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def _count_launches(fn):
+    """Kernels of this library one call of fn launches (torch profiler)."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        n = 0
+        for _ in range(2):  # the first session may start recording late
+            with profile(activities=[ProfilerActivity.CUDA]) as prof:
+                fn()
+                torch.cuda.synchronize()
+            n = max(n, sum(1 for e in prof.events()
+                           if e.device_type == torch.autograd.DeviceType.CUDA
+                           and "m2rnn" in e.name))
+        return n
+    except Exception:  # profiler unavailable
+        return None
+
+
+class Runner:
+    """Preallocated buffers and the step of one workload on this rank."""
+
+    def __init__(self, w, m2rnn, rank):
+        from non_linear_matrix_gb300.inputs import make_inputs
+        self.w, self.m = w, m2rnn
+        seed = w.seed + 1000 * rank  # each rank its own batch (weak scaling)
+        self.x = make_inputs(w.B, w.T, w.N, w.K, w.V, w.dtype, seed, w.f_mean,
+                             with_dy=w.backward)
+        self.g = {n: t.cuda() for n, t in self.x.items()}
+        g = self.g
+        f32 = dict(device="cuda", dtype=torch.float32)
+        self.out = {"y": torch.empty_like(g["v"]),
+                    "HT": torch.empty(w.B, w.N, w.K, w.V, **f32)}
+        if w.backward:
+            nck = -(-w.T // w.ckpt_every)
+            self.out["ckpt"] = torch.empty(w.B, w.N, nck, w.K, w.V, **f32)
+            self.gout = {"dq": torch.empty(w.B, w.T, w.K, **f32),
+                         "dk": torch.empty(w.B, w.T, w.K, **f32),
+                         "dv": torch.empty(w.B, w.T, w.N, w.V, **f32),
+                         "df": torch.empty(w.B, w.T, w.N, **f32),
+                         "dW": torch.empty(w.N, w.V, w.V, **f32),
+                         "dw_r": torch.empty(w.N, w.V, **f32)}
+            shape = m2rnn.make_shape(g["q"], g["v"], w.ckpt_every)
+            self.ws = torch.empty(max(16, m2rnn.bwd_workspace_size(shape, True)),
+                                  device="cuda", dtype=torch.uint8)
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def fwd(self):
+        g = self.g
+        self.m.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], out=self.out,
+                   ckpt_every=self.w.ckpt_every)
+
+    def bwd(self):
+        g = self.g
+        self.m.bwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], g["dy"],
+                   ckpt=self.out["ckpt"], ckpt_every=self.w.ckpt_every, out=self.gout,
+                   workspace=self.ws)
+
+    def step(self):
+        self.fwd()
+        if self.w.backward:
+            self.bwd()
+
+    def timed(self, steps, stream):
+        """Times `steps` steps; returns (ms/step, fwd ms/step, bwd ms/step)."""
+        e0, e1, e2 = self.ev
+        tot = fw = bw = 0.0
+        if not self.w.backward:
+            e0.record(stream)
+            for _ in range(steps):
+                self.fwd()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            tot = fw = e0.elapsed_time(e1)
+        else:
+            for _ in range(steps):  # per-step events split fwd and bwd
+                e0.record(stream)
+                self.fwd()
+                e1.record(stream)
+                self.bwd()
+                e2.record(stream)
+                e2.synchronize()
+                fw += e0.elapsed_time(e1)
+                bw += e1.elapsed_time(e2)
+            tot = fw + bw
+        return tot / steps, fw / steps, bw / steps
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -229,6 +322,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-bwd-line", action="store_true",
+                    help="skip the nested fwd+bwd measurement of the default line")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     w = WORKLOADS[args.workload]
@@ -249,26 +344,25 @@ def main():
         torch.distributed.barrier()
     from non_linear_matrix_gb300 import m2rnn
     m2rnn.lib()
-
-    x = workload_inputs(w, with_dy=False)
-    if rank > 0:  # each rank its own batch (weak scaling)
-        from non_linear_matrix_gb300.inputs import make_inputs
-        x = make_inputs(w.B, w.T, w.N, w.K, w.V, w.dtype, w.seed + 1000 * rank, w.f_mean)
-    g = {n: t.cuda() for n, t in x.items()}
-    y = torch.empty_like(g["v"])
-    HT = torch.empty(w.B, w.N, w.K, w.V, device="cuda", dtype=torch.float32)
-    out = {"y": y, "HT": HT}
     stream = torch.cuda.current_stream()
 
-    def step():
-        m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], out=out)
+    def check_status(where):
+        st, detail = m2rnn.device_status(clear=True)
+        if st != 0:
+            raise RuntimeError(f"device status {st} ({detail}) {where}")
 
+    def max_over_ranks(v):
+        t = torch.tensor([v], device="cuda")
+        if world > 1:
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    run = Runner(w, m2rnn, rank)
     for _ in range(args.warmup):
-        step()
+        run.step()
     torch.cuda.synchronize()
-    st, detail = m2rnn.device_status(clear=True)
-    if st != 0:
-        raise RuntimeError(f"device status {st} ({detail}) after warm-up")
+    check_status("after warm-up")
+    launches = _count_launches(run.step)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -276,38 +370,29 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    ms, fwd_ms, bwd_ms = run.timed(args.steps, stream)
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    st, detail = m2rnn.device_status(clear=True)
-    if st != 0:
-        raise RuntimeError(f"device status {st} ({detail}) in the timed region")
-    t_max = torch.tensor([ms], device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(t_max.item())
+    check_status("in the timed region")
+    ms_max = max_over_ranks(ms)
     value = world * w.th / (ms_max * 1e-3)
 
     # End to end through the public API with host inputs.
     e2e = None
     if not args.no_e2e:
-        hx = {n: t.pin_memory() for n, t in x.items()}
-        hy = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        hx = {n: t.pin_memory() for n, t in run.x.items()}
+        res = [run.out["y"]] if not w.backward else [run.gout[n] for n in sorted(run.gout)]
+        hres = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res]
         h2d = sum(t.numel() * t.element_size() for t in hx.values())
-        d2h = hy.numel() * hy.element_size()
+        d2h = sum(t.numel() * t.element_size() for t in hres)
 
         def e2e_step():
             for n in hx:
-                g[n].copy_(hx[n], non_blocking=True)
-            step()
-            hy.copy_(y, non_blocking=True)
+                run.g[n].copy_(hx[n], non_blocking=True)
+            run.step()
+            for h, r in zip(hres, res):
+                h.copy_(r, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -315,24 +400,48 @@ def main():
         e_steps = max(3, min(args.steps, 50))
         if world > 1:
             torch.distributed.barrier()
-        ev0.record(stream)
+        e0, e1, _ = run.ev
+        e0.record(stream)
         for _ in range(e_steps):
             e2e_step()
-        ev1.record(stream)
+        e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = torch.tensor([ev0.elapsed_time(ev1) / e_steps], device="cuda")
-        if world > 1:
-            torch.distributed.all_reduce(e_ms, op=torch.distributed.ReduceOp.MAX)
-        e2e = {"value": world * w.th / (float(e_ms.item()) * 1e-3), "unit": UNIT,
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps)
+        e2e = {"value": world * w.th / (e_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
-               "ms_per_step": float(e_ms.item())}
+               "ms_per_step": e_ms}
+
+    # Nested fwd+bwd measurement (the backward rows of the path).
+    nested = None
+    if not w.backward and not args.no_bwd_line:
+        wb = WORKLOADS["fwdbwd_bf16_b8_t4096_n32"]
+        rb = Runner(wb, m2rnn, rank)
+        for _ in range(args.warmup):
+            rb.step()
+        torch.cuda.synchronize()
+        check_status("after fwd+bwd warm-up")
+        nb_steps = max(3, min(args.steps, 20))
+        if world > 1:
+            torch.distributed.barrier()
+        b_ms, b_fwd, b_bwd = rb.timed(nb_steps, stream)
+        check_status("in the fwd+bwd timed region")
+        b_ms = max_over_ranks(b_ms)
+        peaks = _peaks()
+        nested = _fwdbwd_summary(wb, world, nb_steps, b_ms, b_fwd, b_bwd, peaks,
+                                 _count_launches(rb.step))
+        del rb
 
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
     peaks = _peaks()
-    roof, roof_json = _roofline(w, ms, peaks, _traffic(w))
+    if w.backward:
+        nested_main = _fwdbwd_summary(w, world, args.steps, ms_max, fwd_ms, bwd_ms, peaks,
+                                      launches)
+        roof, roof_json = nested_main["roofline"], nested_main["roofline_hbm_tensor_serial"]
+    else:
+        roof, roof_json = _roofline(w, fwd_ms, peaks, _traffic(w))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
@@ -341,10 +450,17 @@ def main():
         "config": {"workload": w.name, "B": w.B, "T": w.T, "N": w.N, "K": w.K, "V": w.V,
                    "inputs": w.dtype, "state": "f32", "global_batch": w.B * world,
                    "seq_len": w.T, "parallelism": f"replicas{world}" if world > 1 else "1 GPU",
-                   "l2": "inputs (~0.32 GB) larger than L2; no flush"},
+                   "step": "forward + backward" if w.backward else "forward",
+                   "l2": "inputs larger than L2 (129 MB); no flush"},
         "roofline": roof, "roofline_hbm_tensor_serial": roof_json,
-        "e2e": e2e, "clocks": clocks, "gpu_launches": args.steps,
+        "e2e": e2e, "clocks": clocks,
+        "gpu_launches": launches * args.steps if launches is not None else args.steps,
+        "gpu_launches_per_step": launches,
     }
+    if w.backward:
+        line["fwd_ms"], line["bwd_ms"] = fwd_ms, bwd_ms
+    if nested is not None:
+        line["fwd_bwd"] = nested
     if not args.no_cpu:
         rate, desc, threads, _ = _oracle_rate(w, 12.0)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -352,6 +468,33 @@ def main():
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def _fwdbwd_summary(w, world, steps, ms, fwd_ms, bwd_ms, peaks, launches):
+    """Metric and rooflines of a forward + backward step.  The backward
+    recomputes each interval twice (sub-checkpoints, then sub-intervals), so
+    it evaluates 2*K*V tanh per token x head; the forward K*V."""
+    peak_tanh = NUM_SMS * SFU_TANH_PER_CLK_PER_SM * peaks["sm_max_mhz"] * 1e6
+    th = w.th * world
+    fwd_tanh, bwd_tanh = w.th * w.K * w.V, 2 * w.th * w.K * w.V
+    dom = "bwd" if bwd_ms >= fwd_ms else "fwd"
+    dom_ms = max(bwd_ms, fwd_ms)
+    dom_tanh = bwd_tanh if dom == "bwd" else fwd_tanh
+    achieved = dom_tanh / (dom_ms * 1e-3)
+    t_serial = 3 * w.T * STEP_LATENCY_CLK / (peaks["sm_max_mhz"] * 1e6) * 1e3
+    return {
+        "workload": w.name, "value": th / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "steps": steps, "ckpt_every": w.ckpt_every,
+        "gpu_launches_per_step": launches,
+        "roofline": {"bound": "alu", "kernel": dom, "achieved": achieved / 1e12,
+                     "peak": peak_tanh / 1e12, "unit": "Ttanh/s", "frac": achieved / peak_tanh,
+                     "traffic": None, "units_per_launch": dom_tanh},
+        "roofline_hbm_tensor_serial": {
+            "t_serial_ms": t_serial,
+            "note": "three dependent passes of T steps (forward, recompute, reverse); "
+                    "frac = t_serial / step time",
+            "frac": t_serial / ms},
+    }
 
 
 if __name__ == "__main__":
