@@ -461,7 +461,7 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   p.K = s->K;
   p.C = C;
   p.nck = (s->T + C - 1) / C;
-  p.S2 = C < 8 ? C : 8;
+  p.S2 = m2rnn::bwd_sub_len(s->V, f32);
   p.WPC = 1;
   p.nslices = s->K / 16;
   if (!choose_bwd(p, s->V, f32, sms)) return M2RNN_ERR_UNSUPPORTED_SHAPE;

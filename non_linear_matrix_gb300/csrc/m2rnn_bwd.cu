@@ -21,11 +21,13 @@
 //   1. load the interval's inputs into shared memory;
 //   2. recompute the interval forward from its checkpoint, keeping a
 //      sub-checkpoint every S2 steps (fp32);
-//   3. for each sub-interval, last first: recompute its S2 steps keeping
-//      bf16(H) (as MMA operand fragments) and Z (fp32), then run the reverse
-//      steps over it; per-step partials go to shared memory and are flushed
-//      with vector reductions (head sums of dq, dk) or stores.
-// All per-thread state lives in thread-private shared-memory slots laid out
+//   3. for each sub-interval, last first: recompute its S2 steps keeping,
+//      in registers, bf16(H) (as MMA operand fragments), s = (1-f)(1-Z^2)
+//      (fp32) and e = H_{t-1} - Z (fp16, |e| <= 2; fp32 on the fp32-input
+//      path), what the reverse step needs, then run the
+//      reverse steps over it; per-step partials go to shared memory and are
+//      flushed with vector reductions (head sums of dq, dk) or stores.
+// Sub-checkpoints live in thread-private shared-memory slots laid out
 // lane-contiguously (no bank conflicts).  The recomputation performs the
 // same operations as the forward kernel, so it reproduces its trajectory.
 // Synchronisation is __syncthreads only (no spin waits).
@@ -59,18 +61,17 @@ __device__ __forceinline__ float tof(__nv_bfloat16 x) { return __bfloat162float(
 struct BwdLayout {
   uint32_t in_q, in_k, in_v, in_dy, in_f;  // interval inputs
   uint32_t subck;                          // [NS1][WPC][NT][32][4] fp32
-  uint32_t hs;                             // [S2+1][WPC][KS][32][4] u32 (bf16 frags)
-  uint32_t zs;                             // [S2][WPC][NT][32][4] fp32; dW sums at the end
   uint32_t r_dq, r_dk;                     // [S2][RS] fp32
   uint32_t r_dv;                           // [S2][WPC][V] fp32
   uint32_t r_df;                           // [S2][WPC] fp32
+  uint32_t dwsum;                          // [WPC][V][V] fp32 (end of kernel)
   uint32_t total;
 };
 
 __host__ __device__ inline uint32_t al(uint32_t x) { return (x + 127u) / 128u * 128u; }
 
 __host__ __device__ inline BwdLayout bwd_layout(int V, int C, int S2, int WPC, int es) {
-  const int RS = 16 * WPC, NT = V / 8, KS = V / 16, NS1 = (C + S2 - 1) / S2;
+  const int RS = 16 * WPC, NT = V / 8, NS1 = (C + S2 - 1) / S2;
   BwdLayout L;
   uint32_t o = 0;
   L.in_q = o;
@@ -85,11 +86,6 @@ __host__ __device__ inline BwdLayout bwd_layout(int V, int C, int S2, int WPC, i
   o = al(o + C * 4);
   L.subck = o;
   o = al(o + NS1 * WPC * NT * 512);
-  L.hs = o;
-  o = al(o + (S2 + 1) * WPC * KS * 512);
-  L.zs = o;  // also holds the per-warp dW sums ([WPC][V][V] fp32) at the end
-  const int zs_bytes = S2 * WPC * NT * 512, dw_bytes = WPC * V * V * 4;
-  o = al(o + (zs_bytes > dw_bytes ? zs_bytes : dw_bytes));
   L.r_dq = o;
   o = al(o + S2 * RS * 4);
   L.r_dk = o;
@@ -98,8 +94,16 @@ __host__ __device__ inline BwdLayout bwd_layout(int V, int C, int S2, int WPC, i
   o = al(o + S2 * WPC * V * 4);
   L.r_df = o;
   o = al(o + S2 * WPC * 4);
+  L.dwsum = o;
+  o = al(o + WPC * V * V * 4);
   L.total = o;
   return L;
+}
+
+// Sub-interval length (recomputed steps held in registers) of each variant.
+template <int V, bool F32>
+__host__ __device__ constexpr int sub_len() {
+  return (V == 16 && !F32) ? 8 : (V == 32 && F32) ? 2 : 4;
 }
 
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
@@ -164,17 +168,20 @@ __device__ __forceinline__ void pack_frag_lo(const float (&H)[V / 8][4], const u
 
 // One forward step of Eqs. (10)-(11) for this warp's 16 rows, with exactly
 // the operations of the forward kernel (so trajectories agree bitwise).
-// Returns Z in Zo; updates H, A (and Al on the fp32-input path).
+// Updates H, A (and Al on the fp32-input path); returns, per element,
+// So = (1 - f)(1 - Z^2) and Eo = H_{t-1} - Z, the quantities the reverse step
+// needs.
 template <int V, bool F32>
 __device__ __forceinline__ void recompute_step(float (&H)[V / 8][4], uint32_t (&A)[V / 16][4],
                                                uint32_t (&Al)[V / 16][4],
                                                const uint32_t (&Bw)[V / 16][V / 8][2],
                                                const uint32_t (&Bwl)[V / 16][V / 8][2], float k0,
                                                float k1, const float2 (&vv)[V / 8], float fg,
-                                               float (&Zo)[V / 8][4]) {
+                                               float (&So)[V / 8][4], float (&Eo)[V / 8][4]) {
   constexpr int NT = V / 8, KS = V / 16;
   const float2 kk0 = make_float2(k0, k0), kk1 = make_float2(k1, k1);
   const float2 f2 = make_float2(fg, fg), m1 = make_float2(-1.f, -1.f);
+  const float omf = 1.f - fg;
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -206,8 +213,10 @@ __device__ __forceinline__ void recompute_step(float (&H)[V / 8][4], uint32_t (&
       const float2 hn = __ffma2_rn(f2, d, z);
       H[nt][2 * h] = hn.x;
       H[nt][2 * h + 1] = hn.y;
-      Zo[nt][2 * h] = z.x;
-      Zo[nt][2 * h + 1] = z.y;
+      Eo[nt][2 * h] = d.x;  // H_{t-1} - Z
+      Eo[nt][2 * h + 1] = d.y;
+      So[nt][2 * h] = omf * fmaf(-z.x, z.x, 1.f);
+      So[nt][2 * h + 1] = omf * fmaf(-z.y, z.y, 1.f);
     }
   pack_frag<V>(H, A);
   if (F32) pack_frag_lo<V>(H, A, Al);
@@ -218,11 +227,12 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   using TIn = typename InT<F32>::T;
   constexpr int es = sizeof(TIn);
   constexpr int NT = V / 8, KS = V / 16;
+  constexpr int S2 = sub_len<V, F32>();
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int WPC = p.WPC, RS = 16 * WPC, nthr = 32 * WPC;
-  const int K = p.K, T = p.T, N = p.N, C = p.C, S2 = p.S2;
+  const int K = p.K, T = p.T, N = p.N, C = p.C;
   const int slice = blockIdx.x % p.nslices;
   const int bn = blockIdx.x / p.nslices;
   const int b = bn / N, n = bn % N;
@@ -275,18 +285,17 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   for (int a = 0; a < KS; ++a)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) dW[a][nt][0] = dW[a][nt][1] = dW[a][nt][2] = dW[a][nt][3] = 0.f;
-  float dwr_acc = 0.f;  // thread j < V of slice 0: sum_t u_j v_j
+  float dwr_acc = 0.f;  // this thread's column tid % V of sum_t u (.) v (slice 0)
 
-  // thread-private slot addresses (lane-contiguous 16-byte groups)
+  // thread-private sub-checkpoint slot (lane-contiguous 16-byte groups)
   const uint32_t lane16 = static_cast<uint32_t>(lane * 16);
-  auto slot_f = [&](uint32_t base, int idx, int nt) -> uint32_t {  // fp32 [idx][warp][nt]
-    return base + static_cast<uint32_t>(((idx * WPC + warp) * NT + nt) * 512) + lane16;
+  auto subck_slot = [&](int idx, int nt) -> uint32_t {
+    return sb + L.subck + static_cast<uint32_t>(((idx * WPC + warp) * NT + nt) * 512) + lane16;
   };
-  auto slot_h = [&](int idx, int ks) -> uint32_t {  // bf16 frags [idx][warp][ks]
-    return sb + L.hs + static_cast<uint32_t>(((idx * WPC + warp) * KS + ks) * 512) + lane16;
-  };
+  const uint32_t kq_row = static_cast<uint32_t>((16 * warp) * es);  // this warp's rows
 
   const int nck = p.nck;
+#pragma unroll 1
   for (int ci = nck - 1; ci >= 0; --ci) {
     const int t0 = ci * C;
     const int Lc = min(C, T - t0);
@@ -329,46 +338,45 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
     }
     __syncthreads();
 
-    // per-step input addresses
-    const uint32_t kq_row = static_cast<uint32_t>((16 * warp) * es);
-    auto k_rows = [&](int s, float& k0, float& k1) {
+    // rank-1 inputs of local step s
+    auto step_in = [&](int s, float& k0, float& k1, float2 (&vv)[NT], float& fg) {
       const uint32_t a = sb + L.in_k + static_cast<uint32_t>(s * RS * es) + kq_row;
       k0 = one_f32<F32>(a + g * es);
       k1 = one_f32<F32>(a + (g + 8) * es);
-    };
-    auto v_pairs = [&](int s, float2 (&vv)[NT]) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
         vv[nt] = pair_f32<F32>(sb + L.in_v + static_cast<uint32_t>((s * V + 8 * nt + 2 * c) * es));
+      fg = ptx::lds_f32(sb + L.in_f + 4 * s);
     };
 
     // ---- 2. recompute the interval, sub-checkpoint every S2 steps ----
     uint32_t A[KS][4], Al[KS][4];
     pack_frag<V>(H, A);
     if (F32) pack_frag_lo<V>(H, A, Al);
+    const int nsub = (Lc + S2 - 1) / S2;
 #pragma unroll 1
-    for (int s = 0; s < Lc; ++s) {
-      if (s % S2 == 0) {
+    for (int sj = 0; sj < nsub; ++sj) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          ptx::sts_f32x4(slot_f(sb + L.subck, s / S2, nt), H[nt][0], H[nt][1], H[nt][2], H[nt][3]);
+      for (int nt = 0; nt < NT; ++nt)
+        ptx::sts_f32x4(subck_slot(sj, nt), H[nt][0], H[nt][1], H[nt][2], H[nt][3]);
+      const int s_end = min(Lc, (sj + 1) * S2);
+#pragma unroll 1
+      for (int s = sj * S2; s < s_end; ++s) {
+        float k0, k1, fg, Sd[NT][4], Ed[NT][4];
+        float2 vv[NT];
+        step_in(s, k0, k1, vv, fg);
+        recompute_step<V, F32>(H, A, Al, Bw, Bwl, k0, k1, vv, fg, Sd, Ed);
       }
-      float k0, k1, Zd[NT][4];
-      float2 vv[NT];
-      k_rows(s, k0, k1);
-      v_pairs(s, vv);
-      recompute_step<V, F32>(H, A, Al, Bw, Bwl, k0, k1, vv, ptx::lds_f32(sb + L.in_f + 4 * s), Zd);
     }
 
     // ---- 3. sub-intervals, last first ----
-    const int nsub = (Lc + S2 - 1) / S2;
 #pragma unroll 1
     for (int j = nsub - 1; j >= 0; --j) {
       const int s0 = j * S2;
       const int Ls = min(S2, Lc - s0);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const float4 x = ptx::lds_f32x4(slot_f(sb + L.subck, j, nt));
+        const float4 x = ptx::lds_f32x4(subck_slot(j, nt));
         H[nt][0] = x.x;
         H[nt][1] = x.y;
         H[nt][2] = x.z;
@@ -376,153 +384,165 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
       }
       pack_frag<V>(H, A);
       if (F32) pack_frag_lo<V>(H, A, Al);
+      // registers for the sub-interval: bf16(H_{s0+i}) fragments, s and e
+      uint32_t Hf[S2 + 1][KS][4];
+      float Sreg[S2][NT][4];
+      float Ef[F32 ? S2 : 1][NT][4];       // fp32 e (fp32-input path)
+      uint32_t Eb[F32 ? 1 : S2][KS][4];    // fp16 e (bf16 path), A-fragment order
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) sts_u32x4(slot_h(0, ks), A[ks][0], A[ks][1], A[ks][2], A[ks][3]);
-#pragma unroll 1
-      for (int i = 0; i < Ls; ++i) {
-        float k0, k1, Zd[NT][4];
-        float2 vv[NT];
-        k_rows(s0 + i, k0, k1);
-        v_pairs(s0 + i, vv);
-        recompute_step<V, F32>(H, A, Al, Bw, Bwl, k0, k1, vv,
-                               ptx::lds_f32(sb + L.in_f + 4 * (s0 + i)), Zd);
+      for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          ptx::sts_f32x4(slot_f(sb + L.zs, i, nt), Zd[nt][0], Zd[nt][1], Zd[nt][2], Zd[nt][3]);
+        for (int e = 0; e < 4; ++e) Hf[0][ks][e] = A[ks][e];
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
-          sts_u32x4(slot_h(i + 1, ks), A[ks][0], A[ks][1], A[ks][2], A[ks][3]);
+      for (int i = 0; i < S2; ++i) {
+        if (i < Ls) {
+          float k0, k1, fg, Ed[NT][4];
+          float2 vv[NT];
+          step_in(s0 + i, k0, k1, vv, fg);
+          recompute_step<V, F32>(H, A, Al, Bw, Bwl, k0, k1, vv, fg, Sreg[i], Ed);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) Hf[i + 1][ks][e] = A[ks][e];
+          if constexpr (F32) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) Ef[i][nt][r] = Ed[nt][r];
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+              Eb[i][ks][0] = ptx::pack_f16x2(Ed[2 * ks][0], Ed[2 * ks][1]);
+              Eb[i][ks][1] = ptx::pack_f16x2(Ed[2 * ks][2], Ed[2 * ks][3]);
+              Eb[i][ks][2] = ptx::pack_f16x2(Ed[2 * ks + 1][0], Ed[2 * ks + 1][1]);
+              Eb[i][ks][3] = ptx::pack_f16x2(Ed[2 * ks + 1][2], Ed[2 * ks + 1][3]);
+            }
+          }
+        }
       }
       // reverse steps
-#pragma unroll 1
-      for (int i = Ls - 1; i >= 0; --i) {
-        const int s = s0 + i;
-        uint32_t Hp[KS][4], Hc[KS][4];
-        float Z[NT][4];
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const uint4 a = ptx::lds_u32x4(slot_h(i, ks));
-          const uint4 d = ptx::lds_u32x4(slot_h(i + 1, ks));
-          Hp[ks][0] = a.x; Hp[ks][1] = a.y; Hp[ks][2] = a.z; Hp[ks][3] = a.w;
-          Hc[ks][0] = d.x; Hc[ks][1] = d.y; Hc[ks][2] = d.z; Hc[ks][3] = d.w;
-        }
+      for (int i = S2 - 1; i >= 0; --i) {
+        if (i < Ls) {
+          const int s = s0 + i;
+          const uint32_t qrow = sb + L.in_q + static_cast<uint32_t>(s * RS * es) + kq_row;
+          const uint32_t krow = sb + L.in_k + static_cast<uint32_t>(s * RS * es) + kq_row;
+          const float qa = one_f32<F32>(qrow + g * es), qb = one_f32<F32>(qrow + (g + 8) * es);
+          const float fg = ptx::lds_f32(sb + L.in_f + 4 * s);
+          float2 u[NT];
+          uint32_t ub[KS][2], vb[KS][2], kb[2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const float4 x = ptx::lds_f32x4(slot_f(sb + L.zs, i, nt));
-          Z[nt][0] = x.x;
-          Z[nt][1] = x.y;
-          Z[nt][2] = x.z;
-          Z[nt][3] = x.w;
-        }
-        const uint32_t qrow = sb + L.in_q + static_cast<uint32_t>(s * RS * es) + kq_row;
-        const uint32_t krow = sb + L.in_k + static_cast<uint32_t>(s * RS * es) + kq_row;
-        const float qa = one_f32<F32>(qrow + g * es), qb = one_f32<F32>(qrow + (g + 8) * es);
-        const float fg = ptx::lds_f32(sb + L.in_f + 4 * s);
-        const float omf = 1.f - fg;
-        float2 u[NT];
-        uint32_t ub[KS][2], vb[KS][2], kb[2];
+          for (int nt = 0; nt < NT; ++nt)
+            u[nt] = pair_f32<F32>(sb + L.in_dy + static_cast<uint32_t>((s * V + 8 * nt + 2 * c) * es));
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          u[nt] = pair_f32<F32>(sb + L.in_dy + static_cast<uint32_t>((s * V + 8 * nt + 2 * c) * es));
+          for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t off = static_cast<uint32_t>((s * V + 16 * ks + 8 * h + 2 * c) * es);
-            ub[ks][h] = pair_bf16<F32>(sb + L.in_dy + off);
-            vb[ks][h] = pair_bf16<F32>(sb + L.in_v + off);
-          }
-        kb[0] = pair_bf16<F32>(krow + 2 * c * es);
-        kb[1] = pair_bf16<F32>(krow + (8 + 2 * c) * es);
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t off = static_cast<uint32_t>((s * V + 16 * ks + 8 * h + 2 * c) * es);
+              ub[ks][h] = pair_bf16<F32>(sb + L.in_dy + off);
+              vb[ks][h] = pair_bf16<F32>(sb + L.in_v + off);
+            }
+          kb[0] = pair_bf16<F32>(krow + 2 * c * es);
+          kb[1] = pair_bf16<F32>(krow + (8 + 2 * c) * es);
 
-        // R = C + q u^T;  D = (1 - f) R (.) (1 - Z^2);  df partial = <R, H_{t-1} - Z>
-        float R[NT][4], D[NT][4];
-        float dfp = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int ks = nt >> 1, hh = 2 * (nt & 1);
-          const float hp[4] = {ptx::bf16x2_lo(Hp[ks][hh]), ptx::bf16x2_hi(Hp[ks][hh]),
-                               ptx::bf16x2_lo(Hp[ks][hh + 1]), ptx::bf16x2_hi(Hp[ks][hh + 1])};
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const float qr = (r < 2) ? qa : qb;
-            const float ur = (r & 1) ? u[nt].y : u[nt].x;
-            R[nt][r] = fmaf(qr, ur, Cg[nt][r]);
-            const float z = Z[nt][r];
-            D[nt][r] = omf * R[nt][r] * fmaf(-z, z, 1.f);
-            dfp = fmaf(R[nt][r], hp[r] - z, dfp);
-          }
-        }
-        uint32_t Dh[KS][4], Dl[KS][4];
-        pack_frag<V>(D, Dh);
-        pack_frag_lo<V>(D, Dh, Dl);
-        // C_{t-1} = f R + D W^T   (D as hi + lo bf16 parts)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) Cg[nt][r] = fg * R[nt][r];
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
+          // R = C + q u^T;  D = R (.) s;  df partial = <R, e>
+          float R[NT][4], D[NT][4];
+          float dfp = 0.f;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            ptx::mma_bf16_16816(Cg[nt], Dh[ks], Bt[ks][nt][0], Bt[ks][nt][1]);
-            ptx::mma_bf16_16816(Cg[nt], Dl[ks], Bt[ks][nt][0], Bt[ks][nt][1]);
-            if (F32) ptx::mma_bf16_16816(Cg[nt], Dh[ks], Btl[ks][nt][0], Btl[ks][nt][1]);
+            float ev[4];
+            if constexpr (F32) {
+#pragma unroll
+              for (int r = 0; r < 4; ++r) ev[r] = Ef[i][nt][r];
+            } else {
+              const int ks = nt >> 1, hh = 2 * (nt & 1);
+              ev[0] = ptx::f16x2_lo(Eb[i][ks][hh]);
+              ev[1] = ptx::f16x2_hi(Eb[i][ks][hh]);
+              ev[2] = ptx::f16x2_lo(Eb[i][ks][hh + 1]);
+              ev[3] = ptx::f16x2_hi(Eb[i][ks][hh + 1]);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const float qr = (r < 2) ? qa : qb;
+              const float ur = (r & 1) ? u[nt].y : u[nt].x;
+              R[nt][r] = fmaf(qr, ur, Cg[nt][r]);
+              D[nt][r] = R[nt][r] * Sreg[i][nt][r];
+              dfp = fmaf(R[nt][r], ev[r], dfp);
+            }
           }
-        // dk rows = D v;  dq rows = H_t u  (columns of B all equal)
-        float dk4[4], dq4[4];
-        ptx::mma_bf16_16816_zero(dk4, Dh[0], vb[0][0], vb[0][1]);
-        ptx::mma_bf16_16816_zero(dq4, Hc[0], ub[0][0], ub[0][1]);
+          uint32_t Dh[KS][4], Dl[KS][4];
+          pack_frag<V>(D, Dh);
+          pack_frag_lo<V>(D, Dh, Dl);
+          // C_{t-1} = f R + D W^T   (D as hi + lo bf16 parts)
 #pragma unroll
-        for (int ks = 1; ks < KS; ++ks) {
-          ptx::mma_bf16_16816(dk4, Dh[ks], vb[ks][0], vb[ks][1]);
-          ptx::mma_bf16_16816(dq4, Hc[ks], ub[ks][0], ub[ks][1]);
-        }
-        // transposed fragments of D and H_{t-1}
-        uint32_t DT[KS][4], HT[KS][4];
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
+            for (int r = 0; r < 4; ++r) Cg[nt][r] = fg * R[nt][r];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            DT[ks][e] = ptx::movmatrix_trans(Dh[ks][e]);
-            HT[ks][e] = ptx::movmatrix_trans(Hp[ks][e]);
+          for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              ptx::mma_bf16_16816(Cg[nt], Dh[ks], Bt[ks][nt][0], Bt[ks][nt][1]);
+              ptx::mma_bf16_16816(Cg[nt], Dl[ks], Bt[ks][nt][0], Bt[ks][nt][1]);
+              if (F32) ptx::mma_bf16_16816(Cg[nt], Dh[ks], Btl[ks][nt][0], Btl[ks][nt][1]);
+            }
+          // dk rows = D v;  dq rows = H_t u  (columns of B all equal)
+          float dk4[4], dq4[4];
+          ptx::mma_bf16_16816_zero(dk4, Dh[0], vb[0][0], vb[0][1]);
+          ptx::mma_bf16_16816_zero(dq4, Hf[i + 1][0], ub[0][0], ub[0][1]);
+#pragma unroll
+          for (int ks = 1; ks < KS; ++ks) {
+            ptx::mma_bf16_16816(dk4, Dh[ks], vb[ks][0], vb[ks][1]);
+            ptx::mma_bf16_16816(dq4, Hf[i + 1][ks], ub[ks][0], ub[ks][1]);
           }
-        // dW += H_{t-1}^T D: m-tile over l (= k-step ml of H), n-tile over j
+          // transposed fragments of D and H_{t-1}
+          uint32_t DT[KS][4], HT[KS][4];
 #pragma unroll
-        for (int ml = 0; ml < KS; ++ml) {
-          const uint32_t Aa[4] = {HT[ml][0], HT[ml][2], HT[ml][1], HT[ml][3]};
+          for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-          for (int nj = 0; nj < NT; ++nj)
-            ptx::mma_bf16_16816(dW[ml][nj], Aa, DT[nj >> 1][2 * (nj & 1)], DT[nj >> 1][2 * (nj & 1) + 1]);
-        }
-        // dv (this warp's rows) = D^T k: m-tile over j
-        float dv4[KS][4];
+            for (int e = 0; e < 4; ++e) {
+              DT[ks][e] = ptx::movmatrix_trans(Dh[ks][e]);
+              HT[ks][e] = ptx::movmatrix_trans(Hf[i][ks][e]);
+            }
+          // dW += H_{t-1}^T D: m-tile over l (= k-step ml of H), n-tile over j
 #pragma unroll
-        for (int mj = 0; mj < KS; ++mj) {
-          const uint32_t Aa[4] = {DT[mj][0], DT[mj][2], DT[mj][1], DT[mj][3]};
-          ptx::mma_bf16_16816_zero(dv4[mj], Aa, kb[0], kb[1]);
-        }
-        // warp sum of the df partial
-        dfp += __shfl_xor_sync(0xffffffffu, dfp, 1);
-        dfp += __shfl_xor_sync(0xffffffffu, dfp, 2);
-        dfp += __shfl_xor_sync(0xffffffffu, dfp, 4);
-        dfp += __shfl_xor_sync(0xffffffffu, dfp, 8);
-        dfp += __shfl_xor_sync(0xffffffffu, dfp, 16);
-        if (c == 0) {
-          const uint32_t rq = sb + L.r_dq + static_cast<uint32_t>((i * RS + 16 * warp + g) * 4);
-          const uint32_t rk = sb + L.r_dk + static_cast<uint32_t>((i * RS + 16 * warp + g) * 4);
-          ptx::sts_f32(rq, dq4[0]);
-          ptx::sts_f32(rq + 32, dq4[2]);
-          ptx::sts_f32(rk, dk4[0]);
-          ptx::sts_f32(rk + 32, dk4[2]);
+          for (int ml = 0; ml < KS; ++ml) {
+            const uint32_t Aa[4] = {HT[ml][0], HT[ml][2], HT[ml][1], HT[ml][3]};
+#pragma unroll
+            for (int nj = 0; nj < NT; ++nj)
+              ptx::mma_bf16_16816(dW[ml][nj], Aa, DT[nj >> 1][2 * (nj & 1)],
+                                  DT[nj >> 1][2 * (nj & 1) + 1]);
+          }
+          // dv (this warp's rows) = D^T k: m-tile over j
+          float dv4[KS][4];
 #pragma unroll
           for (int mj = 0; mj < KS; ++mj) {
-            const uint32_t rv = sb + L.r_dv + static_cast<uint32_t>(((i * WPC + warp) * V + 16 * mj + g) * 4);
-            ptx::sts_f32(rv, dv4[mj][0]);
-            ptx::sts_f32(rv + 32, dv4[mj][2]);
+            const uint32_t Aa[4] = {DT[mj][0], DT[mj][2], DT[mj][1], DT[mj][3]};
+            ptx::mma_bf16_16816_zero(dv4[mj], Aa, kb[0], kb[1]);
           }
+          // warp sum of the df partial
+          dfp += __shfl_xor_sync(0xffffffffu, dfp, 1);
+          dfp += __shfl_xor_sync(0xffffffffu, dfp, 2);
+          dfp += __shfl_xor_sync(0xffffffffu, dfp, 4);
+          dfp += __shfl_xor_sync(0xffffffffu, dfp, 8);
+          dfp += __shfl_xor_sync(0xffffffffu, dfp, 16);
+          if (c == 0) {
+            const uint32_t rq = sb + L.r_dq + static_cast<uint32_t>((i * RS + 16 * warp + g) * 4);
+            const uint32_t rk = sb + L.r_dk + static_cast<uint32_t>((i * RS + 16 * warp + g) * 4);
+            ptx::sts_f32(rq, dq4[0]);
+            ptx::sts_f32(rq + 32, dq4[2]);
+            ptx::sts_f32(rk, dk4[0]);
+            ptx::sts_f32(rk + 32, dk4[2]);
+#pragma unroll
+            for (int mj = 0; mj < KS; ++mj) {
+              const uint32_t rv =
+                  sb + L.r_dv + static_cast<uint32_t>(((i * WPC + warp) * V + 16 * mj + g) * 4);
+              ptx::sts_f32(rv, dv4[mj][0]);
+              ptx::sts_f32(rv + 32, dv4[mj][2]);
+            }
+          }
+          if (lane == 0) ptx::sts_f32(sb + L.r_df + static_cast<uint32_t>((i * WPC + warp) * 4), dfp);
         }
-        if (lane == 0) ptx::sts_f32(sb + L.r_df + static_cast<uint32_t>((i * WPC + warp) * 4), dfp);
       }
       __syncthreads();
       // ---- flush the sub-interval's per-step results ----
@@ -550,7 +570,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
           } else {
             red_add(dst, slice == 0 ? fmaf(tof(wr[jj]), uu, acc) : acc);
           }
-          if (slice == 0) dwr_acc = fmaf(uu, vv, dwr_acc);  // thread e % V == jj throughout
+          if (slice == 0) dwr_acc = fmaf(uu, vv, dwr_acc);  // e % V == tid % V throughout
         }
         for (int i = tid; i < Ls; i += nthr) {
           float acc = 0.f;
@@ -586,10 +606,9 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
         *reinterpret_cast<float2*>(p.dH0 + sidx + (row0 + g + 8 * h) * V + 8 * nt + 2 * c) =
             make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
   }
-  // dW: this warp's [V][V] sum -> shared memory (reusing the Z slots) -> CTA sum -> global
-  __syncthreads();
+  // dW: this warp's [V][V] sum -> shared memory -> CTA sum -> global
   {
-    const uint32_t base = sb + L.zs + static_cast<uint32_t>(warp * V * V * 4);
+    const uint32_t base = sb + L.dwsum + static_cast<uint32_t>(warp * V * V * 4);
 #pragma unroll
     for (int ml = 0; ml < KS; ++ml)
 #pragma unroll
@@ -604,7 +623,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   for (int e = tid; e < V * V; e += nthr) {
     float acc = 0.f;
     for (int w = 0; w < WPC; ++w)
-      acc += ptx::lds_f32(sb + L.zs + static_cast<uint32_t>((w * V * V + e) * 4));
+      acc += ptx::lds_f32(sb + L.dwsum + static_cast<uint32_t>((w * V * V + e) * 4));
     red_add(p.dW + static_cast<size_t>(n) * V * V + e, acc);
   }
   // each thread holds the u (.) v sum of column tid % V over the steps it flushed
@@ -613,7 +632,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
 
 template <int V, bool F32>
 cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
-  const BwdLayout L = bwd_layout(V, p.C, p.S2, p.WPC, F32 ? 4 : 2);
+  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2);
   auto kern = bwd_kernel<V, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L.total));
@@ -625,7 +644,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
 
 template <int V, bool F32>
 int bwd_ctas_per_sm_t(const BwdParams& p) {
-  const BwdLayout L = bwd_layout(V, p.C, p.S2, p.WPC, F32 ? 4 : 2);
+  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2);
   auto kern = bwd_kernel<V, F32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(L.total)) != cudaSuccess)
@@ -638,6 +657,11 @@ int bwd_ctas_per_sm_t(const BwdParams& p) {
 
 }  // namespace
 
+int bwd_sub_len(int V, bool f32_inputs) {
+  if (V == 16) return f32_inputs ? sub_len<16, true>() : sub_len<16, false>();
+  return f32_inputs ? sub_len<32, true>() : sub_len<32, false>();
+}
+
 size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs) {
   return bwd_layout(V, C, S2, WPC, f32_inputs ? 4 : 2).total;
 }
@@ -648,7 +672,7 @@ int bwd_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs) {
 }
 
 cudaError_t launch_bwd(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream) {
-  if (p.WPC < 1 || p.WPC > 8 || p.S2 < 1) return cudaErrorInvalidValue;
+  if (p.WPC < 1 || p.WPC > 8 || p.S2 != bwd_sub_len(V, f32_inputs)) return cudaErrorInvalidValue;
   if (V == 16) return f32_inputs ? launch_bwd_t<16, true>(p, stream) : launch_bwd_t<16, false>(p, stream);
   if (V == 32) return f32_inputs ? launch_bwd_t<32, true>(p, stream) : launch_bwd_t<32, false>(p, stream);
   return cudaErrorInvalidValue;

@@ -66,12 +66,13 @@ struct BwdParams {
   int nck;      // checkpoints per (b, n)
   int WPC;      // warps per CTA (16 rows each)
   int nslices;  // K / (16 * WPC)
-  int S2;       // sub-interval length of the recomputation
+  int S2;       // sub-interval length of the recomputation (= bwd_sub_len)
 };
 
 cudaError_t launch_bwd(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream);
 int bwd_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs);
 size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs);
+int bwd_sub_len(int V, bool f32_inputs);  // sub-interval length of the variant
 
 // Launches the forward kernel variant for (V, input dtype, MT m-tiles/warp).
 cudaError_t launch_fwd(const FwdParams& p, int V, bool f32_inputs, int MT, cudaStream_t stream);

@@ -30,6 +30,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Packs two floats into f16x2 (round to nearest even): lo -> bits 0..15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float f16x2_lo(uint32_t x) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(x));
+  return f;
+}
+__device__ __forceinline__ float f16x2_hi(uint32_t x) {
+  float f;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(x));
+  return f;
+}
+
 // The two bf16 halves of a packed register, as floats (exact).
 __device__ __forceinline__ float bf16x2_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16x2_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }

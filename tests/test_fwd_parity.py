@@ -83,10 +83,10 @@ def _restart_parity(oracle_mod, x, y, HT, ck, C, tol, label, H0=None):
     h0 = np.zeros((B, N, K, V)) if H0 is None else H0.double().numpy()
     assert np.abs(ckn[:, :, 0] - h0).max() <= 1e-6, (label, "ckpt[0] != H0")
     worst = {"y": 0.0, "state": 0.0}
-    for c0, c1 in ((0, T // C), (T // C, nck)):  # full intervals, then the ragged tail
+    groups = ((0, T // C, C), (T // C, nck, T - (T // C) * C))  # full intervals, ragged tail
+    for c0, c1, L in groups:
         if c1 <= c0:
             continue
-        L = C if c0 == 0 else T - (T // C) * C
         t0, t1 = c0 * C, c0 * C + (c1 - c0) * L
         nb = c1 - c0
 
