@@ -105,13 +105,17 @@ FwdConfig choose_fwd(const m2rnn_shape* s, int sms) {
       }
     }
   }
-  // Tuning override: M2RNN_FWD_MT=1|2|4 forces the rows-per-warp variant.
+  // Tuning override: M2RNN_FWD_MT=0|1|2|4 forces the rows-per-warp variant
+  // (0 = half slices of 8 rows; measured slower than full slices when all
+  // of a head's warps share one SM, so never chosen automatically).
   if (const char* e = std::getenv("M2RNN_FWD_MT")) {
     const int m = std::atoi(e);
-    if ((m == 1 || m == 2 || m == 4) && mtiles % m == 0 && !(f32 && m != 1) && !(s->V == 32 && m == 4))
+    const bool fits = m != 0 || s->K / 8 <= m2rnn::fwd_max_consumer_warps(s->V, 0, f32);
+    if ((m == 0 || m == 1 || m == 2 || m == 4) && (m == 0 || mtiles % m == 0) &&
+        !(f32 && m != 1) && !(s->V == 32 && m == 4) && fits)
       MT = m;
   }
-  const int WPH = mtiles / MT;
+  const int WPH = MT == 0 ? s->K / 8 : mtiles / MT;
   const int maxw = m2rnn::fwd_max_consumer_warps(s->V, MT, f32);
   int best = 1;
   for (int G = 1; G <= s->N && G * WPH <= maxw; ++G) {

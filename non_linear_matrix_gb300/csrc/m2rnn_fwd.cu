@@ -29,6 +29,10 @@
 //              A    = bf16(H)         (the next step's A operand)
 //              ypart = q^T H          (MMA on movmatrix-transposed A)
 //            The rank-1 inputs of step t+1 are read while step t computes.
+// MT = 0 selects half slices for latency-bound problems: each warp owns 8
+// rows (rows 8..15 of its m16 tile are zero padding), which halves the tanh
+// and elementwise work on each warp's serial chain and doubles the warps
+// working on a head.
 // The fp32-input path keeps the same structure but splits H and W into
 // bf16 hi + lo parts (three MMAs), uses the accurate tanhf and an fp32
 // readout.
@@ -348,7 +352,7 @@ __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout
 
 // Stores the thread's part of the state (rows row0 + 16*mt + g (+8), columns
 // 8*nt + 2c (+1)) to a [K][V] fp32 array.
-template <int V, int MT>
+template <int V, int MT, bool HALF = false>
 __device__ __forceinline__ void store_state(float* dst, const float (&H)[MT][V / 8][4], int row0,
                                             int g, int c) {
 #pragma unroll
@@ -356,22 +360,23 @@ __device__ __forceinline__ void store_state(float* dst, const float (&H)[MT][V /
 #pragma unroll
     for (int nt = 0; nt < V / 8; ++nt)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < (HALF ? 1 : 2); ++h) {
         const int row = row0 + 16 * mt + g + 8 * h;
         *reinterpret_cast<float2*>(dst + row * V + 8 * nt + 2 * c) =
             make_float2(H[mt][nt][2 * h], H[mt][nt][2 * h + 1]);
       }
 }
 
-// Accumulator layout of n-tiles (2ks, 2ks+1) -> A operand of k-step ks.
-template <int V>
+// Accumulator layout of n-tiles (2ks, 2ks+1) -> A operand of k-step ks
+// (rows 8..15 zero for half slices).
+template <int V, bool HALF = false>
 __device__ __forceinline__ void pack_a(const float (&H)[V / 8][4], uint32_t (&A)[V / 16][4]) {
 #pragma unroll
   for (int ks = 0; ks < V / 16; ++ks) {
     A[ks][0] = ptx::pack_bf16x2(H[2 * ks][0], H[2 * ks][1]);
-    A[ks][1] = ptx::pack_bf16x2(H[2 * ks][2], H[2 * ks][3]);
+    A[ks][1] = HALF ? 0u : ptx::pack_bf16x2(H[2 * ks][2], H[2 * ks][3]);
     A[ks][2] = ptx::pack_bf16x2(H[2 * ks + 1][0], H[2 * ks + 1][1]);
-    A[ks][3] = ptx::pack_bf16x2(H[2 * ks + 1][2], H[2 * ks + 1][3]);
+    A[ks][3] = HALF ? 0u : ptx::pack_bf16x2(H[2 * ks + 1][2], H[2 * ks + 1][3]);
   }
 }
 
@@ -399,13 +404,13 @@ struct StepIn {
   float2 vf[NT];
 };
 
-template <int V, int MT, bool F32>
+template <int V, int MT, bool F32, bool HALF = false>
 __device__ __forceinline__ void load_step(StepIn<MT, V / 8, F32>& in, uint32_t kdb, uint32_t vb,
                                           int g, int c) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     in.k0[mt] = ptx::lds_f32x2(kdb + 8 * (16 * mt + g));
-    in.k1[mt] = ptx::lds_f32x2(kdb + 8 * (16 * mt + 8 + g));
+    in.k1[mt] = HALF ? make_float2(0.f, 0.f) : ptx::lds_f32x2(kdb + 8 * (16 * mt + 8 + g));
   }
 #pragma unroll
   for (int nt = 0; nt < V / 8; ++nt) {
@@ -428,7 +433,7 @@ struct WarpState {
 
 // One recurrence step for this warp's MT slices; writes the slices' readout
 // partial (columns 8nt+2c, +1, on lanes with g == 0) to ypaddr.
-template <int V, int MT, bool F32>
+template <int V, int MT, bool F32, bool HALF = false>
 __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V / 8, F32>& in,
                                          uint32_t qb, uint32_t fdaddr, uint32_t ypaddr, int g,
                                          int c) {
@@ -459,7 +464,8 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float2 lo = __fmul2_rn(in.k0[mt], vv[nt]), hi = __fmul2_rn(in.k1[mt], vv[nt]);
+      const float2 lo = __fmul2_rn(in.k0[mt], vv[nt]);
+      const float2 hi = HALF ? make_float2(0.f, 0.f) : __fmul2_rn(in.k1[mt], vv[nt]);
       acc[nt][0] = lo.x;
       acc[nt][1] = lo.y;
       acc[nt][2] = hi.x;
@@ -479,7 +485,7 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < (HALF ? 1 : 2); ++h) {
         float2 z;
         z.x = F32 ? tanhf(acc[nt][2 * h]) : ptx::tanh_approx(acc[nt][2 * h]);
         z.y = F32 ? tanhf(acc[nt][2 * h + 1]) : ptx::tanh_approx(acc[nt][2 * h + 1]);
@@ -489,7 +495,7 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
         S.H[mt][nt][2 * h] = hn.x;
         S.H[mt][nt][2 * h + 1] = hn.y;
       }
-    pack_a<V>(S.H[mt], S.A[mt]);
+    pack_a<V, HALF>(S.H[mt], S.A[mt]);
     if constexpr (F32) {
       pack_a_lo<V>(S.H[mt], S.A[mt], S.Al[mt]);
 #pragma unroll
@@ -508,7 +514,7 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const uint32_t b0 = ptx::movmatrix_trans(S.A[mt][ks][2 * h2]);
-          const uint32_t b1 = ptx::movmatrix_trans(S.A[mt][ks][2 * h2 + 1]);
+          const uint32_t b1 = HALF ? 0u : ptx::movmatrix_trans(S.A[mt][ks][2 * h2 + 1]);
           if (mt == 0)
             ptx::mma_bf16_16816_zero(ya[2 * ks + h2], Aq, b0, b1);
           else
@@ -535,17 +541,19 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
   }
 }
 
-template <int V, int MT, bool F32>
+template <int V, int MT_, bool F32>
 __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout& L, uint32_t sbase,
                                              int b, int n0, int ci) {
   using TIn = typename InType<F32>::T;
+  constexpr bool HALF = MT_ == 0;       // half slices: 8 rows per warp
+  constexpr int MT = HALF ? 1 : MT_;
   constexpr int es = sizeof(TIn);
   constexpr int NT = V / 8, KS = V / 16;
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int K = p.K, T = p.T, N = p.N, G = p.G, WPH = p.WPH;
   const int hl = ci / WPH, w = ci - hl * WPH;
   const int n = n0 + hl;
-  const int row0 = w * 16 * MT;
+  const int row0 = w * (HALF ? 8 : 16 * MT);
   const uint32_t bars = sbase + L.bars;
 
   WarpState<V, MT> S;
@@ -572,11 +580,11 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int row = row0 + 16 * mt + g + 8 * (r >> 1), col = 8 * nt + 2 * c + (r & 1);
-        S.H[mt][nt][r] = p.H0 ? p.H0[hoff + row * V + col] : 0.f;
+        S.H[mt][nt][r] = (p.H0 && (!HALF || r < 2)) ? p.H0[hoff + row * V + col] : 0.f;
       }
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
-    pack_a<V>(S.H[mt], S.A[mt]);
+    pack_a<V, HALF>(S.H[mt], S.A[mt]);
     if (F32) pack_a_lo<V>(S.H[mt], S.A[mt], S.Al[mt]);
   }
 
@@ -613,11 +621,11 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
     // The rank-1 inputs of step tl+1 are read while step tl computes.  The
     // read past the chunk's last step (slot Tc <= TC) stays inside this
     // stage's shared memory and its values are never used.
-    load_step<V, MT, F32>(in0, kdb, vb, g, c);
+    load_step<V, MT, F32, HALF>(in0, kdb, vb, g, c);
     int tl = 0;
     while (tl < Tc) {
       if (t0 + tl == next_ck) {
-        store_state<V, MT>(ckpt, S.H, row0, g, c);
+        store_state<V, MT, HALF>(ckpt, S.H, row0, g, c);
         ckpt += K * V;
         next_ck += p.C;
       }
@@ -625,17 +633,17 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
 #pragma unroll 1
       for (; tl + 1 < seg_end; tl += 2) {
         const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1, u2 = u0 + 2;
-        load_step<V, MT, F32>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
-        fwd_step<V, MT, F32>(S, in0, qb + u0 * q_stride, fdb + u0 * fd_stride,
+        load_step<V, MT, F32, HALF>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
+        fwd_step<V, MT, F32, HALF>(S, in0, qb + u0 * q_stride, fdb + u0 * fd_stride,
                              yb + u0 * yp_stride, g, c);
-        load_step<V, MT, F32>(in0, kdb + u2 * kd_stride, vb + u2 * v_stride, g, c);
-        fwd_step<V, MT, F32>(S, in1, qb + u1 * q_stride, fdb + u1 * fd_stride,
+        load_step<V, MT, F32, HALF>(in0, kdb + u2 * kd_stride, vb + u2 * v_stride, g, c);
+        fwd_step<V, MT, F32, HALF>(S, in1, qb + u1 * q_stride, fdb + u1 * fd_stride,
                              yb + u1 * yp_stride, g, c);
       }
       if (tl < seg_end) {  // odd remainder of the segment
         const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1;
-        load_step<V, MT, F32>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
-        fwd_step<V, MT, F32>(S, in0, qb + u0 * q_stride, fdb + u0 * fd_stride,
+        load_step<V, MT, F32, HALF>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
+        fwd_step<V, MT, F32, HALF>(S, in0, qb + u0 * q_stride, fdb + u0 * fd_stride,
                              yb + u0 * yp_stride, g, c);
         in0 = in1;
         ++tl;
@@ -651,7 +659,7 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
     if (lane == 0) record_timeout(p.status, SITE_FWD_CONSUMER);
     return;
   }
-  if (p.HT != nullptr) store_state<V, MT>(p.HT + hoff, S.H, row0, g, c);
+  if (p.HT != nullptr) store_state<V, MT, HALF>(p.HT + hoff, S.H, row0, g, c);
 }
 
 template <int V, int MT, bool F32>
@@ -727,6 +735,7 @@ size_t fwd_smem_bytes(int K, int V, int G, int WPH, bool f32_inputs, int tc) {
 
 int fwd_max_consumer_warps(int V, int MT, bool f32_inputs) {
   if (f32_inputs) return V == 16 ? max_consumer_warps<16, 1, true>() : max_consumer_warps<32, 1, true>();
+  if (MT == 0) return V == 16 ? max_consumer_warps<16, 0, false>() : max_consumer_warps<32, 0, false>();
   if (V == 16)
     return MT == 1   ? max_consumer_warps<16, 1, false>()
            : MT == 2 ? max_consumer_warps<16, 2, false>()
@@ -736,6 +745,7 @@ int fwd_max_consumer_warps(int V, int MT, bool f32_inputs) {
 
 int fwd_ctas_per_sm(const FwdParams& p, int V, bool f32_inputs, int MT) {
   if (f32_inputs) return V == 16 ? ctas_per_sm_t<16, 1, true>(p) : ctas_per_sm_t<32, 1, true>(p);
+  if (MT == 0) return V == 16 ? ctas_per_sm_t<16, 0, false>(p) : ctas_per_sm_t<32, 0, false>(p);
   if (V == 16)
     return MT == 1 ? ctas_per_sm_t<16, 1, false>(p)
            : MT == 2 ? ctas_per_sm_t<16, 2, false>(p) : ctas_per_sm_t<16, 4, false>(p);
@@ -749,6 +759,7 @@ cudaError_t launch_fwd(const FwdParams& p, int V, bool f32_inputs, int MT, cudaS
     if (V == 32) return launch_t<32, 1, true>(p, stream);
     return cudaErrorInvalidValue;
   }
+  if (MT == 0) return V == 16 ? launch_t<16, 0, false>(p, stream) : launch_t<32, 0, false>(p, stream);
   if (V == 16) {
     if (MT == 1) return launch_t<16, 1, false>(p, stream);
     if (MT == 2) return launch_t<16, 2, false>(p, stream);

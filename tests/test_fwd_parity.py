@@ -178,6 +178,17 @@ def test_restart_parity_ragged_tail_and_H0(m2rnn, oracle_mod):
     _restart_parity(oracle_mod, x, y, HT, ck, 48, TOL["bf16"], "ragged", H0=H0)
 
 
+@pytest.mark.parametrize("mt", ["0", "1", "2", "4"])
+def test_rows_per_warp_variants(m2rnn, oracle_mod, monkeypatch, mt):
+    """Every rows-per-warp variant (forced through M2RNN_FWD_MT; 0 = half
+    slices of 8 rows) on a ragged shape with H0 and checkpoints."""
+    monkeypatch.setenv("M2RNN_FWD_MT", mt)
+    B, T, N = 3, 77, 6
+    x = make_inputs(B, T, N, 64, 16, "bf16", 600 + int(mt))
+    H0 = torch.rand(B, N, 64, 16, generator=torch.Generator().manual_seed(4)) - 0.5
+    _compare(m2rnn, oracle_mod, x, "bf16", H0=H0, ckpt_every=16, label=f"MT={mt}")
+
+
 def test_many_heads_per_cta_groups(m2rnn, oracle_mod):
     """Shapes whose dispatch uses several heads per CTA and 2-slice warps."""
     for (B, T, N) in [(40, 70, 64), (3, 40, 7)]:
