@@ -67,6 +67,25 @@ def _peaks():
         return dict(FALLBACK_PEAKS, sm_max_mhz=SM_MAX_MHZ, source="fallback")
 
 
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling: per-GPU work is fixed)."""
+    return base_seed + 1000 * rank
+
+
+def max_over_ranks(value: float, device: str = "cuda") -> float:
+    """The slowest rank's time (the job finishes when the last rank does)."""
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, ms_slowest: float) -> float:
+    """Whole-job units per second: all ranks' units over the slowest time."""
+    return world * units_per_rank / (ms_slowest * 1e-3)
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -250,7 +269,7 @@ class Runner:
     def __init__(self, w, m2rnn, rank):
         from non_linear_matrix_gb300.inputs import make_inputs
         self.w, self.m = w, m2rnn
-        seed = w.seed + 1000 * rank  # each rank its own batch (weak scaling)
+        seed = rank_seed(w.seed, rank)
         self.x = make_inputs(w.B, w.T, w.N, w.K, w.V, w.dtype, seed, w.f_mean,
                              with_dy=w.backward)
         self.g = {n: t.cuda() for n, t in self.x.items()}
@@ -351,12 +370,6 @@ def main():
         if st != 0:
             raise RuntimeError(f"device status {st} ({detail}) {where}")
 
-    def max_over_ranks(v):
-        t = torch.tensor([v], device="cuda")
-        if world > 1:
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
-
     run = Runner(w, m2rnn, rank)
     for _ in range(args.warmup):
         run.step()
@@ -376,7 +389,7 @@ def main():
     clocks = sampler.stop()
     check_status("in the timed region")
     ms_max = max_over_ranks(ms)
-    value = world * w.th / (ms_max * 1e-3)
+    value = job_throughput(w.th, world, ms_max)
 
     # End to end through the public API with host inputs.
     e2e = None
@@ -407,7 +420,7 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps)
-        e2e = {"value": world * w.th / (e_ms * 1e-3), "unit": UNIT,
+        e2e = {"value": job_throughput(w.th, world, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
                "ms_per_step": e_ms}
 
