@@ -41,7 +41,8 @@ import torch  # noqa: E402
 
 from non_linear_matrix_gb300.inputs import WORKLOADS, workload_inputs  # noqa: E402
 
-METRIC = "M2RNN fwd tokens x heads/s on 1 GB300"
+METRIC = ("M2RNN fwd(+bwd) tokens\u00d7heads/s on 1 GB300; % of roofline "
+          "(tensor/HBM/serial bound)")
 UNIT = "tokens*heads/s"
 DEFAULT_WORKLOAD = "fwd_bf16_b64_t4096_n32"
 

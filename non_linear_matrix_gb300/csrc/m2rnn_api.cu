@@ -275,30 +275,41 @@ int bwd_interval(const m2rnn_shape* s, bool ckpt_given, bool* own_ckpt) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Picks warps per CTA (16 rows each) for the fewest waves; ties go to more
-// rows per CTA (fewer cross-CTA reductions).
+// Picks warps per CTA (16 rows each) and the interleaved variant for the
+// fewest waves; ties go to the interleaved variant, then to more rows per CTA
+// (fewer cross-CTA reductions).  M2RNN_BWD_ILV=0 or 1 restricts the variant.
 bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
   const int mtiles = p.K / 16;
-  int best_w = 0;
+  const char* env = std::getenv("M2RNN_BWD_ILV");
+  const int force = env != nullptr ? std::atoi(env) : -1;
+  int best_w = 0, best_ilv = 0;
   long long best_waves = 0;
-  for (int w = mtiles < 8 ? mtiles : 8; w >= 1; w /= 2) {
-    if (mtiles % w != 0) continue;
-    if (m2rnn::bwd_smem_bytes(V, p.C, p.S2, w, f32) > kSmemBudget) continue;
-    m2rnn::BwdParams q = p;
-    q.WPC = w;
-    q.nslices = mtiles / w;
-    const int R = m2rnn::bwd_ctas_per_sm(q, V, f32);
-    if (R <= 0) continue;
-    const long long ctas = static_cast<long long>(p.B) * p.N * q.nslices;
-    const long long waves = (ctas + static_cast<long long>(sms) * R - 1) / (static_cast<long long>(sms) * R);
-    if (best_w == 0 || waves < best_waves) {
-      best_w = w;
-      best_waves = waves;
+  for (int ilv = 1; ilv >= 0; --ilv) {
+    if (ilv == 1 && (!m2rnn::bwd_has_ilv(V) || force == 0)) continue;
+    if (ilv == 0 && force == 1 && m2rnn::bwd_has_ilv(V)) continue;
+    for (int w = mtiles < 8 ? mtiles : 8; w >= 1; w /= 2) {
+      if (mtiles % w != 0) continue;
+      if (m2rnn::bwd_smem_bytes(V, p.C, p.S2, w, f32, ilv != 0) > kSmemBudget) continue;
+      m2rnn::BwdParams q = p;
+      q.WPC = w;
+      q.nslices = mtiles / w;
+      q.ilv = ilv;
+      const int R = m2rnn::bwd_ctas_per_sm(q, V, f32);
+      if (R <= 0) continue;
+      const long long ctas = static_cast<long long>(p.B) * p.N * q.nslices;
+      const long long waves =
+          (ctas + static_cast<long long>(sms) * R - 1) / (static_cast<long long>(sms) * R);
+      if (best_w == 0 || waves < best_waves) {
+        best_w = w;
+        best_ilv = ilv;
+        best_waves = waves;
+      }
     }
   }
   if (best_w == 0) return false;
   p.WPC = best_w;
   p.nslices = mtiles / best_w;
+  p.ilv = best_ilv;
   return true;
 }
 
@@ -468,6 +479,7 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   p.S2 = m2rnn::bwd_sub_len(s->V, f32);
   p.WPC = 1;
   p.nslices = s->K / 16;
+  p.ilv = 0;
   if (!choose_bwd(p, s->V, f32, sms)) return M2RNN_ERR_UNSUPPORTED_SHAPE;
   const size_t BT = static_cast<size_t>(s->B) * s->T;
   if (cudaMemsetAsync(dq, 0, BT * s->K * sizeof(float), st) != cudaSuccess ||

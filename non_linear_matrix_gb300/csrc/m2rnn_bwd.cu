@@ -35,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "m2rnn.h"
 #include "m2rnn_internal.h"
@@ -57,45 +58,54 @@ struct InT<false> {
 __device__ __forceinline__ float tof(float x) { return x; }
 __device__ __forceinline__ float tof(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// Shared-memory layout of one CTA (byte offsets).
+// Shared-memory layout of one CTA (byte offsets).  With interleaving the
+// k/v/f inputs and the sub-checkpoints are double-buffered (buffer ci & 1
+// holds interval ci); the per-step partials are double-buffered by
+// sub-interval in every variant.
 struct BwdLayout {
-  uint32_t in_q, in_k, in_v, in_dy, in_f;  // interval inputs
-  uint32_t subck;                          // [NS1][WPC][NT][32][4] fp32
-  uint32_t r_dq, r_dk;                     // [S2][RS] fp32
-  uint32_t r_dv;                           // [S2][WPC][V] fp32
-  uint32_t r_df;                           // [S2][WPC] fp32
-  uint32_t dwsum;                          // [WPC][V][V] fp32 (end of kernel)
+  uint32_t in_q, in_dy;              // [C][RS], [C][V]: the interval being reversed
+  uint32_t in_k, in_v, in_f;         // buffer 0: [C][RS], [C][V], [C] fp32
+  uint32_t kbuf, vbuf, fbuf;         // byte stride to buffer 1
+  uint32_t subck, sbuf;              // [NS1][WPC][NT][32][4] fp32, stride to buffer 1
+  uint32_t dwsum;                    // [WPC][V][V] fp32 (end of kernel; aliases subck)
+  uint32_t r_dq, r_dk, r_dv, r_df;   // [2][S2][RS], [2][S2][RS], [2][S2][WPC][V], [2][S2][WPC]
   uint32_t total;
 };
 
 __host__ __device__ inline uint32_t al(uint32_t x) { return (x + 127u) / 128u * 128u; }
 
-__host__ __device__ inline BwdLayout bwd_layout(int V, int C, int S2, int WPC, int es) {
-  const int RS = 16 * WPC, NT = V / 8, NS1 = (C + S2 - 1) / S2;
+__host__ __device__ inline BwdLayout bwd_layout(int V, int C, int S2, int WPC, int es, bool ilv) {
+  // Step buffers hold NS1 * S2 >= C steps: recompute steps past the end of
+  // an interval read the padding and their results are discarded.
+  const uint32_t RS = 16 * WPC, NT = V / 8, NS1 = (C + S2 - 1) / S2, CP = NS1 * S2;
+  const uint32_t nb = ilv ? 2 : 1;
   BwdLayout L;
   uint32_t o = 0;
   L.in_q = o;
   o = al(o + C * RS * es);
-  L.in_k = o;
-  o = al(o + C * RS * es);
-  L.in_v = o;
-  o = al(o + C * V * es);
   L.in_dy = o;
   o = al(o + C * V * es);
+  L.kbuf = al(CP * RS * es);
+  L.in_k = o;
+  o += nb * L.kbuf;
+  L.vbuf = al(CP * V * es);
+  L.in_v = o;
+  o += nb * L.vbuf;
+  L.fbuf = al(CP * 4);
   L.in_f = o;
-  o = al(o + C * 4);
-  L.subck = o;
-  o = al(o + NS1 * WPC * NT * 512);
+  o += nb * L.fbuf;
+  L.sbuf = NS1 * WPC * NT * 512;
+  L.subck = L.dwsum = o;
+  const uint32_t dws = WPC * V * V * 4;
+  o = al(o + (nb * L.sbuf > dws ? nb * L.sbuf : dws));
   L.r_dq = o;
-  o = al(o + S2 * RS * 4);
+  o = al(o + 2 * S2 * RS * 4);
   L.r_dk = o;
-  o = al(o + S2 * RS * 4);
+  o = al(o + 2 * S2 * RS * 4);
   L.r_dv = o;
-  o = al(o + S2 * WPC * V * 4);
+  o = al(o + 2 * S2 * WPC * V * 4);
   L.r_df = o;
-  o = al(o + S2 * WPC * 4);
-  L.dwsum = o;
-  o = al(o + WPC * V * V * 4);
+  o = al(o + 2 * S2 * WPC * 4);
   L.total = o;
   return L;
 }
@@ -222,7 +232,7 @@ __device__ __forceinline__ void recompute_step(float (&H)[V / 8][4], uint32_t (&
   if (F32) pack_frag_lo<V>(H, A, Al);
 }
 
-template <int V, bool F32>
+template <int V, bool F32, bool ILV>
 __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   using TIn = typename InT<F32>::T;
   constexpr int es = sizeof(TIn);
@@ -238,7 +248,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   const int b = bn / N, n = bn % N;
   const int row0c = slice * RS;            // first row of this CTA
   const int row0 = row0c + 16 * warp;      // first row of this warp
-  const BwdLayout L = bwd_layout(V, C, S2, WPC, es);
+  const BwdLayout L = bwd_layout(V, C, S2, WPC, es, ILV);
   const uint32_t sb = ptx::smem_addr(smem);
 
   const TIn* q = static_cast<const TIn*>(p.q);
@@ -289,99 +299,140 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
 
   // thread-private sub-checkpoint slot (lane-contiguous 16-byte groups)
   const uint32_t lane16 = static_cast<uint32_t>(lane * 16);
-  auto subck_slot = [&](int idx, int nt) -> uint32_t {
-    return sb + L.subck + static_cast<uint32_t>(((idx * WPC + warp) * NT + nt) * 512) + lane16;
+  auto subck_slot = [&](int buf, int idx, int nt) -> uint32_t {
+    return sb + L.subck + buf * L.sbuf + static_cast<uint32_t>(((idx * WPC + warp) * NT + nt) * 512) +
+           lane16;
   };
   const uint32_t kq_row = static_cast<uint32_t>((16 * warp) * es);  // this warp's rows
 
+  // rank-1 inputs of local step s of the interval held in k/v/f buffer buf
+  auto step_in = [&](int buf, int s, float& k0, float& k1, float2 (&vv)[NT], float& fg) {
+    const uint32_t a = sb + L.in_k + buf * L.kbuf + static_cast<uint32_t>(s * RS * es) + kq_row;
+    k0 = one_f32<F32>(a + g * es);
+    k1 = one_f32<F32>(a + (g + 8) * es);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      vv[nt] = pair_f32<F32>(sb + L.in_v + buf * L.vbuf +
+                             static_cast<uint32_t>((s * V + 8 * nt + 2 * c) * es));
+    fg = ptx::lds_f32(sb + L.in_f + buf * L.fbuf + 4 * s);
+  };
+  // cooperative loads of an interval's inputs (Lc steps from t0)
+  auto load_qdy = [&](int t0, int Lc) {
+    const size_t bt0 = static_cast<size_t>(b) * T + t0;
+    const int qv = RS * es / 16;  // 16-byte vectors per step
+    for (int e = tid; e < Lc * qv; e += nthr) {
+      const int s = e / qv, x = e - s * qv;
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(q + (bt0 + s) * K + row0c) + x);
+      sts_u32x4(sb + L.in_q + static_cast<uint32_t>(s * RS * es + 16 * x), a.x, a.y, a.z, a.w);
+    }
+    const int vvn = V * es / 16;
+    for (int e = tid; e < Lc * vvn; e += nthr) {
+      const int s = e / vvn, x = e - s * vvn;
+      const uint4 d = __ldg(reinterpret_cast<const uint4*>(dy + ((bt0 + s) * N + n) * V) + x);
+      sts_u32x4(sb + L.in_dy + static_cast<uint32_t>(s * V * es + 16 * x), d.x, d.y, d.z, d.w);
+    }
+  };
+  auto load_kvf = [&](int t0, int Lc, int buf) {
+    const size_t bt0 = static_cast<size_t>(b) * T + t0;
+    const uint32_t kb = sb + L.in_k + buf * L.kbuf, vb = sb + L.in_v + buf * L.vbuf;
+    const int qv = RS * es / 16;
+    for (int e = tid; e < Lc * qv; e += nthr) {
+      const int s = e / qv, x = e - s * qv;
+      const uint4 d = __ldg(reinterpret_cast<const uint4*>(kin + (bt0 + s) * K + row0c) + x);
+      sts_u32x4(kb + static_cast<uint32_t>(s * RS * es + 16 * x), d.x, d.y, d.z, d.w);
+    }
+    const int vvn = V * es / 16;
+    for (int e = tid; e < Lc * vvn; e += nthr) {
+      const int s = e / vvn, x = e - s * vvn;
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(vin + ((bt0 + s) * N + n) * V) + x);
+      sts_u32x4(vb + static_cast<uint32_t>(s * V * es + 16 * x), a.x, a.y, a.z, a.w);
+    }
+    for (int s = tid; s < Lc; s += nthr)
+      ptx::sts_f32(sb + L.in_f + buf * L.fbuf + 4 * s, tof(fin[(bt0 + s) * N + n]));
+  };
+  // checkpoint H_{ci C} of this thread's elements
+  auto load_ckpt = [&](int ci, float (&H)[NT][4]) {
+    const float* ck = p.ckpt + ((static_cast<size_t>(b) * N + n) * p.nck + ci) * K * V;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float2 x = *reinterpret_cast<const float2*>(ck + (row0 + g + 8 * h) * V + 8 * nt + 2 * c);
+        H[nt][2 * h] = x.x;
+        H[nt][2 * h + 1] = x.y;
+      }
+  };
+  // interval recompute, one step at a time: steps [m0, m1) of the interval in
+  // buffer buf, storing a sub-checkpoint before every S2-th step
+  auto interval_recompute = [&](int buf, int m0, int m1, float (&H)[NT][4], uint32_t (&A)[KS][4],
+                                uint32_t (&Al)[KS][4]) {
+#pragma unroll 1
+    for (int m = m0; m < m1; ++m) {
+      if (m % S2 == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          ptx::sts_f32x4(subck_slot(buf, m / S2, nt), H[nt][0], H[nt][1], H[nt][2], H[nt][3]);
+      }
+      float k0, k1, fg, Sd[NT][4], Ed[NT][4];
+      float2 vv[NT];
+      step_in(buf, m, k0, k1, vv, fg);
+      recompute_step<V, F32>(H, A, Al, Bw, Bwl, k0, k1, vv, fg, Sd, Ed);
+    }
+  };
+
   const int nck = p.nck;
+  // state of the interval recompute (of interval ci - 1 while ci is reversed)
+  float H1[NT][4];
+  uint32_t A1[KS][4], Al1[KS][4];
+  if constexpr (ILV) {
+    const int ci = nck - 1;
+    load_kvf(ci * C, T - ci * C, ci & 1);
+    load_ckpt(ci, H1);
+    __syncthreads();
+    pack_frag<V>(H1, A1);
+    if (F32) pack_frag_lo<V>(H1, A1, Al1);
+    interval_recompute(ci & 1, 0, T - ci * C, H1, A1, Al1);
+  }
+
 #pragma unroll 1
   for (int ci = nck - 1; ci >= 0; --ci) {
     const int t0 = ci * C;
     const int Lc = min(C, T - t0);
-    // ---- 1. interval inputs -> shared memory ----
+    const int buf = ILV ? (ci & 1) : 0;
+    const int nbuf = buf ^ 1;
+    // ---- 1. inputs -> shared memory ----
     __syncthreads();
-    {
-      const size_t bt0 = static_cast<size_t>(b) * T + t0;
-      const int qv = RS * es / 16;  // 16-byte vectors per step
-      for (int e = tid; e < Lc * qv; e += nthr) {
-        const int s = e / qv, x = e - s * qv;
-        const uint4 a = __ldg(reinterpret_cast<const uint4*>(q + (bt0 + s) * K + row0c) + x);
-        const uint4 d = __ldg(reinterpret_cast<const uint4*>(kin + (bt0 + s) * K + row0c) + x);
-        sts_u32x4(sb + L.in_q + static_cast<uint32_t>(s * RS * es + 16 * x), a.x, a.y, a.z, a.w);
-        sts_u32x4(sb + L.in_k + static_cast<uint32_t>(s * RS * es + 16 * x), d.x, d.y, d.z, d.w);
-      }
-      const int vvn = V * es / 16;
-      for (int e = tid; e < Lc * vvn; e += nthr) {
-        const int s = e / vvn, x = e - s * vvn;
-        const size_t off = ((bt0 + s) * N + n) * V;
-        const uint4 a = __ldg(reinterpret_cast<const uint4*>(vin + off) + x);
-        const uint4 d = __ldg(reinterpret_cast<const uint4*>(dy + off) + x);
-        sts_u32x4(sb + L.in_v + static_cast<uint32_t>(s * V * es + 16 * x), a.x, a.y, a.z, a.w);
-        sts_u32x4(sb + L.in_dy + static_cast<uint32_t>(s * V * es + 16 * x), d.x, d.y, d.z, d.w);
-      }
-      for (int s = tid; s < Lc; s += nthr)
-        ptx::sts_f32(sb + L.in_f + 4 * s, tof(fin[(bt0 + s) * N + n]));
-    }
-    // checkpoint H_{t0} of this thread's elements
-    float H[NT][4];
-    {
-      const float* ck = p.ckpt + ((static_cast<size_t>(b) * N + n) * nck + ci) * K * V;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float2 x = *reinterpret_cast<const float2*>(ck + (row0 + g + 8 * h) * V + 8 * nt + 2 * c);
-          H[nt][2 * h] = x.x;
-          H[nt][2 * h + 1] = x.y;
-        }
+    load_qdy(t0, Lc);
+    if (!ILV) {
+      load_kvf(t0, Lc, 0);
+      load_ckpt(ci, H1);
+    } else if (ci > 0) {  // next interval to be reversed: recomputed alongside this one
+      load_kvf(t0 - C, C, nbuf);
+      load_ckpt(ci - 1, H1);
     }
     __syncthreads();
-
-    // rank-1 inputs of local step s
-    auto step_in = [&](int s, float& k0, float& k1, float2 (&vv)[NT], float& fg) {
-      const uint32_t a = sb + L.in_k + static_cast<uint32_t>(s * RS * es) + kq_row;
-      k0 = one_f32<F32>(a + g * es);
-      k1 = one_f32<F32>(a + (g + 8) * es);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        vv[nt] = pair_f32<F32>(sb + L.in_v + static_cast<uint32_t>((s * V + 8 * nt + 2 * c) * es));
-      fg = ptx::lds_f32(sb + L.in_f + 4 * s);
-    };
-
-    // ---- 2. recompute the interval, sub-checkpoint every S2 steps ----
-    uint32_t A[KS][4], Al[KS][4];
-    pack_frag<V>(H, A);
-    if (F32) pack_frag_lo<V>(H, A, Al);
-    const int nsub = (Lc + S2 - 1) / S2;
-#pragma unroll 1
-    for (int sj = 0; sj < nsub; ++sj) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        ptx::sts_f32x4(subck_slot(sj, nt), H[nt][0], H[nt][1], H[nt][2], H[nt][3]);
-      const int s_end = min(Lc, (sj + 1) * S2);
-#pragma unroll 1
-      for (int s = sj * S2; s < s_end; ++s) {
-        float k0, k1, fg, Sd[NT][4], Ed[NT][4];
-        float2 vv[NT];
-        step_in(s, k0, k1, vv, fg);
-        recompute_step<V, F32>(H, A, Al, Bw, Bwl, k0, k1, vv, fg, Sd, Ed);
-      }
-    }
+    pack_frag<V>(H1, A1);
+    if (F32) pack_frag_lo<V>(H1, A1, Al1);
+    // ---- 2. (serial variant) recompute the interval, sub-checkpoint every S2 steps ----
+    if (!ILV) interval_recompute(0, 0, Lc, H1, A1, Al1);
 
     // ---- 3. sub-intervals, last first ----
+    const int nsub = (Lc + S2 - 1) / S2;
 #pragma unroll 1
     for (int j = nsub - 1; j >= 0; --j) {
       const int s0 = j * S2;
       const int Ls = min(S2, Lc - s0);
+      const int rb = j & 1;  // partial-results buffer of this sub-interval
+      float H[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const float4 x = ptx::lds_f32x4(subck_slot(j, nt));
+        const float4 x = ptx::lds_f32x4(subck_slot(buf, j, nt));
         H[nt][0] = x.x;
         H[nt][1] = x.y;
         H[nt][2] = x.z;
         H[nt][3] = x.w;
       }
+      uint32_t A[KS][4], Al[KS][4];
       pack_frag<V>(H, A);
       if (F32) pack_frag_lo<V>(H, A, Al);
       // registers for the sub-interval: bf16(H_{s0+i}) fragments, s and e
@@ -393,166 +444,197 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
       for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
         for (int e = 0; e < 4; ++e) Hf[0][ks][e] = A[ks][e];
+      // S2 recompute steps (steps past Ls run on buffer padding and are not
+      // used), interleaved with S2 steps of the interval recompute of ci - 1
+      const int m0 = (nsub - 1 - j) * S2;
 #pragma unroll
       for (int i = 0; i < S2; ++i) {
-        if (i < Ls) {
-          float k0, k1, fg, Ed[NT][4];
+        if constexpr (ILV) {
+          if (i == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              ptx::sts_f32x4(subck_slot(nbuf, m0 / S2, nt), H1[nt][0], H1[nt][1], H1[nt][2],
+                             H1[nt][3]);
+          }
+          float k0, k1, fg, Sd[NT][4], Ed[NT][4];
           float2 vv[NT];
-          step_in(s0 + i, k0, k1, vv, fg);
-          recompute_step<V, F32>(H, A, Al, Bw, Bwl, k0, k1, vv, fg, Sreg[i], Ed);
+          step_in(nbuf, m0 + i, k0, k1, vv, fg);
+          recompute_step<V, F32>(H1, A1, Al1, Bw, Bwl, k0, k1, vv, fg, Sd, Ed);
+        }
+        float k0, k1, fg, Ed[NT][4];
+        float2 vv[NT];
+        step_in(buf, s0 + i, k0, k1, vv, fg);
+        recompute_step<V, F32>(H, A, Al, Bw, Bwl, k0, k1, vv, fg, Sreg[i], Ed);
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks)
+        for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) Hf[i + 1][ks][e] = A[ks][e];
-          if constexpr (F32) {
+          for (int e = 0; e < 4; ++e) Hf[i + 1][ks][e] = A[ks][e];
+        if constexpr (F32) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) Ef[i][nt][r] = Ed[nt][r];
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            Eb[i][ks][0] = ptx::pack_f16x2(Ed[2 * ks][0], Ed[2 * ks][1]);
+            Eb[i][ks][1] = ptx::pack_f16x2(Ed[2 * ks][2], Ed[2 * ks][3]);
+            Eb[i][ks][2] = ptx::pack_f16x2(Ed[2 * ks + 1][0], Ed[2 * ks + 1][1]);
+            Eb[i][ks][3] = ptx::pack_f16x2(Ed[2 * ks + 1][2], Ed[2 * ks + 1][3]);
+          }
+        }
+      }
+      // reverse steps S2-1 .. 0 (those below Ls); full sub-intervals take a
+      // branch-free instantiation
+      auto reverse = [&](auto full_tag) {
+        constexpr bool FULL = decltype(full_tag)::value;
+#pragma unroll
+        for (int i = S2 - 1; i >= 0; --i) {
+          if (FULL || i < Ls) {
+            const int s = s0 + i;
+            const uint32_t qrow = sb + L.in_q + static_cast<uint32_t>(s * RS * es) + kq_row;
+            const uint32_t krow = sb + L.in_k + buf * L.kbuf + static_cast<uint32_t>(s * RS * es) + kq_row;
+            const uint32_t vrow = sb + L.in_v + buf * L.vbuf + static_cast<uint32_t>(s * V * es);
+            const uint32_t urow = sb + L.in_dy + static_cast<uint32_t>(s * V * es);
+            const float qa = one_f32<F32>(qrow + g * es), qb = one_f32<F32>(qrow + (g + 8) * es);
+            const float fg = ptx::lds_f32(sb + L.in_f + buf * L.fbuf + 4 * s);
+            float2 u[NT];
+            uint32_t ub[KS][2], vb[KS][2], kb[2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              u[nt] = pair_f32<F32>(urow + static_cast<uint32_t>((8 * nt + 2 * c) * es));
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t off = static_cast<uint32_t>((16 * ks + 8 * h + 2 * c) * es);
+                ub[ks][h] = pair_bf16<F32>(urow + off);
+                vb[ks][h] = pair_bf16<F32>(vrow + off);
+              }
+            kb[0] = pair_bf16<F32>(krow + 2 * c * es);
+            kb[1] = pair_bf16<F32>(krow + (8 + 2 * c) * es);
+
+            // R = C + q u^T;  D = R (.) s;  df partial = <R, e>
+            float R[NT][4], D[NT][4];
+            float dfp = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              float ev[4];
+              if constexpr (F32) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) ev[r] = Ef[i][nt][r];
+              } else {
+                const int ks = nt >> 1, hh = 2 * (nt & 1);
+                ev[0] = ptx::f16x2_lo(Eb[i][ks][hh]);
+                ev[1] = ptx::f16x2_hi(Eb[i][ks][hh]);
+                ev[2] = ptx::f16x2_lo(Eb[i][ks][hh + 1]);
+                ev[3] = ptx::f16x2_hi(Eb[i][ks][hh + 1]);
+              }
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                const float qr = (r < 2) ? qa : qb;
+                const float ur = (r & 1) ? u[nt].y : u[nt].x;
+                R[nt][r] = fmaf(qr, ur, Cg[nt][r]);
+                D[nt][r] = R[nt][r] * Sreg[i][nt][r];
+                dfp = fmaf(R[nt][r], ev[r], dfp);
+              }
+            }
+            uint32_t Dh[KS][4], Dl[KS][4];
+            pack_frag<V>(D, Dh);
+            pack_frag_lo<V>(D, Dh, Dl);
+            // C_{t-1} = f R + D W^T   (D as hi + lo bf16 parts)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-              for (int r = 0; r < 4; ++r) Ef[i][nt][r] = Ed[nt][r];
-          } else {
+              for (int r = 0; r < 4; ++r) Cg[nt][r] = fg * R[nt][r];
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-              Eb[i][ks][0] = ptx::pack_f16x2(Ed[2 * ks][0], Ed[2 * ks][1]);
-              Eb[i][ks][1] = ptx::pack_f16x2(Ed[2 * ks][2], Ed[2 * ks][3]);
-              Eb[i][ks][2] = ptx::pack_f16x2(Ed[2 * ks + 1][0], Ed[2 * ks + 1][1]);
-              Eb[i][ks][3] = ptx::pack_f16x2(Ed[2 * ks + 1][2], Ed[2 * ks + 1][3]);
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                ptx::mma_bf16_16816(Cg[nt], Dh[ks], Bt[ks][nt][0], Bt[ks][nt][1]);
+                ptx::mma_bf16_16816(Cg[nt], Dl[ks], Bt[ks][nt][0], Bt[ks][nt][1]);
+                if (F32) ptx::mma_bf16_16816(Cg[nt], Dh[ks], Btl[ks][nt][0], Btl[ks][nt][1]);
+              }
+            // dk rows = D v;  dq rows = H_t u  (columns of B all equal)
+            float dk4[4], dq4[4];
+            ptx::mma_bf16_16816_zero(dk4, Dh[0], vb[0][0], vb[0][1]);
+            ptx::mma_bf16_16816_zero(dq4, Hf[i + 1][0], ub[0][0], ub[0][1]);
+#pragma unroll
+            for (int ks = 1; ks < KS; ++ks) {
+              ptx::mma_bf16_16816(dk4, Dh[ks], vb[ks][0], vb[ks][1]);
+              ptx::mma_bf16_16816(dq4, Hf[i + 1][ks], ub[ks][0], ub[ks][1]);
             }
-          }
-        }
-      }
-      // reverse steps
+            // transposed fragments of D and H_{t-1}
+            uint32_t DT[KS][4], HT[KS][4];
 #pragma unroll
-      for (int i = S2 - 1; i >= 0; --i) {
-        if (i < Ls) {
-          const int s = s0 + i;
-          const uint32_t qrow = sb + L.in_q + static_cast<uint32_t>(s * RS * es) + kq_row;
-          const uint32_t krow = sb + L.in_k + static_cast<uint32_t>(s * RS * es) + kq_row;
-          const float qa = one_f32<F32>(qrow + g * es), qb = one_f32<F32>(qrow + (g + 8) * es);
-          const float fg = ptx::lds_f32(sb + L.in_f + 4 * s);
-          float2 u[NT];
-          uint32_t ub[KS][2], vb[KS][2], kb[2];
+            for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            u[nt] = pair_f32<F32>(sb + L.in_dy + static_cast<uint32_t>((s * V + 8 * nt + 2 * c) * es));
+              for (int e = 0; e < 4; ++e) {
+                DT[ks][e] = ptx::movmatrix_trans(Dh[ks][e]);
+                HT[ks][e] = ptx::movmatrix_trans(Hf[i][ks][e]);
+              }
+            // dW += H_{t-1}^T D: m-tile over l (= k-step ml of H), n-tile over j
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks)
+            for (int ml = 0; ml < KS; ++ml) {
+              const uint32_t Aa[4] = {HT[ml][0], HT[ml][2], HT[ml][1], HT[ml][3]};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t off = static_cast<uint32_t>((s * V + 16 * ks + 8 * h + 2 * c) * es);
-              ub[ks][h] = pair_bf16<F32>(sb + L.in_dy + off);
-              vb[ks][h] = pair_bf16<F32>(sb + L.in_v + off);
+              for (int nj = 0; nj < NT; ++nj)
+                ptx::mma_bf16_16816(dW[ml][nj], Aa, DT[nj >> 1][2 * (nj & 1)],
+                                    DT[nj >> 1][2 * (nj & 1) + 1]);
             }
-          kb[0] = pair_bf16<F32>(krow + 2 * c * es);
-          kb[1] = pair_bf16<F32>(krow + (8 + 2 * c) * es);
-
-          // R = C + q u^T;  D = R (.) s;  df partial = <R, e>
-          float R[NT][4], D[NT][4];
-          float dfp = 0.f;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            float ev[4];
-            if constexpr (F32) {
-#pragma unroll
-              for (int r = 0; r < 4; ++r) ev[r] = Ef[i][nt][r];
-            } else {
-              const int ks = nt >> 1, hh = 2 * (nt & 1);
-              ev[0] = ptx::f16x2_lo(Eb[i][ks][hh]);
-              ev[1] = ptx::f16x2_hi(Eb[i][ks][hh]);
-              ev[2] = ptx::f16x2_lo(Eb[i][ks][hh + 1]);
-              ev[3] = ptx::f16x2_hi(Eb[i][ks][hh + 1]);
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const float qr = (r < 2) ? qa : qb;
-              const float ur = (r & 1) ? u[nt].y : u[nt].x;
-              R[nt][r] = fmaf(qr, ur, Cg[nt][r]);
-              D[nt][r] = R[nt][r] * Sreg[i][nt][r];
-              dfp = fmaf(R[nt][r], ev[r], dfp);
-            }
-          }
-          uint32_t Dh[KS][4], Dl[KS][4];
-          pack_frag<V>(D, Dh);
-          pack_frag_lo<V>(D, Dh, Dl);
-          // C_{t-1} = f R + D W^T   (D as hi + lo bf16 parts)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) Cg[nt][r] = fg * R[nt][r];
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              ptx::mma_bf16_16816(Cg[nt], Dh[ks], Bt[ks][nt][0], Bt[ks][nt][1]);
-              ptx::mma_bf16_16816(Cg[nt], Dl[ks], Bt[ks][nt][0], Bt[ks][nt][1]);
-              if (F32) ptx::mma_bf16_16816(Cg[nt], Dh[ks], Btl[ks][nt][0], Btl[ks][nt][1]);
-            }
-          // dk rows = D v;  dq rows = H_t u  (columns of B all equal)
-          float dk4[4], dq4[4];
-          ptx::mma_bf16_16816_zero(dk4, Dh[0], vb[0][0], vb[0][1]);
-          ptx::mma_bf16_16816_zero(dq4, Hf[i + 1][0], ub[0][0], ub[0][1]);
-#pragma unroll
-          for (int ks = 1; ks < KS; ++ks) {
-            ptx::mma_bf16_16816(dk4, Dh[ks], vb[ks][0], vb[ks][1]);
-            ptx::mma_bf16_16816(dq4, Hf[i + 1][ks], ub[ks][0], ub[ks][1]);
-          }
-          // transposed fragments of D and H_{t-1}
-          uint32_t DT[KS][4], HT[KS][4];
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              DT[ks][e] = ptx::movmatrix_trans(Dh[ks][e]);
-              HT[ks][e] = ptx::movmatrix_trans(Hf[i][ks][e]);
-            }
-          // dW += H_{t-1}^T D: m-tile over l (= k-step ml of H), n-tile over j
-#pragma unroll
-          for (int ml = 0; ml < KS; ++ml) {
-            const uint32_t Aa[4] = {HT[ml][0], HT[ml][2], HT[ml][1], HT[ml][3]};
-#pragma unroll
-            for (int nj = 0; nj < NT; ++nj)
-              ptx::mma_bf16_16816(dW[ml][nj], Aa, DT[nj >> 1][2 * (nj & 1)],
-                                  DT[nj >> 1][2 * (nj & 1) + 1]);
-          }
-          // dv (this warp's rows) = D^T k: m-tile over j
-          float dv4[KS][4];
-#pragma unroll
-          for (int mj = 0; mj < KS; ++mj) {
-            const uint32_t Aa[4] = {DT[mj][0], DT[mj][2], DT[mj][1], DT[mj][3]};
-            ptx::mma_bf16_16816_zero(dv4[mj], Aa, kb[0], kb[1]);
-          }
-          // warp sum of the df partial
-          dfp += __shfl_xor_sync(0xffffffffu, dfp, 1);
-          dfp += __shfl_xor_sync(0xffffffffu, dfp, 2);
-          dfp += __shfl_xor_sync(0xffffffffu, dfp, 4);
-          dfp += __shfl_xor_sync(0xffffffffu, dfp, 8);
-          dfp += __shfl_xor_sync(0xffffffffu, dfp, 16);
-          if (c == 0) {
-            const uint32_t rq = sb + L.r_dq + static_cast<uint32_t>((i * RS + 16 * warp + g) * 4);
-            const uint32_t rk = sb + L.r_dk + static_cast<uint32_t>((i * RS + 16 * warp + g) * 4);
-            ptx::sts_f32(rq, dq4[0]);
-            ptx::sts_f32(rq + 32, dq4[2]);
-            ptx::sts_f32(rk, dk4[0]);
-            ptx::sts_f32(rk + 32, dk4[2]);
+            // dv (this warp's rows) = D^T k: m-tile over j
+            float dv4[KS][4];
 #pragma unroll
             for (int mj = 0; mj < KS; ++mj) {
-              const uint32_t rv =
-                  sb + L.r_dv + static_cast<uint32_t>(((i * WPC + warp) * V + 16 * mj + g) * 4);
-              ptx::sts_f32(rv, dv4[mj][0]);
-              ptx::sts_f32(rv + 32, dv4[mj][2]);
+              const uint32_t Aa[4] = {DT[mj][0], DT[mj][2], DT[mj][1], DT[mj][3]};
+              ptx::mma_bf16_16816_zero(dv4[mj], Aa, kb[0], kb[1]);
             }
+            // warp sum of the df partial
+            dfp += __shfl_xor_sync(0xffffffffu, dfp, 1);
+            dfp += __shfl_xor_sync(0xffffffffu, dfp, 2);
+            dfp += __shfl_xor_sync(0xffffffffu, dfp, 4);
+            dfp += __shfl_xor_sync(0xffffffffu, dfp, 8);
+            dfp += __shfl_xor_sync(0xffffffffu, dfp, 16);
+            const int ri = rb * S2 + i;  // row of the partial-results buffers
+            if (c == 0) {
+              const uint32_t rq = sb + L.r_dq + static_cast<uint32_t>((ri * RS + 16 * warp + g) * 4);
+              const uint32_t rk = sb + L.r_dk + static_cast<uint32_t>((ri * RS + 16 * warp + g) * 4);
+              ptx::sts_f32(rq, dq4[0]);
+              ptx::sts_f32(rq + 32, dq4[2]);
+              ptx::sts_f32(rk, dk4[0]);
+              ptx::sts_f32(rk + 32, dk4[2]);
+#pragma unroll
+              for (int mj = 0; mj < KS; ++mj) {
+                const uint32_t rv =
+                    sb + L.r_dv + static_cast<uint32_t>(((ri * WPC + warp) * V + 16 * mj + g) * 4);
+                ptx::sts_f32(rv, dv4[mj][0]);
+                ptx::sts_f32(rv + 32, dv4[mj][2]);
+              }
+            }
+            if (lane == 0)
+              ptx::sts_f32(sb + L.r_df + static_cast<uint32_t>((ri * WPC + warp) * 4), dfp);
           }
-          if (lane == 0) ptx::sts_f32(sb + L.r_df + static_cast<uint32_t>((i * WPC + warp) * 4), dfp);
         }
-      }
+      };
+      if (Ls == S2)
+        reverse(std::true_type{});
+      else
+        reverse(std::false_type{});
+      // ---- flush the sub-interval's per-step results (buffer rb) ----
+      // One barrier per sub-interval: the next sub-interval writes the other
+      // buffer, and the one after that is behind the next barrier.
       __syncthreads();
-      // ---- flush the sub-interval's per-step results ----
       {
         const size_t bt = static_cast<size_t>(b) * T + t0 + s0;
         const int r4 = RS / 4;
+        const uint32_t rq = sb + L.r_dq + static_cast<uint32_t>(rb * S2 * RS * 4);
+        const uint32_t rk = sb + L.r_dk + static_cast<uint32_t>(rb * S2 * RS * 4);
+        const uint32_t rv = sb + L.r_dv + static_cast<uint32_t>(rb * S2 * WPC * V * 4);
+        const uint32_t rf = sb + L.r_df + static_cast<uint32_t>(rb * S2 * WPC * 4);
         for (int e = tid; e < Ls * r4; e += nthr) {
           const int i = e / r4, x = e - i * r4;
-          const float4 a = ptx::lds_f32x4(sb + L.r_dq + static_cast<uint32_t>((i * RS + 4 * x) * 4));
-          const float4 d = ptx::lds_f32x4(sb + L.r_dk + static_cast<uint32_t>((i * RS + 4 * x) * 4));
+          const float4 a = ptx::lds_f32x4(rq + static_cast<uint32_t>((i * RS + 4 * x) * 4));
+          const float4 d = ptx::lds_f32x4(rk + static_cast<uint32_t>((i * RS + 4 * x) * 4));
           red_add_v4(p.dq + (bt + i) * K + row0c + 4 * x, a.x, a.y, a.z, a.w);
           red_add_v4(p.dk + (bt + i) * K + row0c + 4 * x, d.x, d.y, d.z, d.w);
         }
@@ -560,10 +642,10 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
           const int i = e / V, jj = e - i * V;
           float acc = 0.f;
           for (int w = 0; w < WPC; ++w)
-            acc += ptx::lds_f32(sb + L.r_dv + static_cast<uint32_t>(((i * WPC + w) * V + jj) * 4));
+            acc += ptx::lds_f32(rv + static_cast<uint32_t>(((i * WPC + w) * V + jj) * 4));
           const int s = s0 + i;
           const float uu = one_f32<F32>(sb + L.in_dy + static_cast<uint32_t>((s * V + jj) * es));
-          const float vv = one_f32<F32>(sb + L.in_v + static_cast<uint32_t>((s * V + jj) * es));
+          const float vv = one_f32<F32>(sb + L.in_v + buf * L.vbuf + static_cast<uint32_t>((s * V + jj) * es));
           float* dst = p.dv + ((bt + i) * N + n) * V + jj;
           if (p.nslices == 1) {
             *dst = fmaf(tof(wr[jj]), uu, acc);
@@ -574,8 +656,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
         }
         for (int i = tid; i < Ls; i += nthr) {
           float acc = 0.f;
-          for (int w = 0; w < WPC; ++w)
-            acc += ptx::lds_f32(sb + L.r_df + static_cast<uint32_t>((i * WPC + w) * 4));
+          for (int w = 0; w < WPC; ++w) acc += ptx::lds_f32(rf + static_cast<uint32_t>((i * WPC + w) * 4));
           float* dst = p.df + (bt + i) * N + n;
           if (p.nslices == 1)
             *dst = acc;
@@ -583,8 +664,10 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
             red_add(dst, acc);
         }
       }
-      __syncthreads();
     }
+    // the interval recompute of ci - 1 past what ran alongside (when this
+    // interval is the shorter, ragged last one)
+    if (ILV && ci > 0 && nsub * S2 < C) interval_recompute(nbuf, nsub * S2, C, H1, A1, Al1);
     // C now holds dL/dH_{t0}: the gradient of this interval's checkpoint.
     if (p.dckpt != nullptr && ci % p.dck_ratio == 0) {
       float* dst = p.dckpt + ((static_cast<size_t>(b) * N + n) * p.dck_n + ci / p.dck_ratio) * K * V;
@@ -606,7 +689,9 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
         *reinterpret_cast<float2*>(p.dH0 + sidx + (row0 + g + 8 * h) * V + 8 * nt + 2 * c) =
             make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
   }
-  // dW: this warp's [V][V] sum -> shared memory -> CTA sum -> global
+  // dW: this warp's [V][V] sum -> shared memory (over the sub-checkpoints,
+  // no longer read) -> CTA sum -> global
+  __syncthreads();
   {
     const uint32_t base = sb + L.dwsum + static_cast<uint32_t>(warp * V * V * 4);
 #pragma unroll
@@ -630,10 +715,10 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   if (slice == 0) red_add(p.dw_r + static_cast<size_t>(n) * V + tid % V, dwr_acc);
 }
 
-template <int V, bool F32>
+template <int V, bool F32, bool ILV>
 cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
-  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2);
-  auto kern = bwd_kernel<V, F32>;
+  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2, ILV);
+  auto kern = bwd_kernel<V, F32, ILV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L.total));
   if (e != cudaSuccess) return e;
@@ -642,10 +727,10 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int V, bool F32>
+template <int V, bool F32, bool ILV>
 int bwd_ctas_per_sm_t(const BwdParams& p) {
-  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2);
-  auto kern = bwd_kernel<V, F32>;
+  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2, ILV);
+  auto kern = bwd_kernel<V, F32, ILV>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(L.total)) != cudaSuccess)
     return 0;
@@ -662,19 +747,31 @@ int bwd_sub_len(int V, bool f32_inputs) {
   return f32_inputs ? sub_len<32, true>() : sub_len<32, false>();
 }
 
-size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs) {
-  return bwd_layout(V, C, S2, WPC, f32_inputs ? 4 : 2).total;
+bool bwd_has_ilv(int V) { return V == 16; }
+
+size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs, bool ilv) {
+  return bwd_layout(V, C, S2, WPC, f32_inputs ? 4 : 2, ilv).total;
 }
 
 int bwd_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs) {
-  if (V == 16) return f32_inputs ? bwd_ctas_per_sm_t<16, true>(p) : bwd_ctas_per_sm_t<16, false>(p);
-  return f32_inputs ? bwd_ctas_per_sm_t<32, true>(p) : bwd_ctas_per_sm_t<32, false>(p);
+  if (V == 16) {
+    if (p.ilv) return f32_inputs ? bwd_ctas_per_sm_t<16, true, true>(p) : bwd_ctas_per_sm_t<16, false, true>(p);
+    return f32_inputs ? bwd_ctas_per_sm_t<16, true, false>(p) : bwd_ctas_per_sm_t<16, false, false>(p);
+  }
+  if (p.ilv) return 0;
+  return f32_inputs ? bwd_ctas_per_sm_t<32, true, false>(p) : bwd_ctas_per_sm_t<32, false, false>(p);
 }
 
 cudaError_t launch_bwd(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream) {
   if (p.WPC < 1 || p.WPC > 8 || p.S2 != bwd_sub_len(V, f32_inputs)) return cudaErrorInvalidValue;
-  if (V == 16) return f32_inputs ? launch_bwd_t<16, true>(p, stream) : launch_bwd_t<16, false>(p, stream);
-  if (V == 32) return f32_inputs ? launch_bwd_t<32, true>(p, stream) : launch_bwd_t<32, false>(p, stream);
+  if (p.ilv && !bwd_has_ilv(V)) return cudaErrorInvalidValue;
+  if (V == 16) {
+    if (p.ilv)
+      return f32_inputs ? launch_bwd_t<16, true, true>(p, stream) : launch_bwd_t<16, false, true>(p, stream);
+    return f32_inputs ? launch_bwd_t<16, true, false>(p, stream) : launch_bwd_t<16, false, false>(p, stream);
+  }
+  if (V == 32)
+    return f32_inputs ? launch_bwd_t<32, true, false>(p, stream) : launch_bwd_t<32, false, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -198,3 +198,20 @@ def test_workload_fwd_bwd(m2rnn, oracle_mod):
     w = WORKLOADS["fwdbwd_bf16_b8_t4096_n32"]
     x = workload_inputs(w)
     _restart_parity(m2rnn, oracle_mod, x, w.ckpt_every, label=w.name)
+
+
+@pytest.mark.parametrize("ilv", ["0", "1"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T,C", [(100, 12), (61, 7), (130, 64), (64, 64)])
+def test_interleave_variants(m2rnn, oracle_mod, monkeypatch, ilv, dtype, T, C):
+    """Both backward variants: the interval recompute of the next interval
+    either runs alone (0) or alongside the sub-interval recompute (1).
+    C = 12 and 7 are not multiples of the sub-interval length, and the
+    ragged last interval leaves part of the next interval's recompute to run
+    after its sub-intervals."""
+    monkeypatch.setenv("M2RNN_BWD_ILV", ilv)
+    x = make_inputs(2, T, 3, 64, 16, dtype, 300 + T + C, with_dy=True)
+    gen = torch.Generator().manual_seed(C)
+    H0 = torch.rand(2, 3, 64, 16, generator=gen) - 0.5
+    dHT = torch.randn(2, 3, 64, 16, generator=gen)
+    _restart_parity(m2rnn, oracle_mod, x, C, H0=H0, dHT=dHT, label=f"ilv{ilv} {dtype} T{T} C{C}")
