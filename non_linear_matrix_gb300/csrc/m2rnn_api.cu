@@ -275,18 +275,26 @@ int bwd_interval(const m2rnn_shape* s, bool ckpt_given, bool* own_ckpt) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Picks warps per CTA (16 rows each) and the interleaved variant for the
-// fewest waves; ties go to the interleaved variant, then to more rows per CTA
-// (fewer cross-CTA reductions).  M2RNN_BWD_ILV=0 or 1 restricts the variant.
+// Picks warps per CTA (16 rows each) and the interleaving mode for the
+// fewest waves; ties go to interleaving, then to more rows per CTA (fewer
+// cross-CTA reductions).  M2RNN_BWD_ILV=0, 1 or 2 forces the mode.
 bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
+  constexpr int kDefaultIlv = 2;
   const int mtiles = p.K / 16;
-  const char* env = std::getenv("M2RNN_BWD_ILV");
-  const int force = env != nullptr ? std::atoi(env) : -1;
+  int modes[2] = {kDefaultIlv, 0}, nmodes = 2;
+  if (const char* env = std::getenv("M2RNN_BWD_ILV")) {
+    modes[0] = std::atoi(env);
+    nmodes = 1;
+    if (modes[0] < 0 || modes[0] > 2) return false;
+  }
+  if (!m2rnn::bwd_has_ilv(V)) {
+    modes[0] = 0;
+    nmodes = 1;
+  }
   int best_w = 0, best_ilv = 0;
   long long best_waves = 0;
-  for (int ilv = 1; ilv >= 0; --ilv) {
-    if (ilv == 1 && (!m2rnn::bwd_has_ilv(V) || force == 0)) continue;
-    if (ilv == 0 && force == 1 && m2rnn::bwd_has_ilv(V)) continue;
+  for (int mi = 0; mi < nmodes; ++mi) {
+    const int ilv = modes[mi];
     for (int w = mtiles < 8 ? mtiles : 8; w >= 1; w /= 2) {
       if (mtiles % w != 0) continue;
       if (m2rnn::bwd_smem_bytes(V, p.C, p.S2, w, f32, ilv != 0) > kSmemBudget) continue;

@@ -232,7 +232,7 @@ __device__ __forceinline__ void recompute_step(float (&H)[V / 8][4], uint32_t (&
   if (F32) pack_frag_lo<V>(H, A, Al);
 }
 
-template <int V, bool F32, bool ILV>
+template <int V, bool F32, int ILV>
 __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   using TIn = typename InT<F32>::T;
   constexpr int es = sizeof(TIn);
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   const int b = bn / N, n = bn % N;
   const int row0c = slice * RS;            // first row of this CTA
   const int row0 = row0c + 16 * warp;      // first row of this warp
-  const BwdLayout L = bwd_layout(V, C, S2, WPC, es, ILV);
+  const BwdLayout L = bwd_layout(V, C, S2, WPC, es, ILV != 0);
   const uint32_t sb = ptx::smem_addr(smem);
 
   const TIn* q = static_cast<const TIn*>(p.q);
@@ -447,20 +447,21 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
       // S2 recompute steps (steps past Ls run on buffer padding and are not
       // used), interleaved with S2 steps of the interval recompute of ci - 1
       const int m0 = (nsub - 1 - j) * S2;
+      // one step of the interval recompute of ci - 1 (sub-checkpoint first)
+      auto l1_step = [&](int mi) {
+        if (mi == 0) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            ptx::sts_f32x4(subck_slot(nbuf, m0 / S2, nt), H1[nt][0], H1[nt][1], H1[nt][2], H1[nt][3]);
+        }
+        float k0, k1, fg, Sd[NT][4], Ed[NT][4];
+        float2 vv[NT];
+        step_in(nbuf, m0 + mi, k0, k1, vv, fg);
+        recompute_step<V, F32>(H1, A1, Al1, Bw, Bwl, k0, k1, vv, fg, Sd, Ed);
+      };
 #pragma unroll
       for (int i = 0; i < S2; ++i) {
-        if constexpr (ILV) {
-          if (i == 0) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              ptx::sts_f32x4(subck_slot(nbuf, m0 / S2, nt), H1[nt][0], H1[nt][1], H1[nt][2],
-                             H1[nt][3]);
-          }
-          float k0, k1, fg, Sd[NT][4], Ed[NT][4];
-          float2 vv[NT];
-          step_in(nbuf, m0 + i, k0, k1, vv, fg);
-          recompute_step<V, F32>(H1, A1, Al1, Bw, Bwl, k0, k1, vv, fg, Sd, Ed);
-        }
+        if constexpr (ILV == 1) l1_step(i);
         float k0, k1, fg, Ed[NT][4];
         float2 vv[NT];
         step_in(buf, s0 + i, k0, k1, vv, fg);
@@ -490,6 +491,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
         constexpr bool FULL = decltype(full_tag)::value;
 #pragma unroll
         for (int i = S2 - 1; i >= 0; --i) {
+          if constexpr (ILV == 2) l1_step(S2 - 1 - i);
           if (FULL || i < Ls) {
             const int s = s0 + i;
             const uint32_t qrow = sb + L.in_q + static_cast<uint32_t>(s * RS * es) + kq_row;
@@ -667,7 +669,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
     }
     // the interval recompute of ci - 1 past what ran alongside (when this
     // interval is the shorter, ragged last one)
-    if (ILV && ci > 0 && nsub * S2 < C) interval_recompute(nbuf, nsub * S2, C, H1, A1, Al1);
+    if (ILV != 0 && ci > 0 && nsub * S2 < C) interval_recompute(nbuf, nsub * S2, C, H1, A1, Al1);
     // C now holds dL/dH_{t0}: the gradient of this interval's checkpoint.
     if (p.dckpt != nullptr && ci % p.dck_ratio == 0) {
       float* dst = p.dckpt + ((static_cast<size_t>(b) * N + n) * p.dck_n + ci / p.dck_ratio) * K * V;
@@ -715,9 +717,9 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   if (slice == 0) red_add(p.dw_r + static_cast<size_t>(n) * V + tid % V, dwr_acc);
 }
 
-template <int V, bool F32, bool ILV>
+template <int V, bool F32, int ILV>
 cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
-  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2, ILV);
+  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2, ILV != 0);
   auto kern = bwd_kernel<V, F32, ILV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L.total));
@@ -727,9 +729,9 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int V, bool F32, bool ILV>
+template <int V, bool F32, int ILV>
 int bwd_ctas_per_sm_t(const BwdParams& p) {
-  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2, ILV);
+  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2, ILV != 0);
   auto kern = bwd_kernel<V, F32, ILV>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(L.total)) != cudaSuccess)
@@ -753,25 +755,38 @@ size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs, bool ilv) 
   return bwd_layout(V, C, S2, WPC, f32_inputs ? 4 : 2, ilv).total;
 }
 
-int bwd_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs) {
-  if (V == 16) {
-    if (p.ilv) return f32_inputs ? bwd_ctas_per_sm_t<16, true, true>(p) : bwd_ctas_per_sm_t<16, false, true>(p);
-    return f32_inputs ? bwd_ctas_per_sm_t<16, true, false>(p) : bwd_ctas_per_sm_t<16, false, false>(p);
+template <bool F32>
+int bwd_ctas_per_sm_16(const BwdParams& p) {
+  switch (p.ilv) {
+    case 0: return bwd_ctas_per_sm_t<16, F32, 0>(p);
+    case 1: return bwd_ctas_per_sm_t<16, F32, 1>(p);
+    case 2: return bwd_ctas_per_sm_t<16, F32, 2>(p);
   }
-  if (p.ilv) return 0;
-  return f32_inputs ? bwd_ctas_per_sm_t<32, true, false>(p) : bwd_ctas_per_sm_t<32, false, false>(p);
+  return 0;
+}
+
+int bwd_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs) {
+  if (V == 16) return f32_inputs ? bwd_ctas_per_sm_16<true>(p) : bwd_ctas_per_sm_16<false>(p);
+  if (p.ilv != 0) return 0;
+  return f32_inputs ? bwd_ctas_per_sm_t<32, true, 0>(p) : bwd_ctas_per_sm_t<32, false, 0>(p);
+}
+
+template <bool F32>
+cudaError_t launch_bwd_16(const BwdParams& p, cudaStream_t stream) {
+  switch (p.ilv) {
+    case 0: return launch_bwd_t<16, F32, 0>(p, stream);
+    case 1: return launch_bwd_t<16, F32, 1>(p, stream);
+    case 2: return launch_bwd_t<16, F32, 2>(p, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream) {
   if (p.WPC < 1 || p.WPC > 8 || p.S2 != bwd_sub_len(V, f32_inputs)) return cudaErrorInvalidValue;
-  if (p.ilv && !bwd_has_ilv(V)) return cudaErrorInvalidValue;
-  if (V == 16) {
-    if (p.ilv)
-      return f32_inputs ? launch_bwd_t<16, true, true>(p, stream) : launch_bwd_t<16, false, true>(p, stream);
-    return f32_inputs ? launch_bwd_t<16, true, false>(p, stream) : launch_bwd_t<16, false, false>(p, stream);
-  }
+  if (p.ilv < 0 || p.ilv > 2 || (p.ilv != 0 && !bwd_has_ilv(V))) return cudaErrorInvalidValue;
+  if (V == 16) return f32_inputs ? launch_bwd_16<true>(p, stream) : launch_bwd_16<false>(p, stream);
   if (V == 32)
-    return f32_inputs ? launch_bwd_t<32, true, false>(p, stream) : launch_bwd_t<32, false, false>(p, stream);
+    return f32_inputs ? launch_bwd_t<32, true, 0>(p, stream) : launch_bwd_t<32, false, 0>(p, stream);
   return cudaErrorInvalidValue;
 }
 
