@@ -275,19 +275,18 @@ int bwd_interval(const m2rnn_shape* s, bool ckpt_given, bool* own_ckpt) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Picks warps per CTA (16 rows each) and the interleaving mode for the
-// fewest waves; ties go to interleaving, then to more rows per CTA (fewer
-// cross-CTA reductions).  M2RNN_BWD_ILV=0, 1 or 2 forces the mode.
+// Picks the kernel variant and warps per CTA (16 rows each) for the fewest
+// waves; ties go to the earlier variant in the list, then to more rows per
+// CTA (fewer cross-CTA reductions).  M2RNN_BWD_ILV=0..3 forces the variant.
 bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
-  constexpr int kDefaultIlv = 2;
   const int mtiles = p.K / 16;
-  int modes[2] = {kDefaultIlv, 0}, nmodes = 2;
+  int modes[3] = {3, 0, 0}, nmodes = 2;
   if (const char* env = std::getenv("M2RNN_BWD_ILV")) {
     modes[0] = std::atoi(env);
     nmodes = 1;
-    if (modes[0] < 0 || modes[0] > 2) return false;
+    if (modes[0] < 0 || modes[0] > 3) return false;
   }
-  if (!m2rnn::bwd_has_ilv(V)) {
+  if (!m2rnn::bwd_has_ilv(V) && !m2rnn::bwd_has_pipe(V)) {
     modes[0] = 0;
     nmodes = 1;
   }
@@ -297,12 +296,14 @@ bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
     const int ilv = modes[mi];
     for (int w = mtiles < 8 ? mtiles : 8; w >= 1; w /= 2) {
       if (mtiles % w != 0) continue;
-      if (m2rnn::bwd_smem_bytes(V, p.C, p.S2, w, f32, ilv != 0) > kSmemBudget) continue;
+      const size_t smem = ilv == 3 ? m2rnn::bwd_pipe_smem_bytes(V, p.C, w, f32)
+                                   : m2rnn::bwd_smem_bytes(V, p.C, p.S2, w, f32, ilv != 0);
+      if (smem > kSmemBudget) continue;
       m2rnn::BwdParams q = p;
       q.WPC = w;
       q.nslices = mtiles / w;
       q.ilv = ilv;
-      const int R = m2rnn::bwd_ctas_per_sm(q, V, f32);
+      const int R = ilv == 3 ? m2rnn::bwd_pipe_ctas_per_sm(q, V, f32) : m2rnn::bwd_ctas_per_sm(q, V, f32);
       if (R <= 0) continue;
       const long long ctas = static_cast<long long>(p.B) * p.N * q.nslices;
       const long long waves =
@@ -497,7 +498,8 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
                         cudaMemsetAsync(df, 0, BT * s->N * sizeof(float), st) != cudaSuccess))
     return M2RNN_ERR_CUDA;
   (void)es;
-  return status_from_cuda(m2rnn::launch_bwd(p, s->V, f32, st));
+  return status_from_cuda(p.ilv == 3 ? m2rnn::launch_bwd_pipe(p, s->V, f32, st)
+                                     : m2rnn::launch_bwd(p, s->V, f32, st));
 }
 
 }  // extern "C"

@@ -112,6 +112,11 @@ __device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
                : "r"(addr));
   return v;
 }
+__device__ __forceinline__ uint2 lds_u32x2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint4 lds_u32x4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -129,6 +134,21 @@ __device__ __forceinline__ void sts_f32(uint32_t addr, float a) {
 }
 __device__ __forceinline__ void sts_f32x2(uint32_t addr, float a, float b) {
   asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t a) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
+}
+// Stores only where pred is non-zero (a predicated store, no branch).
+__device__ __forceinline__ void sts_f32x2_if(int pred, uint32_t addr, float a, float b) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.s32 p, %0, 0;\n\t@p st.shared.v2.f32 [%1], {%2, %3};\n\t}"
+      ::"r"(pred), "r"(addr), "f"(a), "f"(b)
+      : "memory");
+}
+__device__ __forceinline__ void sts_f32_if(int pred, uint32_t addr, float a) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.s32 p, %0, 0;\n\t@p st.shared.f32 [%1], %2;\n\t}"
+               ::"r"(pred), "r"(addr), "f"(a)
+               : "memory");
 }
 
 // ---- time -------------------------------------------------------------------
@@ -191,6 +211,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
 
 // Global -> shared bulk copy; completion is signalled on `bar` as transaction
 // bytes.  dst, src and bytes must be multiples of 16.
+// Per-thread asynchronous global -> shared copies (cp.async; completion by
+// cp.async.wait_all, which the hardware guarantees to end).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                          uint32_t bar) {
   asm volatile(

@@ -200,13 +200,13 @@ def test_workload_fwd_bwd(m2rnn, oracle_mod):
     _restart_parity(m2rnn, oracle_mod, x, w.ckpt_every, label=w.name)
 
 
-@pytest.mark.parametrize("ilv", ["0", "1", "2"])
+@pytest.mark.parametrize("ilv", ["0", "1", "2", "3"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("T,C", [(100, 12), (61, 7), (130, 64), (64, 64)])
 def test_interleave_variants(m2rnn, oracle_mod, monkeypatch, ilv, dtype, T, C):
     """All backward variants: the interval recompute of the next interval
     runs alone (0), alongside the sub-interval recompute (1) or alongside
-    the reverse steps (2).
+    the reverse steps (2), or the pipelined kernel runs (3).
     C = 12 and 7 are not multiples of the sub-interval length, and the
     ragged last interval leaves part of the next interval's recompute to run
     after its sub-intervals."""
