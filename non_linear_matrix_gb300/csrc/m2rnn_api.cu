@@ -277,7 +277,8 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Picks the kernel variant and warps per CTA (16 rows each) for the fewest
 // waves; ties go to the earlier variant in the list, then to more rows per
-// CTA (fewer cross-CTA reductions).  M2RNN_BWD_ILV=0..3 forces the variant.
+// CTA (fewer cross-CTA reductions).  M2RNN_BWD_ILV=0..3 forces the variant,
+// M2RNN_BWD_WPC the warps per CTA.
 bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
   const int mtiles = p.K / 16;
   int modes[3] = {3, 0, 0}, nmodes = 2;
@@ -290,12 +291,14 @@ bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
     modes[0] = 0;
     nmodes = 1;
   }
+  int force_w = 0;  // M2RNN_BWD_WPC=1/2/4/8 forces the warps per CTA
+  if (const char* env = std::getenv("M2RNN_BWD_WPC")) force_w = std::atoi(env);
   int best_w = 0, best_ilv = 0;
   long long best_waves = 0;
   for (int mi = 0; mi < nmodes; ++mi) {
     const int ilv = modes[mi];
     for (int w = mtiles < 8 ? mtiles : 8; w >= 1; w /= 2) {
-      if (mtiles % w != 0) continue;
+      if (mtiles % w != 0 || (force_w > 0 && w != force_w)) continue;
       const size_t smem = ilv == 3 ? m2rnn::bwd_pipe_smem_bytes(V, p.C, w, f32)
                                    : m2rnn::bwd_smem_bytes(V, p.C, p.S2, w, f32, ilv != 0);
       if (smem > kSmemBudget) continue;

@@ -50,9 +50,9 @@ namespace {
 
 using namespace bwdc;
 
-// Shared-memory layout (byte offsets).
+// Shared-memory layout (byte offsets).  Everything but the sub-checkpoint
+// region, which comes last, is fixed by (V, S2, WPC, input size).
 struct PipeLayout {
-  uint32_t subck;  // [NS1][WPC][NT][32 lanes][4] fp32; dW partials at the end
   uint32_t buf0;   // two input buffers at buf0 + k * bufsz
   uint32_t bufsz;
   // inside an input buffer: the reversed sub-interval ...
@@ -71,18 +71,14 @@ struct PipeLayout {
   uint32_t r_dq, r_dk;  // [2][S2][WPC][8 g][2 h] fp32 per-step partials (row 16w + 8h + g)
   uint32_t r_dv;        // [2][S2][WPC][KS][8 g][2 h] fp32 (column 16ks + 8h + g)
   uint32_t r_df;        // [2][S2][WPC] fp32
-  uint32_t total;
+  uint32_t subck;       // [NS1][WPC][NT][32 lanes][4] fp32; dW partials at the end
 };
 
-__host__ __device__ inline uint32_t al128(uint32_t x) { return (x + 127u) / 128u * 128u; }
+__host__ __device__ constexpr uint32_t al128(uint32_t x) { return (x + 127u) / 128u * 128u; }
 
-__host__ __device__ inline PipeLayout pipe_layout(int V, int C, int S2, int WPC, int es) {
-  const uint32_t NT = V / 8, KS = V / 16, NS1 = (C + S2 - 1) / S2;
-  PipeLayout L;
-  uint32_t o = 0;
-  L.subck = o;
-  const uint32_t sub = NS1 * WPC * NT * 512, dws = WPC * V * V * 4;
-  o = al128(o + (sub > dws ? sub : dws));
+__host__ __device__ constexpr PipeLayout pipe_layout(int V, int S2, int WPC, int es) {
+  const uint32_t NT = V / 8, KS = V / 16;
+  PipeLayout L{};
   uint32_t b = 0;
   L.kd = b;
   b = al128(b + WPC * S2 * 8 * 16);
@@ -107,6 +103,7 @@ __host__ __device__ inline PipeLayout pipe_layout(int V, int C, int S2, int WPC,
   L.lfr = b;
   b = al128(b + S2 * 4);
   L.bufsz = b;
+  uint32_t o = 0;
   L.buf0 = o;
   o += 2 * b;
   L.raw = o;
@@ -119,8 +116,13 @@ __host__ __device__ inline PipeLayout pipe_layout(int V, int C, int S2, int WPC,
   o = al128(o + 2 * S2 * WPC * KS * 8 * 8);
   L.r_df = o;
   o = al128(o + 2 * S2 * WPC * 4);
-  L.total = o;
+  L.subck = o;
   return L;
+}
+__host__ __device__ constexpr uint32_t pipe_smem_total(int V, int C, int S2, int WPC, int es) {
+  const uint32_t NS1 = (C + S2 - 1) / S2;
+  const uint32_t sub = NS1 * WPC * (V / 8) * 512, dws = WPC * V * V * 4;
+  return pipe_layout(V, S2, WPC, es).subck + al128(sub > dws ? sub : dws);
 }
 
 // One forward step with the forward kernel's operations (rank-1 k v^T in fp32
@@ -209,8 +211,8 @@ __device__ __forceinline__ int step_of_lane(int lane) {
   return idx;
 }
 
-template <int V, bool F32>
-__global__ void __launch_bounds__(256) bwd_pipe_kernel(const BwdParams p) {
+template <int V, bool F32, int WPC>
+__global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
   using TIn = typename InT<F32>::T;
   constexpr int es = sizeof(TIn);
   constexpr int NT = V / 8, KS = V / 16;
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(256) bwd_pipe_kernel(const BwdParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int WPC = p.WPC, RS = 16 * WPC, nthr = 32 * WPC;
+  constexpr int RS = 16 * WPC, nthr = 32 * WPC;
   const int K = p.K, T = p.T, N = p.N, C = p.C, nck = p.nck;
   const int NS1 = (C + S2 - 1) / S2;
   const int slice = blockIdx.x % p.nslices;
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(256) bwd_pipe_kernel(const BwdParams p) {
   const int b = bn / N, n = bn % N;
   const int row0c = slice * RS;        // first row of this CTA
   const int row0 = row0c + 16 * warp;  // first row of this warp
-  const PipeLayout L = pipe_layout(V, C, S2, WPC, es);
+  constexpr PipeLayout L = pipe_layout(V, S2, WPC, es);
   const uint32_t sb = ptx::smem_addr(smem);
 
   const TIn* q = static_cast<const TIn*>(p.q);
@@ -363,9 +365,12 @@ __global__ void __launch_bounds__(256) bwd_pipe_kernel(const BwdParams p) {
   const uint32_t rsrc = static_cast<uint32_t>((i_r * RS + r0) * es);
   const uint32_t rkind = static_cast<uint32_t>(S2 * RS * es);  // raw bytes per row kind
   const uint32_t fl_off = static_cast<uint32_t>(((i_r * WPC + rw) * 8 + rg) * 8 + rh * 4);
+  // column items on warp 1, f on warp 2, df on warp 3 (where they exist)
+  constexpr int col_base = WPC >= 2 ? 32 : 0, f_base = WPC >= 3 ? 64 : 0, df_base = WPC >= 4 ? 96 : 0;
   constexpr int vq4 = V / 4;
-  const bool col_ok = tid < S2 * vq4;
-  const int i_c = tid / vq4, j0c = 4 * (tid % vq4);
+  const int ct = tid - col_base, ft = tid - f_base, dt = tid - df_base;
+  const bool col_ok = ct >= 0 && ct < S2 * vq4;
+  const int i_c = ct / vq4, j0c = 4 * (ct % vq4);
   const uint32_t csrc = static_cast<uint32_t>(3 * S2 * RS * es + (i_c * V + j0c) * es);
 
   auto issue = [&](int ci2, int jj2, bool wantR) {
@@ -383,12 +388,12 @@ __global__ void __launch_bounds__(256) bwd_pipe_kernel(const BwdParams p) {
       ptx::cp_async16(raw + static_cast<uint32_t>((tid + u * nthr) * 16),
                       reinterpret_cast<const uint4*>(src) + x);
     }
-    if (tid < 2 * S2) {  // f of R (tid < S2) and of L: the aligned 32-bit word that holds it
-      const bool isR = tid < S2;
-      const int i = isR ? tid : tid - S2;
+    if (ft >= 0 && ft < 2 * S2) {  // f of R (ft < S2) and of L: the aligned 32-bit word holding it
+      const bool isR = ft < S2;
+      const int i = isR ? ft : ft - S2;
       if (i < (isR ? sr.nR : sr.nL)) {
         const size_t idx = ((isR ? sr.tR : sr.tL) + i) * N + n;
-        const uint32_t dst = raw_f + 4 * tid;
+        const uint32_t dst = raw_f + 4 * ft;
         if (es == 4 || (idx | 1) < f_total) {
           ptx::cp_async4(dst, fin + (es == 4 ? idx : (idx & ~static_cast<size_t>(1))));
         } else {  // the last element of an odd-length bf16 array: its word would overrun
@@ -457,11 +462,11 @@ __global__ void __launch_bounds__(256) bwd_pipe_kernel(const BwdParams p) {
         }
       }
     }
-    if (tid < 2 * S2) {
-      const bool isR = tid < S2;
-      const int i = isR ? tid : tid - S2;
+    if (ft >= 0 && ft < 2 * S2) {
+      const bool isR = ft < S2;
+      const int i = isR ? ft : ft - S2;
       if (wantR || !isR) {
-        const uint32_t wbits = ptx::lds_u32(raw_f + 4 * tid);
+        const uint32_t wbits = ptx::lds_u32(raw_f + 4 * ft);
         float fv;
         if constexpr (F32) {
           fv = __uint_as_float(wbits);
@@ -763,6 +768,7 @@ __global__ void __launch_bounds__(256) bwd_pipe_kernel(const BwdParams p) {
         const int i = e / V, jc = e - i * V;
         const int mj = jc >> 4, hh = (jc >> 3) & 1, gg = jc & 7;
         float acc = 0.f;
+#pragma unroll
         for (int w = 0; w < WPC; ++w)
           acc += ptx::lds_f32(rv + static_cast<uint32_t>((((i * WPC + w) * KS + mj) * 8 + gg) * 8 + hh * 4));
         const uint32_t fo = static_cast<uint32_t>(((i * 4 + ((jc & 7) >> 1)) * NT + (jc >> 3)) * 8 + (jc & 1) * 4);
@@ -775,8 +781,10 @@ __global__ void __launch_bounds__(256) bwd_pipe_kernel(const BwdParams p) {
           red_add(dst, slice == 0 ? fmaf(tof(wr[jc]), uu, acc) : acc);
         if (slice == 0) dwr_acc = fmaf(uu, vv, dwr_acc);  // e % V == tid % V throughout
       }
-      for (int i = tid; i < Ls; i += nthr) {
+      if (dt >= 0 && dt < Ls) {
+        const int i = dt;
         float acc = 0.f;
+#pragma unroll
         for (int w = 0; w < WPC; ++w) acc += ptx::lds_f32(rf + static_cast<uint32_t>((i * WPC + w) * 4));
         float* dst = p.df + (bt + i) * N + n;
         if (p.nslices == 1)
@@ -847,29 +855,51 @@ __global__ void __launch_bounds__(256) bwd_pipe_kernel(const BwdParams p) {
   if (slice == 0) red_add(p.dw_r + static_cast<size_t>(n) * V + tid % V, dwr_acc);
 }
 
-template <int V, bool F32>
+template <int V, bool F32, int WPC>
 cudaError_t launch_pipe_t(const BwdParams& p, cudaStream_t stream) {
-  const PipeLayout L = pipe_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2);
-  auto kern = bwd_pipe_kernel<V, F32>;
+  const uint32_t smem = pipe_smem_total(V, p.C, sub_len<V, F32>(), WPC, F32 ? 4 : 2);
+  auto kern = bwd_pipe_kernel<V, F32, WPC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(L.total));
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.B) * p.N * p.nslices;
-  kern<<<grid, 32 * p.WPC, L.total, stream>>>(p);
+  kern<<<grid, 32 * WPC, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int V, bool F32>
+template <int V, bool F32, int WPC>
 int pipe_ctas_per_sm_t(const BwdParams& p) {
-  const PipeLayout L = pipe_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2);
-  auto kern = bwd_pipe_kernel<V, F32>;
+  const uint32_t smem = pipe_smem_total(V, p.C, sub_len<V, F32>(), WPC, F32 ? 4 : 2);
+  auto kern = bwd_pipe_kernel<V, F32, WPC>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(L.total)) != cudaSuccess)
+                           static_cast<int>(smem)) != cudaSuccess)
     return 0;
   int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, 32 * p.WPC, L.total) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, 32 * WPC, smem) != cudaSuccess)
     return 0;
   return nb;
+}
+
+template <bool F32>
+int pipe_ctas_per_sm_w(const BwdParams& p) {
+  switch (p.WPC) {
+    case 1: return pipe_ctas_per_sm_t<16, F32, 1>(p);
+    case 2: return pipe_ctas_per_sm_t<16, F32, 2>(p);
+    case 4: return pipe_ctas_per_sm_t<16, F32, 4>(p);
+    case 8: return pipe_ctas_per_sm_t<16, F32, 8>(p);
+  }
+  return 0;
+}
+
+template <bool F32>
+cudaError_t launch_pipe_w(const BwdParams& p, cudaStream_t stream) {
+  switch (p.WPC) {
+    case 1: return launch_pipe_t<16, F32, 1>(p, stream);
+    case 2: return launch_pipe_t<16, F32, 2>(p, stream);
+    case 4: return launch_pipe_t<16, F32, 4>(p, stream);
+    case 8: return launch_pipe_t<16, F32, 8>(p, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -877,18 +907,17 @@ int pipe_ctas_per_sm_t(const BwdParams& p) {
 bool bwd_has_pipe(int V) { return V == 16; }
 
 size_t bwd_pipe_smem_bytes(int V, int C, int WPC, bool f32_inputs) {
-  return pipe_layout(V, C, bwd_sub_len(V, f32_inputs), WPC, f32_inputs ? 4 : 2).total;
+  return pipe_smem_total(V, C, bwd_sub_len(V, f32_inputs), WPC, f32_inputs ? 4 : 2);
 }
 
 int bwd_pipe_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs) {
   if (V != 16) return 0;
-  return f32_inputs ? pipe_ctas_per_sm_t<16, true>(p) : pipe_ctas_per_sm_t<16, false>(p);
+  return f32_inputs ? pipe_ctas_per_sm_w<true>(p) : pipe_ctas_per_sm_w<false>(p);
 }
 
 cudaError_t launch_bwd_pipe(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream) {
-  if (V != 16 || p.WPC < 1 || p.WPC > 8 || p.S2 != bwd_sub_len(V, f32_inputs))
-    return cudaErrorInvalidValue;
-  return f32_inputs ? launch_pipe_t<16, true>(p, stream) : launch_pipe_t<16, false>(p, stream);
+  if (V != 16 || p.S2 != bwd_sub_len(V, f32_inputs)) return cudaErrorInvalidValue;
+  return f32_inputs ? launch_pipe_w<true>(p, stream) : launch_pipe_w<false>(p, stream);
 }
 
 }  // namespace m2rnn
