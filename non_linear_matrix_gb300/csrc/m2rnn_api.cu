@@ -275,45 +275,46 @@ int bwd_interval(const m2rnn_shape* s, bool ckpt_given, bool* own_ckpt) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Picks the kernel variant and warps per CTA (16 rows each) for the fewest
-// waves; ties go to the earlier variant in the list, then to more rows per
-// CTA (fewer cross-CTA reductions).  M2RNN_BWD_ILV=0..3 forces the variant,
+// Picks the kernel (pipelined where it exists for V, else serial) and the
+// warps per CTA (16 rows each) for the fewest waves; ties go to the
+// pipelined kernel, then to more rows per CTA (fewer cross-CTA reductions).
+// M2RNN_BWD_KERNEL=0 (serial) or 1 (pipelined) forces the kernel and
 // M2RNN_BWD_WPC the warps per CTA.
 bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
   const int mtiles = p.K / 16;
-  int modes[3] = {3, 0, 0}, nmodes = 2;
-  if (const char* env = std::getenv("M2RNN_BWD_ILV")) {
-    modes[0] = std::atoi(env);
-    nmodes = 1;
-    if (modes[0] < 0 || modes[0] > 3) return false;
+  int kinds[2] = {1, 0}, nkinds = 2;
+  if (const char* env = std::getenv("M2RNN_BWD_KERNEL")) {
+    kinds[0] = std::atoi(env);
+    nkinds = 1;
+    if (kinds[0] != 0 && kinds[0] != 1) return false;
   }
-  if (!m2rnn::bwd_has_ilv(V) && !m2rnn::bwd_has_pipe(V)) {
-    modes[0] = 0;
-    nmodes = 1;
+  if (!m2rnn::bwd_has_pipe(V)) {
+    kinds[0] = 0;
+    nkinds = 1;
   }
-  int force_w = 0;  // M2RNN_BWD_WPC=1/2/4/8 forces the warps per CTA
+  int force_w = 0;
   if (const char* env = std::getenv("M2RNN_BWD_WPC")) force_w = std::atoi(env);
-  int best_w = 0, best_ilv = 0;
+  int best_w = 0, best_pipe = 0;
   long long best_waves = 0;
-  for (int mi = 0; mi < nmodes; ++mi) {
-    const int ilv = modes[mi];
+  for (int ki = 0; ki < nkinds; ++ki) {
+    const int pipe = kinds[ki];
     for (int w = mtiles < 8 ? mtiles : 8; w >= 1; w /= 2) {
       if (mtiles % w != 0 || (force_w > 0 && w != force_w)) continue;
-      const size_t smem = ilv == 3 ? m2rnn::bwd_pipe_smem_bytes(V, p.C, w, f32)
-                                   : m2rnn::bwd_smem_bytes(V, p.C, p.S2, w, f32, ilv != 0);
+      const size_t smem = pipe ? m2rnn::bwd_pipe_smem_bytes(V, p.C, w, f32)
+                               : m2rnn::bwd_smem_bytes(V, p.C, p.S2, w, f32);
       if (smem > kSmemBudget) continue;
       m2rnn::BwdParams q = p;
       q.WPC = w;
       q.nslices = mtiles / w;
-      q.ilv = ilv;
-      const int R = ilv == 3 ? m2rnn::bwd_pipe_ctas_per_sm(q, V, f32) : m2rnn::bwd_ctas_per_sm(q, V, f32);
+      q.pipe = pipe;
+      const int R = pipe ? m2rnn::bwd_pipe_ctas_per_sm(q, V, f32) : m2rnn::bwd_ctas_per_sm(q, V, f32);
       if (R <= 0) continue;
       const long long ctas = static_cast<long long>(p.B) * p.N * q.nslices;
       const long long waves =
           (ctas + static_cast<long long>(sms) * R - 1) / (static_cast<long long>(sms) * R);
       if (best_w == 0 || waves < best_waves) {
         best_w = w;
-        best_ilv = ilv;
+        best_pipe = pipe;
         best_waves = waves;
       }
     }
@@ -321,7 +322,7 @@ bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
   if (best_w == 0) return false;
   p.WPC = best_w;
   p.nslices = mtiles / best_w;
-  p.ilv = best_ilv;
+  p.pipe = best_pipe;
   return true;
 }
 
@@ -491,7 +492,7 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   p.S2 = m2rnn::bwd_sub_len(s->V, f32);
   p.WPC = 1;
   p.nslices = s->K / 16;
-  p.ilv = 0;
+  p.pipe = 0;
   if (!choose_bwd(p, s->V, f32, sms)) return M2RNN_ERR_UNSUPPORTED_SHAPE;
   const size_t BT = static_cast<size_t>(s->B) * s->T;
   if (cudaMemsetAsync(dq, 0, BT * s->K * sizeof(float), st) != cudaSuccess ||
@@ -501,8 +502,8 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
                         cudaMemsetAsync(df, 0, BT * s->N * sizeof(float), st) != cudaSuccess))
     return M2RNN_ERR_CUDA;
   (void)es;
-  return status_from_cuda(p.ilv == 3 ? m2rnn::launch_bwd_pipe(p, s->V, f32, st)
-                                     : m2rnn::launch_bwd(p, s->V, f32, st));
+  return status_from_cuda(p.pipe ? m2rnn::launch_bwd_pipe(p, s->V, f32, st)
+                                : m2rnn::launch_bwd(p, s->V, f32, st));
 }
 
 }  // extern "C"

@@ -31,6 +31,10 @@
 // lane-contiguously (no bank conflicts).  The recomputation performs the
 // same operations as the forward kernel, so it reproduces its trajectory.
 // Synchronisation is __syncthreads only (no spin waits).
+//
+// This is the serial variant: the three passes run one after the other in
+// each warp.  m2rnn_bwd_pipe.cu holds the pipelined variant used for V = 16;
+// this one serves V = 32 and any shape the other does not fit.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -63,11 +67,11 @@ struct BwdLayout {
 
 __host__ __device__ inline uint32_t al(uint32_t x) { return (x + 127u) / 128u * 128u; }
 
-__host__ __device__ inline BwdLayout bwd_layout(int V, int C, int S2, int WPC, int es, bool ilv) {
+__host__ __device__ inline BwdLayout bwd_layout(int V, int C, int S2, int WPC, int es) {
   // Step buffers hold NS1 * S2 >= C steps: recompute steps past the end of
   // an interval read the padding and their results are discarded.
   const uint32_t RS = 16 * WPC, NT = V / 8, NS1 = (C + S2 - 1) / S2, CP = NS1 * S2;
-  const uint32_t nb = ilv ? 2 : 1;
+  const uint32_t nb = 1;
   BwdLayout L;
   uint32_t o = 0;
   L.in_q = o;
@@ -99,7 +103,7 @@ __host__ __device__ inline BwdLayout bwd_layout(int V, int C, int S2, int WPC, i
   return L;
 }
 
-template <int V, bool F32, int ILV>
+template <int V, bool F32>
 __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   using TIn = typename InT<F32>::T;
   constexpr int es = sizeof(TIn);
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   const int b = bn / N, n = bn % N;
   const int row0c = slice * RS;            // first row of this CTA
   const int row0 = row0c + 16 * warp;      // first row of this warp
-  const BwdLayout L = bwd_layout(V, C, S2, WPC, es, ILV != 0);
+  const BwdLayout L = bwd_layout(V, C, S2, WPC, es);
   const uint32_t sb = ptx::smem_addr(smem);
 
   const TIn* q = static_cast<const TIn*>(p.q);
@@ -248,40 +252,25 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   };
 
   const int nck = p.nck;
-  // state of the interval recompute (of interval ci - 1 while ci is reversed)
+  // state of the interval recompute
   float H1[NT][4];
   uint32_t A1[KS][4], Al1[KS][4];
-  if constexpr (ILV) {
-    const int ci = nck - 1;
-    load_kvf(ci * C, T - ci * C, ci & 1);
-    load_ckpt(ci, H1);
-    __syncthreads();
-    pack_frag<V>(H1, A1);
-    if (F32) pack_frag_lo<V>(H1, A1, Al1);
-    interval_recompute(ci & 1, 0, T - ci * C, H1, A1, Al1);
-  }
 
 #pragma unroll 1
   for (int ci = nck - 1; ci >= 0; --ci) {
     const int t0 = ci * C;
     const int Lc = min(C, T - t0);
-    const int buf = ILV ? (ci & 1) : 0;
-    const int nbuf = buf ^ 1;
+    const int buf = 0;
     // ---- 1. inputs -> shared memory ----
     __syncthreads();
     load_qdy(t0, Lc);
-    if (!ILV) {
-      load_kvf(t0, Lc, 0);
-      load_ckpt(ci, H1);
-    } else if (ci > 0) {  // next interval to be reversed: recomputed alongside this one
-      load_kvf(t0 - C, C, nbuf);
-      load_ckpt(ci - 1, H1);
-    }
+    load_kvf(t0, Lc, 0);
+    load_ckpt(ci, H1);
     __syncthreads();
     pack_frag<V>(H1, A1);
     if (F32) pack_frag_lo<V>(H1, A1, Al1);
-    // ---- 2. (serial variant) recompute the interval, sub-checkpoint every S2 steps ----
-    if (!ILV) interval_recompute(0, 0, Lc, H1, A1, Al1);
+    // ---- 2. recompute the interval, sub-checkpoint every S2 steps ----
+    interval_recompute(0, 0, Lc, H1, A1, Al1);
 
     // ---- 3. sub-intervals, last first ----
     const int nsub = (Lc + S2 - 1) / S2;
@@ -312,23 +301,9 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) Hf[0][ks][e] = A[ks][e];
       // S2 recompute steps (steps past Ls run on buffer padding and are not
-      // used), interleaved with S2 steps of the interval recompute of ci - 1
-      const int m0 = (nsub - 1 - j) * S2;
-      // one step of the interval recompute of ci - 1 (sub-checkpoint first)
-      auto l1_step = [&](int mi) {
-        if (mi == 0) {
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            ptx::sts_f32x4(subck_slot(nbuf, m0 / S2, nt), H1[nt][0], H1[nt][1], H1[nt][2], H1[nt][3]);
-        }
-        float k0, k1, fg, Sd[NT][4], Ed[NT][4];
-        float2 vv[NT];
-        step_in(nbuf, m0 + mi, k0, k1, vv, fg);
-        recompute_step<V, F32>(H1, A1, Al1, Bw, Bwl, k0, k1, vv, fg, Sd, Ed);
-      };
+      // used)
 #pragma unroll
       for (int i = 0; i < S2; ++i) {
-        if constexpr (ILV == 1) l1_step(i);
         float k0, k1, fg, Ed[NT][4];
         float2 vv[NT];
         step_in(buf, s0 + i, k0, k1, vv, fg);
@@ -358,7 +333,6 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
         constexpr bool FULL = decltype(full_tag)::value;
 #pragma unroll
         for (int i = S2 - 1; i >= 0; --i) {
-          if constexpr (ILV == 2) l1_step(S2 - 1 - i);
           if (FULL || i < Ls) {
             const int s = s0 + i;
             const uint32_t qrow = sb + L.in_q + static_cast<uint32_t>(s * RS * es) + kq_row;
@@ -534,9 +508,6 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
         }
       }
     }
-    // the interval recompute of ci - 1 past what ran alongside (when this
-    // interval is the shorter, ragged last one)
-    if (ILV != 0 && ci > 0 && nsub * S2 < C) interval_recompute(nbuf, nsub * S2, C, H1, A1, Al1);
     // C now holds dL/dH_{t0}: the gradient of this interval's checkpoint.
     if (p.dckpt != nullptr && ci % p.dck_ratio == 0) {
       float* dst = p.dckpt + ((static_cast<size_t>(b) * N + n) * p.dck_n + ci / p.dck_ratio) * K * V;
@@ -584,10 +555,10 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   if (slice == 0) red_add(p.dw_r + static_cast<size_t>(n) * V + tid % V, dwr_acc);
 }
 
-template <int V, bool F32, int ILV>
+template <int V, bool F32>
 cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
-  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2, ILV != 0);
-  auto kern = bwd_kernel<V, F32, ILV>;
+  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2);
+  auto kern = bwd_kernel<V, F32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L.total));
   if (e != cudaSuccess) return e;
@@ -596,10 +567,10 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int V, bool F32, int ILV>
+template <int V, bool F32>
 int bwd_ctas_per_sm_t(const BwdParams& p) {
-  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2, ILV != 0);
-  auto kern = bwd_kernel<V, F32, ILV>;
+  const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2);
+  auto kern = bwd_kernel<V, F32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(L.total)) != cudaSuccess)
     return 0;
@@ -616,44 +587,19 @@ int bwd_sub_len(int V, bool f32_inputs) {
   return f32_inputs ? sub_len<32, true>() : sub_len<32, false>();
 }
 
-bool bwd_has_ilv(int V) { return V == 16; }
-
-size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs, bool ilv) {
-  return bwd_layout(V, C, S2, WPC, f32_inputs ? 4 : 2, ilv).total;
-}
-
-template <bool F32>
-int bwd_ctas_per_sm_16(const BwdParams& p) {
-  switch (p.ilv) {
-    case 0: return bwd_ctas_per_sm_t<16, F32, 0>(p);
-    case 1: return bwd_ctas_per_sm_t<16, F32, 1>(p);
-    case 2: return bwd_ctas_per_sm_t<16, F32, 2>(p);
-  }
-  return 0;
+size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs) {
+  return bwd_layout(V, C, S2, WPC, f32_inputs ? 4 : 2).total;
 }
 
 int bwd_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs) {
-  if (V == 16) return f32_inputs ? bwd_ctas_per_sm_16<true>(p) : bwd_ctas_per_sm_16<false>(p);
-  if (p.ilv != 0) return 0;
-  return f32_inputs ? bwd_ctas_per_sm_t<32, true, 0>(p) : bwd_ctas_per_sm_t<32, false, 0>(p);
-}
-
-template <bool F32>
-cudaError_t launch_bwd_16(const BwdParams& p, cudaStream_t stream) {
-  switch (p.ilv) {
-    case 0: return launch_bwd_t<16, F32, 0>(p, stream);
-    case 1: return launch_bwd_t<16, F32, 1>(p, stream);
-    case 2: return launch_bwd_t<16, F32, 2>(p, stream);
-  }
-  return cudaErrorInvalidValue;
+  if (V == 16) return f32_inputs ? bwd_ctas_per_sm_t<16, true>(p) : bwd_ctas_per_sm_t<16, false>(p);
+  return f32_inputs ? bwd_ctas_per_sm_t<32, true>(p) : bwd_ctas_per_sm_t<32, false>(p);
 }
 
 cudaError_t launch_bwd(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream) {
   if (p.WPC < 1 || p.WPC > 8 || p.S2 != bwd_sub_len(V, f32_inputs)) return cudaErrorInvalidValue;
-  if (p.ilv < 0 || p.ilv > 2 || (p.ilv != 0 && !bwd_has_ilv(V))) return cudaErrorInvalidValue;
-  if (V == 16) return f32_inputs ? launch_bwd_16<true>(p, stream) : launch_bwd_16<false>(p, stream);
-  if (V == 32)
-    return f32_inputs ? launch_bwd_t<32, true, 0>(p, stream) : launch_bwd_t<32, false, 0>(p, stream);
+  if (V == 16) return f32_inputs ? launch_bwd_t<16, true>(p, stream) : launch_bwd_t<16, false>(p, stream);
+  if (V == 32) return f32_inputs ? launch_bwd_t<32, true>(p, stream) : launch_bwd_t<32, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -67,18 +67,15 @@ struct BwdParams {
   int WPC;      // warps per CTA (16 rows each)
   int nslices;  // K / (16 * WPC)
   int S2;       // sub-interval length of the recomputation (= bwd_sub_len)
-  int ilv;      // kernel variant: 0 serial interval recompute; 1 / 2 the
-                // recompute of interval c-1 runs alongside the sub-interval
-                // recompute / the reverse steps of c (V = 16); 3 the
-                // pipelined kernel (V = 16, m2rnn_bwd_pipe.cu)
+  int pipe;     // 1: the pipelined kernel (m2rnn_bwd_pipe.cu, V = 16); 0: the
+                // serial one (m2rnn_bwd.cu)
 };
 
 cudaError_t launch_bwd(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream);
 int bwd_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs);
-size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs, bool ilv);
-bool bwd_has_ilv(int V);  // whether the variant has an interleaved build
+size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs);
 
-// Pipelined backward kernel (variant 3).
+// Pipelined backward kernel.
 bool bwd_has_pipe(int V);
 size_t bwd_pipe_smem_bytes(int V, int C, int WPC, bool f32_inputs);
 int bwd_pipe_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs);

@@ -200,22 +200,20 @@ def test_workload_fwd_bwd(m2rnn, oracle_mod):
     _restart_parity(m2rnn, oracle_mod, x, w.ckpt_every, label=w.name)
 
 
-@pytest.mark.parametrize("ilv", ["0", "1", "2", "3"])
+@pytest.mark.parametrize("kernel", ["0", "1"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("T,C", [(100, 12), (61, 7), (130, 64), (64, 64)])
-def test_interleave_variants(m2rnn, oracle_mod, monkeypatch, ilv, dtype, T, C):
-    """All backward variants: the interval recompute of the next interval
-    runs alone (0), alongside the sub-interval recompute (1) or alongside
-    the reverse steps (2), or the pipelined kernel runs (3).
-    C = 12 and 7 are not multiples of the sub-interval length, and the
-    ragged last interval leaves part of the next interval's recompute to run
-    after its sub-intervals."""
-    monkeypatch.setenv("M2RNN_BWD_ILV", ilv)
+def test_kernel_variants(m2rnn, oracle_mod, monkeypatch, kernel, dtype, T, C):
+    """Both backward kernels: serial (0) and pipelined (1).  C = 12 and 7
+    are not multiples of the sub-interval length, and the ragged last
+    interval leaves part of the next interval's recompute to run after its
+    sub-intervals in the pipelined kernel."""
+    monkeypatch.setenv("M2RNN_BWD_KERNEL", kernel)
     x = make_inputs(2, T, 3, 64, 16, dtype, 300 + T + C, with_dy=True)
     gen = torch.Generator().manual_seed(C)
     H0 = torch.rand(2, 3, 64, 16, generator=gen) - 0.5
     dHT = torch.randn(2, 3, 64, 16, generator=gen)
-    _restart_parity(m2rnn, oracle_mod, x, C, H0=H0, dHT=dHT, label=f"ilv{ilv} {dtype} T{T} C{C}")
+    _restart_parity(m2rnn, oracle_mod, x, C, H0=H0, dHT=dHT, label=f"kernel{kernel} {dtype} T{T} C{C}")
 
 
 @pytest.mark.parametrize("wpc", ["1", "2", "4"])
@@ -228,7 +226,7 @@ def test_pipelined_warps_per_cta(m2rnn, oracle_mod, monkeypatch, wpc, dtype):
     1e-3-4e-3 relative perturbation of W -- seed 604 is one -- and then even
     32-step restarts leave tanh-approximation differences near the 1 %
     bound; this draw moves by 0.15 %.)"""
-    monkeypatch.setenv("M2RNN_BWD_ILV", "3")
+    monkeypatch.setenv("M2RNN_BWD_KERNEL", "1")
     monkeypatch.setenv("M2RNN_BWD_WPC", wpc)
     x = make_inputs(2, 150, 3, 64, 16, dtype, 600, with_dy=True)
     gen = torch.Generator().manual_seed(11)
