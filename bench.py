@@ -224,12 +224,13 @@ def run_reference(args, w):
     if rank != 0:
         return
     per_step_budget = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    rate_fn = _oracle_decode_rate if w.decode else _oracle_rate
     for _ in range(args.warmup):
-        _oracle_rate(w, per_step_budget / 4)
+        rate_fn(w, per_step_budget / 4)
     times, th = [], 0.0
     desc, threads = "", 0
     for _ in range(args.steps):
-        rate, desc, threads, dt = _oracle_rate(w, per_step_budget)
+        rate, desc, threads, dt = rate_fn(w, per_step_budget)
         times.append(dt)
         th += rate * dt
     value = th / sum(times)
@@ -333,6 +334,73 @@ class Runner:
         return tot / steps, fw / steps, bw / steps
 
 
+class DecodeRunner:
+    """Single-step decode of B sequences: the state stays in HBM and is
+    updated in place by every step."""
+
+    def __init__(self, w, m2rnn, rank):
+        from non_linear_matrix_gb300.inputs import decode_state, make_inputs
+        self.w, self.m = w, m2rnn
+        seed = rank_seed(w.seed, rank)
+        x = make_inputs(w.B, 1, w.N, w.K, w.V, w.dtype, seed, w.f_mean)
+        self.x = {n: (t[:, 0].contiguous() if n in ("q", "k", "v", "f") else t)
+                  for n, t in x.items()}
+        self.g = {n: t.cuda() for n, t in self.x.items()}
+        self.H = decode_state(w.B, w.N, w.K, w.V, seed).cuda()
+        self.out = {"y": torch.empty_like(self.g["v"])}
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def step(self):
+        g = self.g
+        self.m.decode(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], self.H, H_out=self.H,
+                      y=self.out["y"])
+
+    def timed(self, steps, stream):
+        e0, e1, _ = self.ev
+        e0.record(stream)
+        for _ in range(steps):
+            self.step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        return ms, ms, 0.0
+
+
+def _decode_roofline(w, ms, peaks):
+    """Decode is bound by HBM: the state is read and written once per step."""
+    es = 2 if w.dtype == "bf16" else 4
+    heads = w.B * w.N
+    bytes_step = heads * (2 * w.K * w.V * 4 + 2 * w.V * es + es) + w.B * 2 * w.K * es + \
+        w.N * (w.V * w.V + w.V) * es
+    achieved = bytes_step / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": bytes_step,
+            "peak_basis": ("measured copy bandwidth (MEASURED_PEAKS.json)"
+                           if peaks["source"] == "measured" else "fallback 6.8 TB/s")}
+
+
+def _oracle_decode_rate(w, budget_s: float):
+    """fp64 oracle at T = 1 on a sample of sequences: (units/s, desc, threads)."""
+    import oracle
+    from non_linear_matrix_gb300.inputs import decode_state, make_inputs
+    oracle.build()
+    threads = oracle.threads()
+
+    def run(Bs):
+        x = make_inputs(Bs, 1, w.N, w.K, w.V, w.dtype, w.seed, w.f_mean)
+        H = decode_state(Bs, w.N, w.K, w.V, w.seed)
+        t0 = time.perf_counter()
+        oracle.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], H0=H)
+        return time.perf_counter() - t0
+
+    Bp = min(w.B, 64)
+    rate = Bp * w.N / max(run(Bp), 1e-6)
+    Bs = int(max(1, min(w.B, budget_s * rate / w.N)))
+    dt = run(Bs)
+    desc = f"one decode step of {Bs} sequences x {w.N} heads of {w.name} (K={w.K}, V={w.V})"
+    return Bs * w.N / dt, desc, threads, dt
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -371,7 +439,7 @@ def main():
         if st != 0:
             raise RuntimeError(f"device status {st} ({detail}) {where}")
 
-    run = Runner(w, m2rnn, rank)
+    run = DecodeRunner(w, m2rnn, rank) if w.decode else Runner(w, m2rnn, rank)
     for _ in range(args.warmup):
         run.step()
     torch.cuda.synchronize()
@@ -395,7 +463,10 @@ def main():
     # End to end through the public API with host inputs.
     e2e = None
     if not args.no_e2e:
-        hx = {n: t.pin_memory() for n, t in run.x.items()}
+        # decode: the step's inputs are q, k, v, f (the carried state and the
+        # weights stay on the device); every step returns y
+        hx = {n: t.pin_memory() for n, t in run.x.items()
+              if not w.decode or n in ("q", "k", "v", "f")}
         res = [run.out["y"]] if not w.backward else [run.gout[n] for n in sorted(run.gout)]
         hres = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res]
         h2d = sum(t.numel() * t.element_size() for t in hx.values())
@@ -427,7 +498,7 @@ def main():
 
     # Nested fwd+bwd measurement (the backward rows of the path).
     nested = None
-    if not w.backward and not args.no_bwd_line:
+    if not w.backward and not w.decode and not args.no_bwd_line:
         wb = WORKLOADS["fwdbwd_bf16_b8_t4096_n32"]
         rb = Runner(wb, m2rnn, rank)
         for _ in range(args.warmup):
@@ -454,6 +525,8 @@ def main():
         nested_main = _fwdbwd_summary(w, world, args.steps, ms_max, fwd_ms, bwd_ms, peaks,
                                       launches)
         roof, roof_json = nested_main["roofline"], nested_main["roofline_hbm_tensor_serial"]
+    elif w.decode:
+        roof, roof_json = _decode_roofline(w, fwd_ms, peaks), None
     else:
         roof, roof_json = _roofline(w, fwd_ms, peaks, _traffic(w))
     line = {
@@ -464,8 +537,12 @@ def main():
         "config": {"workload": w.name, "B": w.B, "T": w.T, "N": w.N, "K": w.K, "V": w.V,
                    "inputs": w.dtype, "state": "f32", "global_batch": w.B * world,
                    "seq_len": w.T, "parallelism": f"replicas{world}" if world > 1 else "1 GPU",
-                   "step": "forward + backward" if w.backward else "forward",
-                   "l2": "inputs larger than L2 (129 MB); no flush"},
+                   "step": ("forward + backward" if w.backward else
+                            "decode (one step, state updated in place)" if w.decode else
+                            "forward"),
+                   "l2": ("state (%.0f MB) larger than L2 (129 MB); no flush"
+                          % (w.B * w.N * w.K * w.V * 4 / 1e6) if w.decode else
+                          "inputs larger than L2 (129 MB); no flush")},
         "roofline": roof, "roofline_hbm_tensor_serial": roof_json,
         "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches * args.steps if launches is not None else args.steps,
@@ -476,7 +553,8 @@ def main():
     if nested is not None:
         line["fwd_bwd"] = nested
     if not args.no_cpu:
-        rate, desc, threads, _ = _oracle_rate(w, 12.0)
+        rate, desc, threads, _ = (_oracle_decode_rate(w, 12.0) if w.decode else
+                                  _oracle_rate(w, 12.0))
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "sample": desc}
     print(json.dumps(line), flush=True)

@@ -176,6 +176,26 @@ int m2rnn_bwd_noalloc(const m2rnn_shape *s, const void *q, const void *k, const 
                       const void *dy, const float *dH_T, float *dq, float *dk, float *dv,
                       float *df, float *dW, float *dw_r, float *dH0, void *stream);
 
+/* Single-step decode: the inference path, one new token for each of B
+ * sequences with the state carried between calls.  One step of Eqs.
+ * (10)-(12) per (b, n):
+ *     H_out = f H_in + (1 - f) tanh(H_in W + k v^T),  y = H_out^T q + w_r (.) v.
+ * The paper's pages give the recurrence, not a decoding kernel; this is the
+ * forward pass at T = 1 with the state in and out, kept apart because it is
+ * bound by the state's HBM traffic rather than by the serial chain.
+ *   s->T must be 1; s->ckpt_every is ignored.
+ *   q, k  : [B,K]      (in_dtype)      v : [B,N,V] (in_dtype)
+ *   f     : [B,N]      (in_dtype)      W, w_r : as for m2rnn_fwd
+ *   H_in  : [B,N,K,V]  (float32), the state before the step (required)
+ *   H_out : [B,N,K,V]  (float32), the state after it (required); it may be
+ *           H_in itself (in-place update), otherwise the two must not overlap
+ *   y     : [B,N,V]    (in_dtype), output
+ * The state update performs the forward kernel's operations in the same
+ * order, so T calls reproduce m2rnn_fwd's H_T for the same inputs. */
+int m2rnn_decode(const m2rnn_shape *s, const void *q, const void *k, const void *v,
+                 const void *f, const void *W, const void *w_r, const float *H_in,
+                 float *H_out, void *y, void *stream);
+
 /* Test hook for the time-out path.  mode 1: kernels launched afterwards
  * from this process start no input transfers, so every internal wait runs
  * into the wait limit, the kernel stops early (outputs unspecified) and

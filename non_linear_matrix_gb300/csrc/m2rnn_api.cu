@@ -378,6 +378,41 @@ int m2rnn_device_status(int* status, int* detail, int clear, void* stream) {
   return M2RNN_OK;
 }
 
+int m2rnn_decode(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
+                 const void* W, const void* w_r, const float* H_in, float* H_out, void* y,
+                 void* stream) {
+  int rc = check_shape(s);
+  if (rc != M2RNN_OK) return rc;
+  if (s->T != 1) return M2RNN_ERR_INVALID_ARG;
+  int dev, sms;
+  int* status;
+  rc = device_info(&dev, &status, &sms);
+  if (rc != M2RNN_OK) return rc;
+  const void* req[] = {q, k, v, f, W, w_r, H_in, H_out, y};
+  for (const void* p : req)
+    if ((rc = check_ptr(p, dev, true)) != M2RNN_OK) return rc;
+  if (H_out != H_in) {  // distinct state buffers must not overlap
+    const size_t bytes = static_cast<size_t>(s->B) * s->N * s->K * s->V * sizeof(float);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(H_in), b = reinterpret_cast<uintptr_t>(H_out);
+    if (a < b + bytes && b < a + bytes) return M2RNN_ERR_INVALID_ARG;
+  }
+  m2rnn::DecodeParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.f = f;
+  p.W = W;
+  p.w_r = w_r;
+  p.H_in = H_in;
+  p.H_out = H_out;
+  p.y = y;
+  p.B = s->B;
+  p.N = s->N;
+  p.K = s->K;
+  return status_from_cuda(m2rnn::launch_decode(p, s->V, s->in_dtype == M2RNN_F32,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
               const void* W, const void* w_r, const float* H0, void* y, float* H_T, float* ckpt,
               void* stream) {

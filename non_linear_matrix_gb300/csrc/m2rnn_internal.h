@@ -82,6 +82,21 @@ int bwd_pipe_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs);
 cudaError_t launch_bwd_pipe(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream);
 int bwd_sub_len(int V, bool f32_inputs);  // sub-interval length of the variant
 
+// Single-step decode (m2rnn_decode.cu).
+struct DecodeParams {
+  const void* q;      // [B,K]
+  const void* k;      // [B,K]
+  const void* v;      // [B,N,V]
+  const void* f;      // [B,N]
+  const void* W;      // [N,V,V]
+  const void* w_r;    // [N,V]
+  const float* H_in;  // [B,N,K,V]
+  float* H_out;       // [B,N,K,V], may equal H_in
+  void* y;            // [B,N,V]
+  int B, N, K;
+};
+cudaError_t launch_decode(const DecodeParams& p, int V, bool f32_inputs, cudaStream_t stream);
+
 // Launches the forward kernel variant for (V, input dtype, MT m-tiles/warp).
 cudaError_t launch_fwd(const FwdParams& p, int V, bool f32_inputs, int MT, cudaStream_t stream);
 

@@ -19,6 +19,10 @@ share a 100B-token training protocol"; long contexts to 16K and beyond):
     dy ~ N(0,1) [B,T,N,V]   (drawn last, only when requested)
   then every tensor is cast to the workload's input dtype (round to nearest
   even for bf16).  H0 = 0 unless a test supplies one.
+
+  Decode workloads (T = 1, state carried between calls) draw the state with
+  ``decode_state``: U(-0.9, 0.9) fp32 [B,N,K,V] from a generator seeded with
+  ``seed + 1`` (any reachable state has |H| <= 1).
 """
 from __future__ import annotations
 
@@ -40,6 +44,7 @@ class Workload:
     f_mean: float = 2.0
     backward: bool = False
     ckpt_every: int = 0  # checkpoint interval C for the backward (0 = none)
+    decode: bool = False  # single-step decode (T = 1, state carried in HBM)
 
     @property
     def th(self) -> int:
@@ -58,6 +63,7 @@ WORKLOADS = {
         Workload("fwd_bf16_b64_t4096_n32_v32", 64, 4096, 32, 64, 32, "bf16", 3),
         Workload("fwdbwd_bf16_b8_t4096_n32", 8, 4096, 32, 64, 16, "bf16", 4,
                  backward=True, ckpt_every=64),
+        Workload("decode_bf16_b2048_n32", 2048, 1, 32, 64, 16, "bf16", 6, decode=True),
     )
 }
 
@@ -82,6 +88,13 @@ def make_inputs(B: int, T: int, N: int, K: int, V: int, dtype: str = "bf16",
         out["dy"] = torch.randn(B, T, N, V, generator=g)
     td = TORCH_DTYPES[dtype]
     return {name: t.to(td).contiguous() for name, t in out.items()}
+
+
+def decode_state(B: int, N: int, K: int, V: int, seed: int) -> torch.Tensor:
+    """A state to decode from (see the module docstring)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 1)
+    return (torch.rand(B, N, K, V, generator=g) * 2 - 1) * 0.9
 
 
 def workload_inputs(w: Workload, with_dy: bool | None = None) -> dict:

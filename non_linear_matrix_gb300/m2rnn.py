@@ -39,6 +39,7 @@ _EXPORTS = {
     "m2rnn_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_longlong]),
     "m2rnn_set_fault_injection": (ctypes.c_int, [ctypes.c_int]),
     "m2rnn_bwd_noalloc": (ctypes.c_int, [_VP] * 18),
+    "m2rnn_decode": (ctypes.c_int, [_VP] * 11),
 }
 
 
@@ -140,6 +141,28 @@ def fwd(q, k, v, f, W, w_r, H0=None, *, ckpt_every: int = 0, want_HT: bool = Tru
                          _ptr(H0), _ptr(y), _ptr(HT), _ptr(ck), _stream(stream))
     _check(rc, "m2rnn_fwd")
     return y, HT, ck
+
+
+def decode(q, k, v, f, W, w_r, H, *, H_out=None, y=None, stream=None):
+    """One decode step for B sequences.  Returns (y, H_out).
+
+    q, k [B,K]; v [B,N,V]; f [B,N]; W [N,V,V]; w_r [N,V], one dtype (bf16 or
+    f32); H [B,N,K,V] fp32 is the state before the step.  H_out defaults to
+    a new tensor; pass ``H_out=H`` to update the state in place."""
+    B, K = q.shape
+    N, V = v.shape[1], v.shape[2]
+    for t in (k, v, f, W, w_r):
+        if t.dtype != q.dtype:
+            raise TypeError("q, k, v, f, W, w_r must share one dtype")
+    s = Shape(B, 1, N, K, V, _dtype_code(q), 0)
+    if H_out is None:
+        H_out = torch.empty_like(H)
+    if y is None:
+        y = torch.empty_like(v)
+    rc = lib().m2rnn_decode(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W),
+                            _ptr(w_r), _ptr(H), _ptr(H_out), _ptr(y), _stream(stream))
+    _check(rc, "m2rnn_decode")
+    return y, H_out
 
 
 def bwd_workspace_size(shape: Shape, ckpt_given: bool) -> int:

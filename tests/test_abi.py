@@ -82,3 +82,13 @@ def test_bwd_rejects_bad_shapes_before_launch(lib):
     rc = lib.m2rnn_bwd(s, *([p] * 6), None, None, p, None, *([p] * 6), None, None, p,
                        ctypes.c_size_t(1 << 20), None)
     assert rc in (-1, -2)
+
+
+def test_decode_rejects_bad_arguments_before_launch(lib):
+    """T must be 1 and K, V supported; both are checked before any device
+    call."""
+    from non_linear_matrix_gb300.m2rnn import Shape
+    p = ctypes.c_void_p(16)
+    assert lib.m2rnn_decode(ctypes.byref(Shape(4, 2, 2, 64, 16, 1, 0)), *([p] * 10)) == -1
+    assert lib.m2rnn_decode(ctypes.byref(Shape(4, 1, 2, 48, 16, 1, 0)), *([p] * 10)) == -2
+    assert lib.m2rnn_decode(None, *([p] * 10)) == -1
