@@ -5,7 +5,8 @@
 //
 //     H' = f H + (1 - f) tanh(H W + k v^T),    y = H'^T q + w_r (.) v
 //
-// One CTA per (sequence b, head n), one warp per 16 rows of the K x V state.
+// One CTA per (sequence b, head n), one warp per 32 rows (two 16-row MMA
+// tiles, 16 rows when K = 16) of the K x V state.
 // A step reads and writes the whole fp32 state (2 K V 4 bytes per head)
 // against a few hundred bytes of inputs, so the kernel is bound by HBM
 // bandwidth: every state element is loaded once (float2 per lane, whole
@@ -43,17 +44,17 @@ __device__ __forceinline__ float dtof(__nv_bfloat16 x) { return __bfloat162float
 __device__ __forceinline__ void dstore(float* p, float x) { *p = x; }
 __device__ __forceinline__ void dstore(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-template <int V, bool F32>
+template <int V, bool F32, int MT>
 __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
   using TIn = typename DecIn<F32>::T;
   constexpr int NT = V / 8, KS = V / 16;
-  __shared__ float ysum[8][V];  // per-warp readout partials (K <= 128: 8 warps)
+  __shared__ float ysum[8][V];  // per-warp readout partials (at most 8 warps)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int K = p.K, N = p.N, nw = K / 16;
+  const int K = p.K, N = p.N, nw = K / (16 * MT);
   const size_t head = blockIdx.x;  // b * N + n
   const int b = static_cast<int>(head / N), n = static_cast<int>(head % N);
-  const int row0 = 16 * warp;
+  const int row0 = 16 * MT * warp;  // MT 16-row tiles per warp
 
   const TIn* q = static_cast<const TIn*>(p.q) + static_cast<size_t>(b) * K;
   const TIn* k = static_cast<const TIn*>(p.k) + static_cast<size_t>(b) * K;
@@ -63,16 +64,20 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
   const float* Hin = p.H_in + head * K * V;
   float* Hout = p.H_out + head * K * V;
 
-  // the state first: the loads that decide the kernel's time
-  float H[NT][4];
+  // the state first: the loads that decide the kernel's time, all in flight
+  // before any use
+  float H[MT][NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int m = 0; m < MT; ++m)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float2 x = __ldcs(reinterpret_cast<const float2*>(Hin + (row0 + g + 8 * h) * V + 8 * nt + 2 * c));
-      H[nt][2 * h] = x.x;
-      H[nt][2 * h + 1] = x.y;
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float2 x = __ldcs(reinterpret_cast<const float2*>(
+            Hin + (row0 + 16 * m + g + 8 * h) * V + 8 * nt + 2 * c));
+        H[m][nt][2 * h] = x.x;
+        H[m][nt][2 * h + 1] = x.y;
+      }
   // W as the B operand of H W (k-index l, n-index j), bf16 hi (+ lo for fp32 inputs)
   uint32_t Bw[KS][NT][2], Bwl[KS][NT][2];
 #pragma unroll
@@ -88,71 +93,77 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
                                                 w1 - ptx::bf16x2_hi(Bw[ks][nt][h]))
                              : 0u;
       }
-  const float k0 = dtof(k[row0 + g]), k1 = dtof(k[row0 + g + 8]);
-  const float q0 = dtof(q[row0 + g]), q1 = dtof(q[row0 + g + 8]);
   float2 vv[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
     vv[nt] = make_float2(dtof(v[8 * nt + 2 * c]), dtof(v[8 * nt + 2 * c + 1]));
   const float fg = dtof(static_cast<const TIn*>(p.f)[head]);
-
-  // bf16 A fragments of H (hi, and lo for fp32 inputs)
-  uint32_t A[KS][4], Al[KS][4];
-#pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    A[ks][0] = ptx::pack_bf16x2(H[2 * ks][0], H[2 * ks][1]);
-    A[ks][1] = ptx::pack_bf16x2(H[2 * ks][2], H[2 * ks][3]);
-    A[ks][2] = ptx::pack_bf16x2(H[2 * ks + 1][0], H[2 * ks + 1][1]);
-    A[ks][3] = ptx::pack_bf16x2(H[2 * ks + 1][2], H[2 * ks + 1][3]);
-    if (F32) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int nt = 2 * ks + (i >> 1), r = 2 * (i & 1);
-        Al[ks][i] = ptx::pack_bf16x2(H[nt][r] - ptx::bf16x2_lo(A[ks][i]),
-                                     H[nt][r + 1] - ptx::bf16x2_hi(A[ks][i]));
-      }
-    }
-  }
-  // Z = tanh(H W + k v^T);  H' = Z + f (H - Z)
-  const float2 kk0 = make_float2(k0, k0), kk1 = make_float2(k1, k1);
-  float acc[NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const float2 lo = __fmul2_rn(kk0, vv[nt]), hi = __fmul2_rn(kk1, vv[nt]);
-    acc[nt][0] = lo.x;
-    acc[nt][1] = lo.y;
-    acc[nt][2] = hi.x;
-    acc[nt][3] = hi.y;
-  }
-#pragma unroll
-  for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      ptx::mma_bf16_16816(acc[nt], A[ks], Bw[ks][nt][0], Bw[ks][nt][1]);
-      if (F32) {
-        ptx::mma_bf16_16816(acc[nt], A[ks], Bwl[ks][nt][0], Bwl[ks][nt][1]);
-        ptx::mma_bf16_16816(acc[nt], Al[ks], Bw[ks][nt][0], Bw[ks][nt][1]);
-      }
-    }
   const float2 f2 = make_float2(fg, fg), m1 = make_float2(-1.f, -1.f);
+
   float ypart[NT][2];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    float hn[4];
+  for (int nt = 0; nt < NT; ++nt) ypart[nt][0] = ypart[nt][1] = 0.f;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float2 z;
-      z.x = F32 ? tanhf(acc[nt][2 * h]) : ptx::tanh_approx(acc[nt][2 * h]);
-      z.y = F32 ? tanhf(acc[nt][2 * h + 1]) : ptx::tanh_approx(acc[nt][2 * h + 1]);
-      const float2 d = __ffma2_rn(m1, z, make_float2(H[nt][2 * h], H[nt][2 * h + 1]));
-      const float2 r = __ffma2_rn(f2, d, z);
-      hn[2 * h] = r.x;
-      hn[2 * h + 1] = r.y;
-      __stcs(reinterpret_cast<float2*>(Hout + (row0 + g + 8 * h) * V + 8 * nt + 2 * c), r);
+  for (int m = 0; m < MT; ++m) {
+    const int r0 = row0 + 16 * m;
+    const float k0 = dtof(k[r0 + g]), k1 = dtof(k[r0 + g + 8]);
+    const float q0 = dtof(q[r0 + g]), q1 = dtof(q[r0 + g + 8]);
+    // bf16 A fragments of H (hi, and lo for fp32 inputs)
+    uint32_t A[KS][4], Al[KS][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      A[ks][0] = ptx::pack_bf16x2(H[m][2 * ks][0], H[m][2 * ks][1]);
+      A[ks][1] = ptx::pack_bf16x2(H[m][2 * ks][2], H[m][2 * ks][3]);
+      A[ks][2] = ptx::pack_bf16x2(H[m][2 * ks + 1][0], H[m][2 * ks + 1][1]);
+      A[ks][3] = ptx::pack_bf16x2(H[m][2 * ks + 1][2], H[m][2 * ks + 1][3]);
+      if (F32) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int nt = 2 * ks + (i >> 1), r = 2 * (i & 1);
+          Al[ks][i] = ptx::pack_bf16x2(H[m][nt][r] - ptx::bf16x2_lo(A[ks][i]),
+                                       H[m][nt][r + 1] - ptx::bf16x2_hi(A[ks][i]));
+        }
+      }
     }
-    // this lane's two rows of the readout for columns 8nt + 2c, 8nt + 2c + 1
-    ypart[nt][0] = fmaf(hn[0], q0, hn[2] * q1);
-    ypart[nt][1] = fmaf(hn[1], q0, hn[3] * q1);
+    // Z = tanh(H W + k v^T);  H' = Z + f (H - Z)
+    const float2 kk0 = make_float2(k0, k0), kk1 = make_float2(k1, k1);
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float2 lo = __fmul2_rn(kk0, vv[nt]), hi = __fmul2_rn(kk1, vv[nt]);
+      acc[nt][0] = lo.x;
+      acc[nt][1] = lo.y;
+      acc[nt][2] = hi.x;
+      acc[nt][3] = hi.y;
+    }
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        ptx::mma_bf16_16816(acc[nt], A[ks], Bw[ks][nt][0], Bw[ks][nt][1]);
+        if (F32) {
+          ptx::mma_bf16_16816(acc[nt], A[ks], Bwl[ks][nt][0], Bwl[ks][nt][1]);
+          ptx::mma_bf16_16816(acc[nt], Al[ks], Bw[ks][nt][0], Bw[ks][nt][1]);
+        }
+      }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float hn[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float2 z;
+        z.x = F32 ? tanhf(acc[nt][2 * h]) : ptx::tanh_approx(acc[nt][2 * h]);
+        z.y = F32 ? tanhf(acc[nt][2 * h + 1]) : ptx::tanh_approx(acc[nt][2 * h + 1]);
+        const float2 d = __ffma2_rn(m1, z, make_float2(H[m][nt][2 * h], H[m][nt][2 * h + 1]));
+        const float2 r = __ffma2_rn(f2, d, z);
+        hn[2 * h] = r.x;
+        hn[2 * h + 1] = r.y;
+        __stcs(reinterpret_cast<float2*>(Hout + (r0 + g + 8 * h) * V + 8 * nt + 2 * c), r);
+      }
+      // this lane's two rows of the readout for columns 8nt + 2c, 8nt + 2c + 1
+      ypart[nt][0] += fmaf(hn[0], q0, hn[2] * q1);
+      ypart[nt][1] += fmaf(hn[1], q0, hn[3] * q1);
+    }
   }
   // sum over the 8 row groups of the warp (lanes with equal c)
 #pragma unroll
@@ -177,7 +188,10 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
 template <int V, bool F32>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   const size_t heads = static_cast<size_t>(p.B) * p.N;
-  decode_kernel<V, F32><<<static_cast<unsigned>(heads), 32 * (p.K / 16), 0, stream>>>(p);
+  if (p.K >= 32)  // two 16-row tiles per warp: twice the state bytes in flight per warp
+    decode_kernel<V, F32, 2><<<static_cast<unsigned>(heads), 32 * (p.K / 32), 0, stream>>>(p);
+  else
+    decode_kernel<V, F32, 1><<<static_cast<unsigned>(heads), 32 * (p.K / 16), 0, stream>>>(p);
   return cudaGetLastError();
 }
 
