@@ -16,7 +16,9 @@ share a 100B-token training protocol"; long contexts to 16K and beyond):
     f  = sigmoid(N(f_mean, 1)) [B,T,N]
     W  ~ N(0, 1/V) [N,V,V]
     w_r ~ N(0,1) [N,V]
-    dy ~ N(0,1) [B,T,N,V]   (drawn last, only when requested)
+    dy ~ N(0,1) [B,T,N,V]   (only when requested)
+    a  ~ N(0,1) [B,T,N], alpha ~ U(0.5, 1.5) [N], beta ~ N(-2, 0.5) [N]
+                            (drawn last, only for the fused input gate)
   then every tensor is cast to the workload's input dtype (round to nearest
   even for bf16).  H0 = 0 unless a test supplies one.
 
@@ -71,7 +73,8 @@ TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
 def make_inputs(B: int, T: int, N: int, K: int, V: int, dtype: str = "bf16",
-                seed: int = 0, f_mean: float = 2.0, with_dy: bool = False) -> dict:
+                seed: int = 0, f_mean: float = 2.0, with_dy: bool = False,
+                gated: bool = False) -> dict:
     """Draw one seeded input set on the CPU (see the module docstring)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
@@ -86,6 +89,10 @@ def make_inputs(B: int, T: int, N: int, K: int, V: int, dtype: str = "bf16",
     out = {"q": q, "k": k, "v": v, "f": f, "W": W, "w_r": w_r}
     if with_dy:
         out["dy"] = torch.randn(B, T, N, V, generator=g)
+    if gated:
+        out["a"] = torch.randn(B, T, N, generator=g)
+        out["alpha"] = torch.rand(N, generator=g) + 0.5
+        out["beta"] = torch.randn(N, generator=g) * 0.5 - 2.0
     td = TORCH_DTYPES[dtype]
     return {name: t.to(td).contiguous() for name, t in out.items()}
 

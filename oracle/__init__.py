@@ -14,6 +14,11 @@ arrays to contiguous float64 and marshals pointers.
 
 Layouts: q, k [B,T,K]; v [B,T,N,V]; f [B,T,N]; W [N,V,V] with
 (H W)_{ij} = sum_l H_{il} W_{lj}; w_r [N,V]; H0/H_T [B,N,K,V]; y [B,T,N,V].
+
+The gated functions follow the frame "The gate preserves a direct path
+through time": f_{t,n} = exp(-alpha_n softplus(a_{t,n} + beta_n)), with a
+[B,T,N] and alpha, beta [N].  They compute f (and the gate's derivatives) in
+numpy fp64 and call the same C routines.
 """
 from __future__ import annotations
 
@@ -122,3 +127,39 @@ def bwd(q, k, v, f, W, w_r, dy, H0=None, dHT=None):
     if rc != 0:
         raise RuntimeError(f"m2rnn_oracle_bwd failed: {rc}")
     return out
+
+
+def _gate_parts(a, alpha, beta):
+    """x = a + beta, softplus(x), f = exp(-alpha softplus(x)), sigmoid(x) (fp64)."""
+    a, alpha, beta = map(_f64, (a, alpha, beta))
+    x = a + beta                                   # beta broadcasts over [..., N]
+    sp = np.logaddexp(0.0, x)                      # softplus(x) = log(1 + e^x)
+    f = np.exp(-alpha * sp)
+    sig = 0.5 * (1.0 + np.tanh(0.5 * x))           # sigmoid(x) = softplus'(x)
+    return x, sp, f, sig
+
+
+def gate(a, alpha, beta):
+    """f_{t,n} = exp(-alpha_n softplus(a_{t,n} + beta_n)) (float64)."""
+    return _gate_parts(a, alpha, beta)[2]
+
+
+def fwd_gated(q, k, v, a, alpha, beta, W, w_r, H0=None, want_states: bool = False):
+    """Forward pass with the input gate computed from a."""
+    return fwd(q, k, v, gate(a, alpha, beta), W, w_r, H0, want_states)
+
+
+def bwd_gated(q, k, v, a, alpha, beta, W, w_r, dy, H0=None, dHT=None):
+    """Backward pass with the input gate: the chain rule through
+    f = exp(-alpha s), s = softplus(a + beta):
+        df/da = df/dbeta = -alpha f sigmoid(a + beta),   df/dalpha = -s f.
+    Returns dict(dq, dk, dv, da, dalpha, dbeta, dW, dw_r, dH0) (float64)."""
+    _, sp, f, sig = _gate_parts(a, alpha, beta)
+    r = bwd(q, k, v, f, W, w_r, dy, H0, dHT)
+    alpha64 = _f64(alpha)
+    df = r.pop("df")
+    da = df * (-alpha64 * f * sig)
+    r["da"] = da
+    r["dalpha"] = (df * (-sp * f)).reshape(-1, df.shape[-1]).sum(axis=0)
+    r["dbeta"] = da.reshape(-1, da.shape[-1]).sum(axis=0)
+    return r

@@ -220,3 +220,70 @@ def test_backward_f_one(oracle_mod):
     g = oracle_mod.bwd(x["q"], x["k"], x["v"], f, x["W"], x["w_r"], x["dy"])
     assert np.all(g["dW"] == 0) and np.all(g["dk"] == 0) and np.all(g["dq"] == 0)
     np.testing.assert_array_equal(g["dv"], _np(x["w_r"])[None, None] * _np(x["dy"]))
+
+
+# --- fused input gate (frame "The gate preserves a direct path through time")
+
+def test_gate_special_values(oracle_mod):
+    """softplus(0) = ln 2, so a = -beta gives f = 2^(-alpha); alpha = 0 gives
+    f = 1 for every a; for a + beta >> 1, softplus(x) -> x."""
+    alpha = np.array([0.0, 0.5, 1.0, 2.0])
+    beta = np.array([-2.0, 0.3, 1.5, -0.7])
+    a = np.broadcast_to(-beta, (2, 3, 4)).copy()
+    f = oracle_mod.gate(a, alpha, beta)
+    assert np.allclose(f, np.broadcast_to(2.0 ** (-alpha), f.shape), rtol=1e-15, atol=0)
+    f0 = oracle_mod.gate(np.random.default_rng(0).normal(size=(2, 3, 4)) * 5, np.zeros(4), beta)
+    assert np.array_equal(f0, np.ones_like(f0))
+    big = oracle_mod.gate(np.full((1, 1, 4), 40.0), alpha, beta)[0, 0]
+    assert np.allclose(big, np.exp(-alpha * (40.0 + beta)), rtol=1e-12, atol=0)
+
+
+def test_gate_alpha_zero_keeps_zero_state(oracle_mod):
+    """alpha = 0 makes f = 1: H stays 0, y = w_r (.) v, and a, beta get no
+    gradient."""
+    x = make_inputs(2, 6, 3, 8, 4, "f32", 5, with_dy=True, gated=True)
+    alpha = torch.zeros(3)
+    o = oracle_mod.fwd_gated(x["q"], x["k"], x["v"], x["a"], alpha, x["beta"], x["W"], x["w_r"])
+    assert np.array_equal(o["HT"], np.zeros_like(o["HT"]))
+    assert np.allclose(o["y"], _np(x["w_r"])[None, None] * _np(x["v"]), rtol=1e-15, atol=0)
+    g = oracle_mod.bwd_gated(x["q"], x["k"], x["v"], x["a"], alpha, x["beta"], x["W"], x["w_r"],
+                             x["dy"])
+    assert np.count_nonzero(g["da"]) == 0 and np.count_nonzero(g["dbeta"]) == 0
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_gated_backward_matches_central_differences(oracle_mod, T):
+    """da, dalpha, dbeta of the gated backward against brute-force central
+    differences of L = sum y (.) dy + sum H_T (.) dH_T in fp64, every
+    element of a, alpha and beta."""
+    B, N, K, V = 2, 2, 3, 3
+    x = make_inputs(B, T, N, K, V, "f32", 300 + T, with_dy=True, gated=True)
+    rng = np.random.default_rng(T + 7)
+    inp = {n: _np(x[n]).copy() for n in ("q", "k", "v", "a", "alpha", "beta", "W", "w_r")}
+    H0 = rng.uniform(-0.5, 0.5, size=(B, N, K, V))
+    dy = _np(x["dy"])
+    dHT = rng.normal(size=(B, N, K, V))
+
+    def loss():
+        o = oracle_mod.fwd_gated(inp["q"], inp["k"], inp["v"], inp["a"], inp["alpha"],
+                                 inp["beta"], inp["W"], inp["w_r"], H0=H0)
+        return float(np.sum(o["y"] * dy) + np.sum(o["HT"] * dHT))
+
+    g = oracle_mod.bwd_gated(inp["q"], inp["k"], inp["v"], inp["a"], inp["alpha"], inp["beta"],
+                             inp["W"], inp["w_r"], dy, H0=H0, dHT=dHT)
+    h = 1e-6
+    for name, gname in (("a", "da"), ("alpha", "dalpha"), ("beta", "dbeta")):
+        arr = inp[name]
+        fd = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = loss()
+            arr[idx] = old - h
+            lm = loss()
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.abs(g[gname] - fd).max() / max(1.0, np.abs(fd).max())
+        assert err <= 1e-6, (gname, err)
