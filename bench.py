@@ -201,9 +201,14 @@ def _oracle_rate(w, budget_s: float, seed_offset: int = 0):
 
     def run(T_):
         x = make_inputs(1, T_, heads, w.K, w.V, w.dtype, w.seed + seed_offset, w.f_mean,
-                        with_dy=w.backward)
+                        with_dy=w.backward, gated=w.gated)
         t0 = time.perf_counter()
-        if w.backward:  # forward + BPTT backward (the oracle's backward reruns the forward)
+        if w.gated:  # the oracle's gated forward (+ backward through the gate)
+            gi = (x["a"], x["alpha"], x["beta"])
+            oracle.fwd_gated(x["q"], x["k"], x["v"], *gi, x["W"], x["w_r"])
+            if w.backward:
+                oracle.bwd_gated(x["q"], x["k"], x["v"], *gi, x["W"], x["w_r"], x["dy"])
+        elif w.backward:  # forward + BPTT backward (the oracle's backward reruns the forward)
             oracle.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"])
             oracle.bwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], x["dy"])
         else:
@@ -273,7 +278,7 @@ class Runner:
         self.w, self.m = w, m2rnn
         seed = rank_seed(w.seed, rank)
         self.x = make_inputs(w.B, w.T, w.N, w.K, w.V, w.dtype, seed, w.f_mean,
-                             with_dy=w.backward)
+                             with_dy=w.backward, gated=w.gated)
         self.g = {n: t.cuda() for n, t in self.x.items()}
         g = self.g
         f32 = dict(device="cuda", dtype=torch.float32)
@@ -285,9 +290,13 @@ class Runner:
             self.gout = {"dq": torch.empty(w.B, w.T, w.K, **f32),
                          "dk": torch.empty(w.B, w.T, w.K, **f32),
                          "dv": torch.empty(w.B, w.T, w.N, w.V, **f32),
-                         "df": torch.empty(w.B, w.T, w.N, **f32),
                          "dW": torch.empty(w.N, w.V, w.V, **f32),
                          "dw_r": torch.empty(w.N, w.V, **f32)}
+            if w.gated:
+                self.gout.update(da=torch.empty(w.B, w.T, w.N, **f32),
+                                 dalpha=torch.empty(w.N, **f32), dbeta=torch.empty(w.N, **f32))
+            else:
+                self.gout["df"] = torch.empty(w.B, w.T, w.N, **f32)
             shape = m2rnn.make_shape(g["q"], g["v"], w.ckpt_every)
             self.ws = torch.empty(max(16, m2rnn.bwd_workspace_size(shape, True)),
                                   device="cuda", dtype=torch.uint8)
@@ -295,14 +304,23 @@ class Runner:
 
     def fwd(self):
         g = self.g
-        self.m.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], out=self.out,
-                   ckpt_every=self.w.ckpt_every)
+        if self.w.gated:
+            self.m.fwd_gated(g["q"], g["k"], g["v"], g["a"], g["alpha"], g["beta"], g["W"],
+                             g["w_r"], out=self.out, ckpt_every=self.w.ckpt_every)
+        else:
+            self.m.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], out=self.out,
+                       ckpt_every=self.w.ckpt_every)
 
     def bwd(self):
         g = self.g
-        self.m.bwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], g["dy"],
-                   ckpt=self.out["ckpt"], ckpt_every=self.w.ckpt_every, out=self.gout,
-                   workspace=self.ws)
+        if self.w.gated:
+            self.m.bwd_gated(g["q"], g["k"], g["v"], g["a"], g["alpha"], g["beta"], g["W"],
+                             g["w_r"], g["dy"], ckpt=self.out["ckpt"],
+                             ckpt_every=self.w.ckpt_every, out=self.gout, workspace=self.ws)
+        else:
+            self.m.bwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], g["dy"],
+                       ckpt=self.out["ckpt"], ckpt_every=self.w.ckpt_every, out=self.gout,
+                       workspace=self.ws)
 
     def step(self):
         self.fwd()
@@ -466,7 +484,7 @@ def main():
         # decode: the step's inputs are q, k, v, f (the carried state and the
         # weights stay on the device); every step returns y
         hx = {n: t.pin_memory() for n, t in run.x.items()
-              if not w.decode or n in ("q", "k", "v", "f")}
+              if (not w.decode or n in ("q", "k", "v", "f")) and not (w.gated and n == "f")}
         res = [run.out["y"]] if not w.backward else [run.gout[n] for n in sorted(run.gout)]
         hres = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res]
         h2d = sum(t.numel() * t.element_size() for t in hx.values())
@@ -537,7 +555,8 @@ def main():
         "config": {"workload": w.name, "B": w.B, "T": w.T, "N": w.N, "K": w.K, "V": w.V,
                    "inputs": w.dtype, "state": "f32", "global_batch": w.B * world,
                    "seq_len": w.T, "parallelism": f"replicas{world}" if world > 1 else "1 GPU",
-                   "step": ("forward + backward" if w.backward else
+                   "step": ("forward + backward" + (" (fused input gate)" if w.gated else "")
+                            if w.backward else
                             "decode (one step, state updated in place)" if w.decode else
                             "forward"),
                    "l2": ("state (%.0f MB) larger than L2 (129 MB); no flush"

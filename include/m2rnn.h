@@ -129,6 +129,35 @@ int m2rnn_bwd(const m2rnn_shape *s, const void *q, const void *k, const void *v,
               float *dq, float *dk, float *dv, float *df, float *dW, float *dw_r,
               float *dH0, float *dckpt, void *workspace, size_t ws_bytes, void *stream);
 
+/* Forward pass with the fused input gate of the frame "The gate preserves a
+ * direct path through time" (Eq. 13):
+ *     f_{t,n} = exp(-alpha_n softplus(a_{t,n} + beta_n)),   alpha_n >= 0,
+ * evaluated in fp32 inside the kernel instead of reading f.
+ *   a     : [B,T,N] (in_dtype), the gate's pre-activation (required)
+ *   alpha : [N] (in_dtype), beta : [N] (in_dtype) (required)
+ * Everything else is as for m2rnn_fwd.  alpha < 0 is not rejected (the
+ * formula is evaluated as given); f then exceeds 1. */
+int m2rnn_fwd_gated(const m2rnn_shape *s, const void *q, const void *k, const void *v,
+                    const void *a, const void *alpha, const void *beta, const void *W,
+                    const void *w_r, const float *H0, void *y, float *H_T, float *ckpt,
+                    void *stream);
+
+/* Backward pass through the fused input gate: as m2rnn_bwd, with f computed
+ * from (a, alpha, beta) as in m2rnn_fwd_gated, and the chain rule
+ *     df/da = df/dbeta = -alpha f sigmoid(a + beta),  df/dalpha = -softplus(a + beta) f
+ * applied inside the kernel:
+ *   da     : [B,T,N] float32, dL/da (in place of df)
+ *   dalpha : [N] float32, dL/dalpha summed over b and t (overwritten)
+ *   dbeta  : [N] float32, dL/dbeta summed over b and t (overwritten)
+ * ckpt (if given) must come from m2rnn_fwd_gated with the same inputs.
+ * The workspace rule is that of m2rnn_bwd (m2rnn_bwd_workspace_size). */
+int m2rnn_bwd_gated(const m2rnn_shape *s, const void *q, const void *k, const void *v,
+                    const void *a, const void *alpha, const void *beta, const void *W,
+                    const void *w_r, const float *H0, const float *ckpt, const void *dy,
+                    const float *dH_T, float *dq, float *dk, float *dv, float *da,
+                    float *dalpha, float *dbeta, float *dW, float *dw_r, float *dH0,
+                    float *dckpt, void *workspace, size_t ws_bytes, void *stream);
+
 /* Reads (after synchronising `stream`) and optionally clears the device
  * status word of the current device.  *status receives M2RNN_OK or the code
  * a kernel recorded (M2RNN_ERR_TIMEOUT); *detail receives the location code

@@ -183,6 +183,14 @@ WavePlan plan_full_waves(const m2rnn_shape* s, int sms, const FwdConfig& cfg,
   return {static_cast<int>(B1), bestG, bestTc};
 }
 
+// The fused input gate's inputs (a [B,T,N], alpha and beta [N]); a null
+// Gate pointer means f is given directly.
+struct Gate {
+  const void* a;
+  const void* alpha;
+  const void* beta;
+};
+
 // Parameters with every per-batch pointer advanced by b0 batch items.
 m2rnn::FwdParams offset_batch(const m2rnn::FwdParams& p, int b0, const m2rnn_shape* s, int es) {
   m2rnn::FwdParams r = p;
@@ -190,7 +198,8 @@ m2rnn::FwdParams offset_batch(const m2rnn::FwdParams& p, int b0, const m2rnn_sha
   r.q = static_cast<const char*>(p.q) + B0 * T * K * es;
   r.k = static_cast<const char*>(p.k) + B0 * T * K * es;
   r.v = static_cast<const char*>(p.v) + B0 * T * N * V * es;
-  r.f = static_cast<const char*>(p.f) + B0 * T * N * es;
+  if (p.f) r.f = static_cast<const char*>(p.f) + B0 * T * N * es;
+  if (p.a) r.a = static_cast<const char*>(p.a) + B0 * T * N * es;
   r.y = static_cast<char*>(p.y) + B0 * T * N * V * es;
   if (p.H0) r.H0 = p.H0 + B0 * N * K * V;
   if (p.HT) r.HT = p.HT + B0 * N * K * V;
@@ -201,8 +210,8 @@ m2rnn::FwdParams offset_batch(const m2rnn::FwdParams& p, int b0, const m2rnn_sha
 // Plans and launches the forward pass (pointers already validated).  y may
 // be NULL (checkpoint-only runs for the backward pass).
 int run_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
-            const void* W, const void* w_r, const float* H0, void* y, float* H_T, float* ckpt,
-            cudaStream_t st, int* status, int sms) {
+            const Gate* gate, const void* W, const void* w_r, const float* H0, void* y,
+            float* H_T, float* ckpt, cudaStream_t st, int* status, int sms) {
   const bool want_ckpt = ckpt != nullptr && s->ckpt_every > 0 && s->T > 0;
   const bool f32 = s->in_dtype == M2RNN_F32;
   const FwdConfig cfg = choose_fwd(s, sms);
@@ -230,6 +239,13 @@ int run_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, c
   p.status = status;
   p.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
   p.inject_stall = g_fault_injection.load();
+  if (gate != nullptr) {
+    p.f = nullptr;
+    p.a = gate->a;
+    p.alpha = gate->alpha;
+    p.beta = gate->beta;
+    p.gated = 1;
+  }
 
   // Wave planning.  All CTAs of a launch run equally long, so when the heads
   // fill some whole waves plus a remainder, the remainder's batch items get a
@@ -300,7 +316,7 @@ bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
     const int pipe = kinds[ki];
     for (int w = mtiles < 8 ? mtiles : 8; w >= 1; w /= 2) {
       if (mtiles % w != 0 || (force_w > 0 && w != force_w)) continue;
-      const size_t smem = pipe ? m2rnn::bwd_pipe_smem_bytes(V, p.C, w, f32)
+      const size_t smem = pipe ? m2rnn::bwd_pipe_smem_bytes(V, p.C, w, f32, p.gated != 0)
                                : m2rnn::bwd_smem_bytes(V, p.C, p.S2, w, f32);
       if (smem > kSmemBudget) continue;
       m2rnn::BwdParams q = p;
@@ -413,9 +429,14 @@ int m2rnn_decode(const m2rnn_shape* s, const void* q, const void* k, const void*
                                                static_cast<cudaStream_t>(stream)));
 }
 
-int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
-              const void* W, const void* w_r, const float* H0, void* y, float* H_T, float* ckpt,
-              void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Forward entry: validation, then run_fwd.  gate = NULL: f is given.
+int fwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
+             const Gate* gate, const void* W, const void* w_r, const float* H0, void* y,
+             float* H_T, float* ckpt, void* stream) {
   int rc = check_shape(s);
   if (rc != M2RNN_OK) return rc;
   int dev, sms;
@@ -425,6 +446,10 @@ int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   const bool want_ckpt = s->ckpt_every > 0 && s->T > 0;
   if ((rc = check_ptr(H0, dev, false)) != M2RNN_OK) return rc;
   if ((rc = check_ptr(H_T, dev, false)) != M2RNN_OK) return rc;
+  if (gate != nullptr) {  // per-head gate parameters
+    if ((rc = check_ptr(gate->alpha, dev, true)) != M2RNN_OK) return rc;
+    if ((rc = check_ptr(gate->beta, dev, true)) != M2RNN_OK) return rc;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t state_bytes = static_cast<size_t>(s->B) * s->N * s->K * s->V * sizeof(float);
   if (s->T == 0) {  // empty sequences: the [B,0,...] tensors may have no storage
@@ -432,26 +457,21 @@ int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
     return status_from_cuda(H0 ? cudaMemcpyAsync(H_T, H0, state_bytes, cudaMemcpyDeviceToDevice, st)
                                : cudaMemsetAsync(H_T, 0, state_bytes, st));
   }
-  const void* req[] = {q, k, v, f, W, w_r, y};
+  const void* req[] = {q, k, v, gate ? gate->a : f, W, w_r, y};
   for (const void* p : req)
     if ((rc = check_ptr(p, dev, true)) != M2RNN_OK) return rc;
   if ((rc = check_ptr(ckpt, dev, false)) != M2RNN_OK) return rc;
-  return run_fwd(s, q, k, v, f, W, w_r, H0, y, H_T, want_ckpt ? ckpt : nullptr, st, status, sms);
+  return run_fwd(s, q, k, v, f, gate, W, w_r, H0, y, H_T, want_ckpt ? ckpt : nullptr, st, status,
+                 sms);
 }
 
-size_t m2rnn_bwd_workspace_size(const m2rnn_shape* s, int ckpt_given) {
-  if (check_shape(s) != M2RNN_OK || s->ckpt_every <= 0 || s->T == 0) return 0;
-  bool own = false;
-  const int C = bwd_interval(s, ckpt_given != 0, &own);
-  if (!own) return 0;
-  const size_t nck = static_cast<size_t>((s->T + C - 1) / C);
-  return align256(static_cast<size_t>(s->B) * s->N * nck * s->K * s->V * sizeof(float));
-}
-
-int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
-              const void* W, const void* w_r, const float* H0, const float* ckpt, const void* dy,
-              const float* dH_T, float* dq, float* dk, float* dv, float* df, float* dW, float* dw_r,
-              float* dH0, float* dckpt, void* workspace, size_t ws_bytes, void* stream) {
+// Backward entry.  gate = NULL: f is given and dfa receives dL/df; otherwise
+// dfa receives dL/da and dalpha, dbeta the gate parameters' gradients.
+int bwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
+             const Gate* gate, const void* W, const void* w_r, const float* H0, const float* ckpt,
+             const void* dy, const float* dH_T, float* dq, float* dk, float* dv, float* dfa,
+             float* dalpha, float* dbeta, float* dW, float* dw_r, float* dH0, float* dckpt,
+             void* workspace, size_t ws_bytes, void* stream) {
   int rc = check_shape(s);
   if (rc != M2RNN_OK) return rc;
   if (s->ckpt_every <= 0) return M2RNN_ERR_INVALID_ARG;
@@ -462,23 +482,30 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   const void* always[] = {W, w_r, dW, dw_r};
   for (const void* x : always)
     if ((rc = check_ptr(x, dev, true)) != M2RNN_OK) return rc;
+  if (gate != nullptr) {
+    const void* gp[] = {gate->alpha, gate->beta, dalpha, dbeta};
+    for (const void* x : gp)
+      if ((rc = check_ptr(x, dev, true)) != M2RNN_OK) return rc;
+  }
   const void* optional[] = {H0, dH_T, dH0, dckpt};
   for (const void* x : optional)
     if ((rc = check_ptr(x, dev, false)) != M2RNN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool f32 = s->in_dtype == M2RNN_F32;
-  const size_t es = f32 ? 4 : 2;
   const size_t NV = static_cast<size_t>(s->N) * s->V;
   const size_t state_bytes = static_cast<size_t>(s->B) * s->N * s->K * s->V * sizeof(float);
   if (cudaMemsetAsync(dW, 0, NV * s->V * sizeof(float), st) != cudaSuccess ||
       cudaMemsetAsync(dw_r, 0, NV * sizeof(float), st) != cudaSuccess)
+    return M2RNN_ERR_CUDA;
+  if (gate != nullptr && (cudaMemsetAsync(dalpha, 0, s->N * sizeof(float), st) != cudaSuccess ||
+                          cudaMemsetAsync(dbeta, 0, s->N * sizeof(float), st) != cudaSuccess))
     return M2RNN_ERR_CUDA;
   if (s->T == 0) {  // no steps: dH0 = dH_T
     if (dH0 == nullptr) return M2RNN_OK;
     return status_from_cuda(dH_T ? cudaMemcpyAsync(dH0, dH_T, state_bytes, cudaMemcpyDeviceToDevice, st)
                                  : cudaMemsetAsync(dH0, 0, state_bytes, st));
   }
-  const void* req[] = {q, k, v, f, dy, dq, dk, dv, df};
+  const void* req[] = {q, k, v, gate ? gate->a : f, dy, dq, dk, dv, dfa};
   for (const void* x : req)
     if ((rc = check_ptr(x, dev, true)) != M2RNN_OK) return rc;
   if ((rc = check_ptr(ckpt, dev, false)) != M2RNN_OK) return rc;
@@ -493,8 +520,8 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   if (own) {  // checkpoints at interval C into the workspace (no y written)
     m2rnn_shape sf = *s;
     sf.ckpt_every = C;
-    rc = run_fwd(&sf, q, k, v, f, W, w_r, H0, nullptr, nullptr, static_cast<float*>(workspace), st,
-                 status, sms);
+    rc = run_fwd(&sf, q, k, v, f, gate, W, w_r, H0, nullptr, nullptr,
+                 static_cast<float*>(workspace), st, status, sms);
     if (rc != M2RNN_OK) return rc;
     ck = static_cast<const float*>(workspace);
   }
@@ -502,7 +529,7 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   p.q = q;
   p.k = k;
   p.v = v;
-  p.f = f;
+  p.f = gate ? nullptr : f;
   p.W = W;
   p.w_r = w_r;
   p.ckpt = ck;
@@ -511,11 +538,19 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  p.df = df;
+  p.df = dfa;
   p.dW = dW;
   p.dw_r = dw_r;
   p.dH0 = dH0;
   p.dckpt = dckpt;
+  if (gate != nullptr) {
+    p.a = gate->a;
+    p.alpha = gate->alpha;
+    p.beta = gate->beta;
+    p.gated = 1;
+    p.dalpha = dalpha;
+    p.dbeta = dbeta;
+  }
   p.dck_ratio = s->ckpt_every / C;
   p.dck_n = static_cast<int>(m2rnn_num_checkpoints(s));
   p.B = s->B;
@@ -534,11 +569,56 @@ int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v,
       cudaMemsetAsync(dk, 0, BT * s->K * sizeof(float), st) != cudaSuccess)
     return M2RNN_ERR_CUDA;
   if (p.nslices > 1 && (cudaMemsetAsync(dv, 0, BT * NV * sizeof(float), st) != cudaSuccess ||
-                        cudaMemsetAsync(df, 0, BT * s->N * sizeof(float), st) != cudaSuccess))
+                        cudaMemsetAsync(dfa, 0, BT * s->N * sizeof(float), st) != cudaSuccess))
     return M2RNN_ERR_CUDA;
-  (void)es;
   return status_from_cuda(p.pipe ? m2rnn::launch_bwd_pipe(p, s->V, f32, st)
                                 : m2rnn::launch_bwd(p, s->V, f32, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int m2rnn_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
+              const void* W, const void* w_r, const float* H0, void* y, float* H_T, float* ckpt,
+              void* stream) {
+  return fwd_impl(s, q, k, v, f, nullptr, W, w_r, H0, y, H_T, ckpt, stream);
+}
+
+int m2rnn_fwd_gated(const m2rnn_shape* s, const void* q, const void* k, const void* v,
+                    const void* a, const void* alpha, const void* beta, const void* W,
+                    const void* w_r, const float* H0, void* y, float* H_T, float* ckpt,
+                    void* stream) {
+  const Gate gate{a, alpha, beta};
+  return fwd_impl(s, q, k, v, nullptr, &gate, W, w_r, H0, y, H_T, ckpt, stream);
+}
+
+size_t m2rnn_bwd_workspace_size(const m2rnn_shape* s, int ckpt_given) {
+  if (check_shape(s) != M2RNN_OK || s->ckpt_every <= 0 || s->T == 0) return 0;
+  bool own = false;
+  const int C = bwd_interval(s, ckpt_given != 0, &own);
+  if (!own) return 0;
+  const size_t nck = static_cast<size_t>((s->T + C - 1) / C);
+  return align256(static_cast<size_t>(s->B) * s->N * nck * s->K * s->V * sizeof(float));
+}
+
+int m2rnn_bwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
+              const void* W, const void* w_r, const float* H0, const float* ckpt, const void* dy,
+              const float* dH_T, float* dq, float* dk, float* dv, float* df, float* dW, float* dw_r,
+              float* dH0, float* dckpt, void* workspace, size_t ws_bytes, void* stream) {
+  return bwd_impl(s, q, k, v, f, nullptr, W, w_r, H0, ckpt, dy, dH_T, dq, dk, dv, df, nullptr,
+                  nullptr, dW, dw_r, dH0, dckpt, workspace, ws_bytes, stream);
+}
+
+int m2rnn_bwd_gated(const m2rnn_shape* s, const void* q, const void* k, const void* v,
+                    const void* a, const void* alpha, const void* beta, const void* W,
+                    const void* w_r, const float* H0, const float* ckpt, const void* dy,
+                    const float* dH_T, float* dq, float* dk, float* dv, float* da, float* dalpha,
+                    float* dbeta, float* dW, float* dw_r, float* dH0, float* dckpt,
+                    void* workspace, size_t ws_bytes, void* stream) {
+  const Gate gate{a, alpha, beta};
+  return bwd_impl(s, q, k, v, nullptr, &gate, W, w_r, H0, ckpt, dy, dH_T, dq, dk, dv, da, dalpha,
+                  dbeta, dW, dw_r, dH0, dckpt, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

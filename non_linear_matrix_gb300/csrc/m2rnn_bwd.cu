@@ -45,6 +45,7 @@
 #include "m2rnn_internal.h"
 #include "ptx.cuh"
 #include "m2rnn_bwd_common.cuh"
+#include "m2rnn_gate.cuh"
 
 namespace m2rnn {
 namespace {
@@ -103,7 +104,7 @@ __host__ __device__ inline BwdLayout bwd_layout(int V, int C, int S2, int WPC, i
   return L;
 }
 
-template <int V, bool F32>
+template <int V, bool F32, bool GATED>
 __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   using TIn = typename InT<F32>::T;
   constexpr int es = sizeof(TIn);
@@ -125,7 +126,12 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   const TIn* q = static_cast<const TIn*>(p.q);
   const TIn* kin = static_cast<const TIn*>(p.k);
   const TIn* vin = static_cast<const TIn*>(p.v);
-  const TIn* fin = static_cast<const TIn*>(p.f);
+  // f, or with the fused input gate its input a (same layout and dtype)
+  constexpr bool gated = GATED;
+  const TIn* fin = static_cast<const TIn*>(gated ? p.a : p.f);
+  const float g_alpha = gated ? tof(static_cast<const TIn*>(p.alpha)[n]) : 0.f;
+  const float g_beta = gated ? tof(static_cast<const TIn*>(p.beta)[n]) : 0.f;
+  float dalpha_acc = 0.f, dbeta_acc = 0.f;  // gate parameter sums of this thread's steps
   const TIn* dy = static_cast<const TIn*>(p.dy);
   const TIn* Wn = static_cast<const TIn*>(p.W) + static_cast<size_t>(n) * V * V;
   const TIn* wr = static_cast<const TIn*>(p.w_r) + static_cast<size_t>(n) * V;
@@ -218,8 +224,10 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
       const uint4 a = __ldg(reinterpret_cast<const uint4*>(vin + ((bt0 + s) * N + n) * V) + x);
       sts_u32x4(vb + static_cast<uint32_t>(s * V * es + 16 * x), a.x, a.y, a.z, a.w);
     }
-    for (int s = tid; s < Lc; s += nthr)
-      ptx::sts_f32(sb + L.in_f + buf * L.fbuf + 4 * s, tof(fin[(bt0 + s) * N + n]));
+    for (int s = tid; s < Lc; s += nthr) {
+      const float x = tof(fin[(bt0 + s) * N + n]);
+      ptx::sts_f32(sb + L.in_f + buf * L.fbuf + 4 * s, gated ? gate_f(x, g_alpha, g_beta) : x);
+    }
   };
   // checkpoint H_{ci C} of this thread's elements
   auto load_ckpt = [&](int ci, float (&H)[NT][4]) {
@@ -500,6 +508,13 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
         for (int i = tid; i < Ls; i += nthr) {
           float acc = 0.f;
           for (int w = 0; w < WPC; ++w) acc += ptx::lds_f32(rf + static_cast<uint32_t>((i * WPC + w) * 4));
+          if (gated) {  // chain rule through the gate: this slice's share of da, dalpha, dbeta
+            float gf, gda, gdal;
+            gate_f_grads(tof(fin[(bt + i) * N + n]), g_alpha, g_beta, gf, gda, gdal);
+            dalpha_acc = fmaf(acc, gdal, dalpha_acc);
+            acc *= gda;
+            dbeta_acc += acc;
+          }
           float* dst = p.df + (bt + i) * N + n;
           if (p.nslices == 1)
             *dst = acc;
@@ -553,12 +568,16 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   }
   // each thread holds the u (.) v sum of column tid % V over the steps it flushed
   if (slice == 0) red_add(p.dw_r + static_cast<size_t>(n) * V + tid % V, dwr_acc);
+  if (gated && tid < S2) {  // the threads that flushed df
+    red_add(p.dalpha + n, dalpha_acc);
+    red_add(p.dbeta + n, dbeta_acc);
+  }
 }
 
 template <int V, bool F32>
 cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2);
-  auto kern = bwd_kernel<V, F32>;
+  auto kern = p.gated ? bwd_kernel<V, F32, true> : bwd_kernel<V, F32, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L.total));
   if (e != cudaSuccess) return e;
@@ -570,7 +589,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
 template <int V, bool F32>
 int bwd_ctas_per_sm_t(const BwdParams& p) {
   const BwdLayout L = bwd_layout(V, p.C, sub_len<V, F32>(), p.WPC, F32 ? 4 : 2);
-  auto kern = bwd_kernel<V, F32>;
+  auto kern = p.gated ? bwd_kernel<V, F32, true> : bwd_kernel<V, F32, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(L.total)) != cudaSuccess)
     return 0;

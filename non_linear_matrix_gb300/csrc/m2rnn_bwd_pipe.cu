@@ -42,6 +42,7 @@
 
 #include "m2rnn.h"
 #include "m2rnn_bwd_common.cuh"
+#include "m2rnn_gate.cuh"
 #include "m2rnn_internal.h"
 #include "ptx.cuh"
 
@@ -64,6 +65,7 @@ struct PipeLayout {
   uint32_t uf;  // as vf, for dy
   uint32_t ub;  // as vb, for dy
   uint32_t fr;  // [S2] fp32 f
+  uint32_t gd, gl;  // [S2] fp32 df/da and df/dalpha of the fused input gate
   // ... and the steps of the interval recomputed alongside
   uint32_t lkd, lvf, lfr;
   uint32_t raw;         // one slot's inputs as copied: q, k, k' [S2][RS], v, dy, v' [S2][V]
@@ -76,7 +78,7 @@ struct PipeLayout {
 
 __host__ __device__ constexpr uint32_t al128(uint32_t x) { return (x + 127u) / 128u * 128u; }
 
-__host__ __device__ constexpr PipeLayout pipe_layout(int V, int S2, int WPC, int es) {
+__host__ __device__ constexpr PipeLayout pipe_layout(int V, int S2, int WPC, int es, bool gated) {
   const uint32_t NT = V / 8, KS = V / 16;
   PipeLayout L{};
   uint32_t b = 0;
@@ -96,6 +98,10 @@ __host__ __device__ constexpr PipeLayout pipe_layout(int V, int S2, int WPC, int
   b = al128(b + S2 * 4 * KS * 8);
   L.fr = b;
   b = al128(b + S2 * 4);
+  L.gd = b;  // (the gate's arrays exist in gated launches only)
+  b = gated ? al128(b + S2 * 4) : b;
+  L.gl = b;
+  b = gated ? al128(b + S2 * 4) : b;
   L.lkd = b;
   b = al128(b + WPC * S2 * 8 * 16);
   L.lvf = b;
@@ -119,10 +125,11 @@ __host__ __device__ constexpr PipeLayout pipe_layout(int V, int S2, int WPC, int
   L.subck = o;
   return L;
 }
-__host__ __device__ constexpr uint32_t pipe_smem_total(int V, int C, int S2, int WPC, int es) {
+__host__ __device__ constexpr uint32_t pipe_smem_total(int V, int C, int S2, int WPC, int es,
+                                                       bool gated) {
   const uint32_t NS1 = (C + S2 - 1) / S2;
   const uint32_t sub = NS1 * WPC * (V / 8) * 512, dws = WPC * V * V * 4;
-  return pipe_layout(V, S2, WPC, es).subck + al128(sub > dws ? sub : dws);
+  return pipe_layout(V, S2, WPC, es, gated).subck + al128(sub > dws ? sub : dws);
 }
 
 // One forward step with the forward kernel's operations (rank-1 k v^T in fp32
@@ -211,7 +218,7 @@ __device__ __forceinline__ int step_of_lane(int lane) {
   return idx;
 }
 
-template <int V, bool F32, int WPC>
+template <int V, bool F32, int WPC, bool GATED>
 __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
   using TIn = typename InT<F32>::T;
   constexpr int es = sizeof(TIn);
@@ -228,13 +235,18 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
   const int b = bn / N, n = bn % N;
   const int row0c = slice * RS;        // first row of this CTA
   const int row0 = row0c + 16 * warp;  // first row of this warp
-  constexpr PipeLayout L = pipe_layout(V, S2, WPC, es);
+  constexpr PipeLayout L = pipe_layout(V, S2, WPC, es, GATED);
   const uint32_t sb = ptx::smem_addr(smem);
 
   const TIn* q = static_cast<const TIn*>(p.q);
   const TIn* kin = static_cast<const TIn*>(p.k);
   const TIn* vin = static_cast<const TIn*>(p.v);
-  const TIn* fin = static_cast<const TIn*>(p.f);
+  // f, or with the fused input gate its input a (same layout and dtype)
+  constexpr bool gated = GATED;
+  const TIn* fin = static_cast<const TIn*>(gated ? p.a : p.f);
+  const float g_alpha = gated ? tof(static_cast<const TIn*>(p.alpha)[n]) : 0.f;
+  const float g_beta = gated ? tof(static_cast<const TIn*>(p.beta)[n]) : 0.f;
+  float dalpha_acc = 0.f, dbeta_acc = 0.f;  // gate parameter sums of this thread's steps
   const TIn* dy = static_cast<const TIn*>(p.dy);
   const TIn* Wn = static_cast<const TIn*>(p.W) + static_cast<size_t>(n) * V * V;
   const TIn* wr = static_cast<const TIn*>(p.w_r) + static_cast<size_t>(n) * V;
@@ -474,6 +486,15 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
           const SlotRange sr = slot_range(ci2, jj2, wantR);
           const size_t idx = ((isR ? sr.tR : sr.tL) + i) * N + n;
           fv = (idx & 1) ? ptx::bf16x2_hi(wbits) : ptx::bf16x2_lo(wbits);
+        }
+        if (gated) {  // fv is a: f and, for reversed steps, its derivatives
+          float gf, gda, gdal;
+          gate_f_grads(fv, g_alpha, g_beta, gf, gda, gdal);
+          fv = gf;
+          if (isR) {
+            ptx::sts_f32(B0 + L.gd + 4 * i, gda);
+            ptx::sts_f32(B0 + L.gl + 4 * i, gdal);
+          }
         }
         ptx::sts_f32(B0 + (isR ? L.fr : L.lfr) + 4 * i, fv);
       }
@@ -786,6 +807,12 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
         float acc = 0.f;
 #pragma unroll
         for (int w = 0; w < WPC; ++w) acc += ptx::lds_f32(rf + static_cast<uint32_t>((i * WPC + w) * 4));
+        if (gated) {  // chain rule through the gate: this slice's share of da, dalpha, dbeta
+          const float gda = ptx::lds_f32(B0 + L.gd + 4 * i);
+          dalpha_acc = fmaf(acc, ptx::lds_f32(B0 + L.gl + 4 * i), dalpha_acc);
+          acc *= gda;
+          dbeta_acc += acc;
+        }
         float* dst = p.df + (bt + i) * N + n;
         if (p.nslices == 1)
           *dst = acc;
@@ -853,12 +880,16 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
   }
   // each thread holds the u (.) v sum of column tid % V over the steps it flushed
   if (slice == 0) red_add(p.dw_r + static_cast<size_t>(n) * V + tid % V, dwr_acc);
+  if (gated && dt >= 0 && dt < S2) {
+    red_add(p.dalpha + n, dalpha_acc);
+    red_add(p.dbeta + n, dbeta_acc);
+  }
 }
 
 template <int V, bool F32, int WPC>
 cudaError_t launch_pipe_t(const BwdParams& p, cudaStream_t stream) {
-  const uint32_t smem = pipe_smem_total(V, p.C, sub_len<V, F32>(), WPC, F32 ? 4 : 2);
-  auto kern = bwd_pipe_kernel<V, F32, WPC>;
+  const uint32_t smem = pipe_smem_total(V, p.C, sub_len<V, F32>(), WPC, F32 ? 4 : 2, p.gated);
+  auto kern = p.gated ? bwd_pipe_kernel<V, F32, WPC, true> : bwd_pipe_kernel<V, F32, WPC, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -869,8 +900,8 @@ cudaError_t launch_pipe_t(const BwdParams& p, cudaStream_t stream) {
 
 template <int V, bool F32, int WPC>
 int pipe_ctas_per_sm_t(const BwdParams& p) {
-  const uint32_t smem = pipe_smem_total(V, p.C, sub_len<V, F32>(), WPC, F32 ? 4 : 2);
-  auto kern = bwd_pipe_kernel<V, F32, WPC>;
+  const uint32_t smem = pipe_smem_total(V, p.C, sub_len<V, F32>(), WPC, F32 ? 4 : 2, p.gated);
+  auto kern = p.gated ? bwd_pipe_kernel<V, F32, WPC, true> : bwd_pipe_kernel<V, F32, WPC, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return 0;
@@ -906,8 +937,8 @@ cudaError_t launch_pipe_w(const BwdParams& p, cudaStream_t stream) {
 
 bool bwd_has_pipe(int V) { return V == 16; }
 
-size_t bwd_pipe_smem_bytes(int V, int C, int WPC, bool f32_inputs) {
-  return pipe_smem_total(V, C, bwd_sub_len(V, f32_inputs), WPC, f32_inputs ? 4 : 2);
+size_t bwd_pipe_smem_bytes(int V, int C, int WPC, bool f32_inputs, bool gated) {
+  return pipe_smem_total(V, C, bwd_sub_len(V, f32_inputs), WPC, f32_inputs ? 4 : 2, gated);
 }
 
 int bwd_pipe_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs) {

@@ -45,6 +45,7 @@
 
 #include "m2rnn_internal.h"
 #include "ptx.cuh"
+#include "m2rnn_gate.cuh"
 
 namespace m2rnn {
 namespace {
@@ -137,7 +138,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
 // ---------------------------------------------------------------------------
 // producer warp
 // ---------------------------------------------------------------------------
-template <int V, bool F32>
+template <int V, bool F32, bool GATED>
 __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout& L, uint32_t sbase,
                                              int b, int n0, int Geff) {
   using TIn = typename InType<F32>::T;
@@ -150,10 +151,13 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
   const TIn* q = static_cast<const TIn*>(p.q);
   const TIn* k = static_cast<const TIn*>(p.k);
   const TIn* v = static_cast<const TIn*>(p.v);
-  const TIn* f = static_cast<const TIn*>(p.f);
+  // f, or (GATED) the input gate's a, with alpha and beta per head
+  const TIn* f = static_cast<const TIn*>(GATED ? p.a : p.f);
+  const TIn* galpha = static_cast<const TIn*>(p.alpha);
+  const TIn* gbeta = static_cast<const TIn*>(p.beta);
 
   // Waits for a free stage, starts the bulk copies of chunk ch and writes
-  // its f as fp32 pairs.
+  // its f (or, gated, f computed from a) as fp32 pairs.
   auto issue = [&](int ch) -> bool {
     const int s = ch % NSTAGE;
     if (!warp_wait(bar_in_empty(bars, s), ((ch / NSTAGE) & 1) ^ 1, p.wait_limit_ns)) return false;
@@ -181,7 +185,12 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
       for (int i = 0; i < 8; ++i) {
         const int e = base + lane + 32 * i;
         const int tl = e / Geff, h = e - tl * Geff;
-        fv[i] = e < nf ? to_f(f[(bt0 + tl) * N + n0 + h]) : 0.f;
+        if constexpr (GATED)
+          fv[i] = e < nf ? gate_f(to_f(f[(bt0 + tl) * N + n0 + h]), to_f(galpha[n0 + h]),
+                                  to_f(gbeta[n0 + h]))
+                         : 0.f;
+        else
+          fv[i] = e < nf ? to_f(f[(bt0 + tl) * N + n0 + h]) : 0.f;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -662,7 +671,7 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
   if (p.HT != nullptr) store_state<V, MT, HALF>(p.HT + hoff, S.H, row0, g, c);
 }
 
-template <int V, int MT, bool F32>
+template <int V, int MT, bool F32, bool GATED>
 __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1)
     fwd_kernel(const FwdParams p) {
   using TIn = typename InType<F32>::T;
@@ -691,7 +700,7 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
   if (warp == 0) {
     // With fault injection on, the producer issues nothing, so every wait of
     // the other warps runs into its time limit (tests of the time-out path).
-    if (p.inject_stall == 0) fwd_producer<V, F32>(p, L, sbase, b, n0, Geff);
+    if (p.inject_stall == 0) fwd_producer<V, F32, GATED>(p, L, sbase, b, n0, Geff);
   } else if (warp == 1) {
     fwd_epilogue<V, F32>(p, L, sbase, b, n0, Geff);
   } else if (warp - 2 < ncons) {
@@ -702,7 +711,7 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
 template <int V, int MT, bool F32>
 int ctas_per_sm_t(const FwdParams& p) {
   const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc);
-  auto kern = fwd_kernel<V, MT, F32>;
+  auto kern = p.gated ? fwd_kernel<V, MT, F32, true> : fwd_kernel<V, MT, F32, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(L.total)) != cudaSuccess)
     return 0;
@@ -718,7 +727,7 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
   const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc);
   if (p.tc < 2 || p.tc > 32) return cudaErrorInvalidValue;
   if (p.G * p.WPH > max_consumer_warps<V, MT, F32>()) return cudaErrorInvalidConfiguration;
-  auto kern = fwd_kernel<V, MT, F32>;
+  auto kern = p.gated ? fwd_kernel<V, MT, F32, true> : fwd_kernel<V, MT, F32, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L.total));
   if (e != cudaSuccess) return e;

@@ -39,6 +39,12 @@ struct FwdParams {
   int* status;
   unsigned long long wait_limit_ns;
   int inject_stall;  // test hook: 1 = the producer issues nothing
+  // fused input gate (gated = 1): f = exp(-alpha softplus(a + beta)) from
+  // a [B,T,N] and alpha, beta [N] (input dtype) instead of f
+  const void* a = nullptr;
+  const void* alpha = nullptr;
+  const void* beta = nullptr;
+  int gated = 0;
 };
 
 struct BwdParams {
@@ -69,6 +75,15 @@ struct BwdParams {
   int S2;       // sub-interval length of the recomputation (= bwd_sub_len)
   int pipe;     // 1: the pipelined kernel (m2rnn_bwd_pipe.cu, V = 16); 0: the
                 // serial one (m2rnn_bwd.cu)
+  // fused input gate (gated = 1): f from a, alpha, beta as in FwdParams; df
+  // then receives dL/da, and dalpha, dbeta [N] (zeroed by the caller) are
+  // accumulated
+  const void* a = nullptr;
+  const void* alpha = nullptr;
+  const void* beta = nullptr;
+  int gated = 0;
+  float* dalpha = nullptr;
+  float* dbeta = nullptr;
 };
 
 cudaError_t launch_bwd(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream);
@@ -77,7 +92,7 @@ size_t bwd_smem_bytes(int V, int C, int S2, int WPC, bool f32_inputs);
 
 // Pipelined backward kernel.
 bool bwd_has_pipe(int V);
-size_t bwd_pipe_smem_bytes(int V, int C, int WPC, bool f32_inputs);
+size_t bwd_pipe_smem_bytes(int V, int C, int WPC, bool f32_inputs, bool gated);
 int bwd_pipe_ctas_per_sm(const BwdParams& p, int V, bool f32_inputs);
 cudaError_t launch_bwd_pipe(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream);
 int bwd_sub_len(int V, bool f32_inputs);  // sub-interval length of the variant

@@ -40,6 +40,8 @@ _EXPORTS = {
     "m2rnn_set_fault_injection": (ctypes.c_int, [ctypes.c_int]),
     "m2rnn_bwd_noalloc": (ctypes.c_int, [_VP] * 18),
     "m2rnn_decode": (ctypes.c_int, [_VP] * 11),
+    "m2rnn_fwd_gated": (ctypes.c_int, [_VP] * 14),
+    "m2rnn_bwd_gated": (ctypes.c_int, [_VP] * 24 + [ctypes.c_size_t, _VP]),
 }
 
 
@@ -143,6 +145,33 @@ def fwd(q, k, v, f, W, w_r, H0=None, *, ckpt_every: int = 0, want_HT: bool = Tru
     return y, HT, ck
 
 
+def fwd_gated(q, k, v, a, alpha, beta, W, w_r, H0=None, *, ckpt_every: int = 0,
+              want_HT: bool = True, out=None, stream=None):
+    """Forward pass with the fused input gate f = exp(-alpha softplus(a + beta)),
+    computed inside the kernel.  a [B,T,N]; alpha, beta [N]; the rest as for
+    ``fwd``.  Returns (y, H_T or None, ckpt or None)."""
+    s = make_shape(q, v, ckpt_every)
+    for t in (k, v, a, alpha, beta, W, w_r):
+        if t.dtype != q.dtype:
+            raise TypeError("q, k, v, a, alpha, beta, W, w_r must share one dtype")
+    out = dict(out or {})
+    y = out.get("y")
+    if y is None:
+        y = torch.empty_like(v)
+    HT = out.get("HT")
+    if HT is None and want_HT:
+        HT = torch.empty(s.B, s.N, s.K, s.V, device=q.device, dtype=torch.float32)
+    ck = out.get("ckpt")
+    nck = num_checkpoints(s)
+    if ck is None and nck > 0:
+        ck = torch.empty(s.B, s.N, nck, s.K, s.V, device=q.device, dtype=torch.float32)
+    rc = lib().m2rnn_fwd_gated(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(alpha),
+                               _ptr(beta), _ptr(W), _ptr(w_r), _ptr(H0), _ptr(y), _ptr(HT),
+                               _ptr(ck), _stream(stream))
+    _check(rc, "m2rnn_fwd_gated")
+    return y, HT, ck
+
+
 def decode(q, k, v, f, W, w_r, H, *, H_out=None, y=None, stream=None):
     """One decode step for B sequences.  Returns (y, H_out).
 
@@ -233,6 +262,43 @@ def bwd_noalloc(q, k, v, f, W, w_r, dy, H0=None, dHT=None, *, ckpt_every: int = 
     _check(rc, "m2rnn_bwd_noalloc")
     if dH0 is not None:
         g["dH0"] = dH0
+    return g
+
+
+def bwd_gated(q, k, v, a, alpha, beta, W, w_r, dy, H0=None, ckpt=None, dHT=None, *,
+              ckpt_every: int = 64, want_dH0: bool = False, want_dckpt: bool = False,
+              workspace=None, out=None, stream=None):
+    """BPTT backward through the fused input gate.  Returns dict(dq, dk, dv,
+    da, dalpha, dbeta, dW, dw_r[, dH0][, dckpt]) (fp32); ``ckpt`` must come
+    from ``fwd_gated`` with the same inputs."""
+    s = make_shape(q, v, ckpt_every)
+    f32 = dict(device=q.device, dtype=torch.float32)
+    out = dict(out or {})
+    shapes = {"dq": (s.B, s.T, s.K), "dk": (s.B, s.T, s.K), "dv": (s.B, s.T, s.N, s.V),
+              "da": (s.B, s.T, s.N), "dalpha": (s.N,), "dbeta": (s.N,),
+              "dW": (s.N, s.V, s.V), "dw_r": (s.N, s.V)}
+    g = {n: out.get(n) if out.get(n) is not None else torch.empty(shp, **f32)
+         for n, shp in shapes.items()}
+    dH0 = out.get("dH0")
+    if dH0 is None and want_dH0:
+        dH0 = torch.empty(s.B, s.N, s.K, s.V, **f32)
+    dck = out.get("dckpt")
+    if dck is None and want_dckpt:
+        dck = torch.empty(s.B, s.N, num_checkpoints(s), s.K, s.V, **f32)
+    need = bwd_workspace_size(s, ckpt is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    rc = lib().m2rnn_bwd_gated(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(alpha),
+                               _ptr(beta), _ptr(W), _ptr(w_r), _ptr(H0), _ptr(ckpt), _ptr(dy),
+                               _ptr(dHT), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                               _ptr(g["da"]), _ptr(g["dalpha"]), _ptr(g["dbeta"]), _ptr(g["dW"]),
+                               _ptr(g["dw_r"]), _ptr(dH0), _ptr(dck), _ptr(workspace),
+                               ctypes.c_size_t(workspace.numel()), _stream(stream))
+    _check(rc, "m2rnn_bwd_gated")
+    if dH0 is not None:
+        g["dH0"] = dH0
+    if dck is not None:
+        g["dckpt"] = dck
     return g
 
 

@@ -92,3 +92,16 @@ def test_decode_rejects_bad_arguments_before_launch(lib):
     assert lib.m2rnn_decode(ctypes.byref(Shape(4, 2, 2, 64, 16, 1, 0)), *([p] * 10)) == -1
     assert lib.m2rnn_decode(ctypes.byref(Shape(4, 1, 2, 48, 16, 1, 0)), *([p] * 10)) == -2
     assert lib.m2rnn_decode(None, *([p] * 10)) == -1
+
+
+def test_gated_entry_points_reject_bad_shapes_before_launch(lib):
+    from non_linear_matrix_gb300.m2rnn import Shape
+    p = ctypes.c_void_p(16)
+    bad = ctypes.byref(Shape(1, 8, 2, 48, 16, 1, 4))
+    assert lib.m2rnn_fwd_gated(bad, *([p] * 8), None, p, None, None, None) == -2
+    assert lib.m2rnn_fwd_gated(None, *([p] * 8), None, p, None, None, None) == -1
+    assert lib.m2rnn_bwd_gated(bad, *([p] * 8), None, None, p, None, *([p] * 8), None, None, p,
+                               ctypes.c_size_t(1 << 20), None) == -2
+    nock = ctypes.byref(Shape(1, 8, 2, 64, 16, 1, 0))  # ckpt_every must be > 0
+    assert lib.m2rnn_bwd_gated(nock, *([p] * 8), None, None, p, None, *([p] * 8), None, None, p,
+                               ctypes.c_size_t(1 << 20), None) == -1
