@@ -10,8 +10,9 @@ value head, frame "Shared queries and keys buy more recurrent capacity";
 share a 100B-token training protocol"; long contexts to 16K and beyond):
 
   torch CPU generator seeded with ``seed``; draws in this order, all fp32:
-    q  ~ N(0,1) [B,T,K], then L2-normalised over K (shared by all heads)
-    k  ~ N(0,1) [B,T,K], then L2-normalised over K
+    q  ~ N(0,1) [B,T,K], then L2-normalised over K (shared by all heads);
+                            [B,T,G,K] with G > 1 query/key groups
+    k  ~ N(0,1) [B,T,K] (or [B,T,G,K]), then L2-normalised over K
     v  ~ N(0,1)/4 [B,T,N,V]
     f  = sigmoid(N(f_mean, 1)) [B,T,N]
     W  ~ N(0, 1/V) [N,V,V]
@@ -77,13 +78,14 @@ TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 def make_inputs(B: int, T: int, N: int, K: int, V: int, dtype: str = "bf16",
                 seed: int = 0, f_mean: float = 2.0, with_dy: bool = False,
-                gated: bool = False) -> dict:
+                gated: bool = False, groups: int = 1) -> dict:
     """Draw one seeded input set on the CPU (see the module docstring)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
-    q = torch.randn(B, T, K, generator=g)
+    qk_shape = (B, T, K) if groups == 1 else (B, T, groups, K)
+    q = torch.randn(*qk_shape, generator=g)
     q = q / q.norm(dim=-1, keepdim=True).clamp_min(1e-12)
-    k = torch.randn(B, T, K, generator=g)
+    k = torch.randn(*qk_shape, generator=g)
     k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
     v = torch.randn(B, T, N, V, generator=g) / 4.0
     f = torch.sigmoid(torch.randn(B, T, N, generator=g) + f_mean)

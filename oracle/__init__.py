@@ -15,6 +15,15 @@ arrays to contiguous float64 and marshals pointers.
 Layouts: q, k [B,T,K]; v [B,T,N,V]; f [B,T,N]; W [N,V,V] with
 (H W)_{ij} = sum_l H_{il} W_{lj}; w_r [N,V]; H0/H_T [B,N,K,V]; y [B,T,N,V].
 
+Grouped queries and keys (frame "Tensor parallelism trades topology
+dependence for sync": one query/key group per group of value heads, N_q =
+N_k = G): q and k may be given as [B,T,G,K] with G dividing N.  Value head n
+then reads group n // (N / G) (contiguous blocks of N / G heads, one block
+per tensor-parallel rank in the deck's topology-aware form), and dq, dk are
+[B,T,G,K], summed over the heads of each group.  Each group is an
+independent problem with N_q = 1, so fwd / bwd run the C routines once per
+group on that group's slices.
+
 The gated functions follow the frame "The gate preserves a direct path
 through time": f_{t,n} = exp(-alpha_n softplus(a_{t,n} + beta_n)), with a
 [B,T,N] and alpha, beta [N].  They compute f (and the gate's derivatives) in
@@ -90,11 +99,31 @@ def _dims(q, v):
     return B, T, N, K, V
 
 
+def _groups(q, v):
+    """Head blocks [(group, first head, last head + 1)] of grouped q/k."""
+    G, N = q.shape[2], v.shape[2]
+    if N % G != 0:
+        raise ValueError(f"{G} q/k groups do not divide {N} value heads")
+    hpg = N // G
+    return [(g, g * hpg, (g + 1) * hpg) for g in range(G)]
+
+
 def fwd(q, k, v, f, W, w_r, H0=None, want_states: bool = False):
     """Forward pass.  Returns dict(y, HT[, states]) as float64 arrays.
 
-    ``states`` (if requested) holds H_0..H_T as [B,N,T+1,K,V]."""
+    ``states`` (if requested) holds H_0..H_T as [B,N,T+1,K,V].  q, k are
+    [B,T,K] (shared by all heads) or [B,T,G,K] (grouped)."""
     q, k, v, f, W, w_r, H0 = map(_f64, (q, k, v, f, W, w_r, H0))
+    if q.ndim == 4:  # grouped: one N_q = 1 problem per group of heads
+        parts = [(h0, h1, fwd(q[:, :, g], k[:, :, g], v[:, :, h0:h1], f[:, :, h0:h1],
+                              W[h0:h1], w_r[h0:h1], None if H0 is None else H0[:, h0:h1],
+                              want_states))
+                 for g, h0, h1 in _groups(q, v)]
+        out = {"y": np.concatenate([r["y"] for *_, r in parts], axis=2),
+               "HT": np.concatenate([r["HT"] for *_, r in parts], axis=1)}
+        if want_states:
+            out["states"] = np.concatenate([r["states"] for *_, r in parts], axis=1)
+        return out
     B, T, N, K, V = _dims(q, v)
     y = np.zeros((B, T, N, V))
     HT = np.zeros((B, N, K, V))
@@ -111,8 +140,18 @@ def fwd(q, k, v, f, W, w_r, H0=None, want_states: bool = False):
 
 
 def bwd(q, k, v, f, W, w_r, dy, H0=None, dHT=None):
-    """BPTT backward.  Returns dict(dq, dk, dv, df, dW, dw_r, dH0) (float64)."""
+    """BPTT backward.  Returns dict(dq, dk, dv, df, dW, dw_r, dH0) (float64);
+    with grouped q, k ([B,T,G,K]) dq and dk are [B,T,G,K]."""
     q, k, v, f, W, w_r, dy, H0, dHT = map(_f64, (q, k, v, f, W, w_r, dy, H0, dHT))
+    if q.ndim == 4:  # grouped: one N_q = 1 problem per group of heads
+        sl = lambda a, h0, h1: None if a is None else a[:, h0:h1]  # noqa: E731
+        parts = [bwd(q[:, :, g], k[:, :, g], v[:, :, h0:h1], f[:, :, h0:h1], W[h0:h1],
+                     w_r[h0:h1], dy[:, :, h0:h1], sl(H0, h0, h1), sl(dHT, h0, h1))
+                 for g, h0, h1 in _groups(q, v)]
+        out = {n: np.stack([r[n] for r in parts], axis=2) for n in ("dq", "dk")}
+        for n, ax in (("dv", 2), ("df", 2), ("dW", 0), ("dw_r", 0), ("dH0", 1)):
+            out[n] = np.concatenate([r[n] for r in parts], axis=ax)
+        return out
     B, T, N, K, V = _dims(q, v)
     out = {
         "dq": np.zeros((B, T, K)), "dk": np.zeros((B, T, K)),

@@ -287,3 +287,81 @@ def test_gated_backward_matches_central_differences(oracle_mod, T):
             fd[idx] = (lp - lm) / (2 * h)
         err = np.abs(g[gname] - fd).max() / max(1.0, np.abs(fd).max())
         assert err <= 1e-6, (gname, err)
+
+
+# --- grouped queries and keys (frame "Tensor parallelism trades topology
+# dependence for sync": one query/key group per block of value heads) -------
+
+def test_grouped_identical_groups_equal_shared(oracle_mod):
+    """Every group given the same q, k is the shared form N_q = 1: y, H_T
+    and all parameter gradients agree, and the shared dq, dk are the sums of
+    the per-group ones (the heads of a group sum into its dq, dk)."""
+    x = make_inputs(2, 5, 6, 8, 4, "f32", 41, with_dy=True)
+    G = 3
+    qg = x["q"][:, :, None].expand(-1, -1, G, -1).contiguous()
+    kg = x["k"][:, :, None].expand(-1, -1, G, -1).contiguous()
+    rng = np.random.default_rng(2)
+    H0 = rng.uniform(-0.5, 0.5, size=(2, 6, 8, 4))
+    a = oracle_mod.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], H0=H0)
+    b = oracle_mod.fwd(qg, kg, x["v"], x["f"], x["W"], x["w_r"], H0=H0)
+    np.testing.assert_allclose(b["y"], a["y"], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(b["HT"], a["HT"], rtol=0, atol=1e-15)
+    ga = oracle_mod.bwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], x["dy"], H0=H0)
+    gb = oracle_mod.bwd(qg, kg, x["v"], x["f"], x["W"], x["w_r"], x["dy"], H0=H0)
+    assert gb["dq"].shape == (2, 5, G, 8)
+    np.testing.assert_allclose(gb["dq"].sum(axis=2), ga["dq"], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(gb["dk"].sum(axis=2), ga["dk"], rtol=1e-12, atol=1e-14)
+    for n in ("dv", "df", "dW", "dw_r", "dH0"):
+        np.testing.assert_allclose(gb[n], ga[n], rtol=1e-12, atol=1e-14)
+
+
+def test_grouped_head_blocks(oracle_mod):
+    """Value head n reads group n // (N / G): with N = 4, G = 2, heads 0-1
+    use group 0 and heads 2-3 group 1.  Each block run alone as a shared
+    problem with its group's q, k gives the same outputs."""
+    x = make_inputs(2, 6, 4, 8, 4, "f32", 43, with_dy=True, groups=2)
+    o = oracle_mod.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"])
+    for grp, heads in ((0, slice(0, 2)), (1, slice(2, 4))):
+        r = oracle_mod.fwd(x["q"][:, :, grp], x["k"][:, :, grp], x["v"][:, :, heads],
+                           x["f"][:, :, heads], x["W"][heads], x["w_r"][heads])
+        np.testing.assert_array_equal(o["y"][:, :, heads], r["y"])
+    # swapping the two groups' q, k changes the outputs (the mapping matters)
+    sw = oracle_mod.fwd(x["q"].flip(2), x["k"].flip(2), x["v"], x["f"], x["W"], x["w_r"])
+    assert np.abs(sw["y"] - o["y"]).max() > 1e-3
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_grouped_backward_matches_central_differences(oracle_mod, T):
+    """dq, dk of the grouped backward against brute-force central
+    differences of L = sum y (.) dy + sum H_T (.) dH_T in fp64, every
+    element of the grouped q and k (N = 4 heads in G = 2 groups)."""
+    B, N, K, V, G = 2, 4, 3, 3, 2
+    x = make_inputs(B, T, N, K, V, "f32", 350 + T, with_dy=True, groups=G)
+    rng = np.random.default_rng(T + 9)
+    inp = {n: _np(x[n]).copy() for n in ("q", "k", "v", "f", "W", "w_r")}
+    H0 = rng.uniform(-0.5, 0.5, size=(B, N, K, V))
+    dy = _np(x["dy"])
+    dHT = rng.normal(size=(B, N, K, V))
+
+    def loss():
+        o = oracle_mod.fwd(inp["q"], inp["k"], inp["v"], inp["f"], inp["W"], inp["w_r"], H0=H0)
+        return float(np.sum(o["y"] * dy) + np.sum(o["HT"] * dHT))
+
+    g = oracle_mod.bwd(inp["q"], inp["k"], inp["v"], inp["f"], inp["W"], inp["w_r"], dy, H0=H0,
+                       dHT=dHT)
+    h = 1e-6
+    for name, gname in (("q", "dq"), ("k", "dk")):
+        arr = inp[name]
+        fd = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = loss()
+            arr[idx] = old - h
+            lm = loss()
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * h)
+        err = np.abs(g[gname] - fd).max() / max(1.0, np.abs(fd).max())
+        assert err <= 1e-6, (gname, err)
