@@ -12,14 +12,17 @@
  *
  * with H_0 = 0 unless an initial state is passed.  q and k are shared by the
  * N value heads (frame "Shared queries and keys buy more recurrent
- * capacity": N_q = N_k = 1, N_v = N_f = N_w = N).  The backward pass is the
+ * capacity": N_q = N_k = 1, N_v = N_f = N_w = N), or by groups of them:
+ * with Nq = N_q = N_k > 1 query/key groups (frame "Tensor parallelism
+ * trades topology dependence for sync", one group per block of heads),
+ * value head n reads group n / (N / Nq).  The backward pass is the
  * chain rule of the backup frame "the recurrent gradient needs both paths"
  * (R_t = C_t + q_t u_t^T, D_t = ((1-f_t) R_t) (.) (1 - Z_t (.) Z_t),
  * C_{t-1} = f_t R_t + D_t W^T, df_t = <R_t, H_{t-1} - Z_t>, dW = sum H_{t-1}^T D_t)
  * plus the value-residual and q/k/v terms that follow from Eqs. (10)-(12).
  *
  * Layouts (all row-major and contiguous; element type in brackets):
- *   q, k          [B,T,K]     (in_dtype)
+ *   q, k          [B,T,Nq,K]  (in_dtype); [B,T,K] when Nq = 1
  *   v             [B,T,N,V]   (in_dtype)
  *   f             [B,T,N]     (in_dtype), values in [0,1]
  *   W             [N,V,V]     (in_dtype); (H W)_{ij} = sum_l H_{il} W[n][l][j]
@@ -29,7 +32,7 @@
  *   ckpt          [B,N,nck,K,V] (float32), nck = ceil(T / ckpt_every);
  *                 ckpt[b][n][c] is the state after c*ckpt_every steps
  *                 (ckpt[b][n][0] = H0, or 0)
- *   dq, dk        [B,T,K]     (float32), summed over the N heads
+ *   dq, dk        [B,T,Nq,K]  (float32), summed over the heads of each group
  *   dv            [B,T,N,V]   (float32)
  *   df            [B,T,N]     (float32)
  *   dW            [N,V,V]     (float32), summed over b and t
@@ -37,7 +40,7 @@
  *   dH_T, dH0     [B,N,K,V]   (float32)
  *
  * Supported shapes: K in {16, 32, 64, 128}, V in {16, 32}, B, N >= 1,
- * T >= 0, B*T*N*V < 2^40.  T = 0 launches no recurrence and writes
+ * T >= 0, Nq >= 1 dividing N, B*T*N*V < 2^40.  T = 0 launches no recurrence and writes
  * H_T = H0 (or 0).
  *
  * Ownership and execution: every tensor pointer is device memory (cudaMalloc
@@ -83,10 +86,12 @@ typedef struct {
     int B, T, N, K, V;
     int in_dtype;    /* m2rnn_dtype */
     int ckpt_every;  /* checkpoint interval C in steps; 0 = no checkpoints */
+    int Nq;          /* query/key groups N_q = N_k; 0 is read as 1 (shared by
+                        all heads); must divide N.  Zero-initialise the struct. */
 } m2rnn_shape;
 
 /* Library version (major*10000 + minor*100 + patch). */
-int m2rnn_version(void);
+int m2rnn_version(void);  /* 200 and later: m2rnn_shape carries Nq */
 
 /* Human-readable text for a status code; never NULL. */
 const char *m2rnn_status_string(int status);
@@ -213,7 +218,7 @@ int m2rnn_bwd_noalloc(const m2rnn_shape *s, const void *q, const void *k, const 
  * forward pass at T = 1 with the state in and out, kept apart because it is
  * bound by the state's HBM traffic rather than by the serial chain.
  *   s->T must be 1; s->ckpt_every is ignored.
- *   q, k  : [B,K]      (in_dtype)      v : [B,N,V] (in_dtype)
+ *   q, k  : [B,Nq,K]   (in_dtype)      v : [B,N,V] (in_dtype)
  *   f     : [B,N]      (in_dtype)      W, w_r : as for m2rnn_fwd
  *   H_in  : [B,N,K,V]  (float32), the state before the step (required)
  *   H_out : [B,N,K,V]  (float32), the state after it (required); it may be

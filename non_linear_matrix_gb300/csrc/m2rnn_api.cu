@@ -68,9 +68,13 @@ int check_ptr(const void* p, int dev, bool required) {
   return M2RNN_OK;
 }
 
+// Query/key groups of a shape (0 is read as 1).
+int groups(const m2rnn_shape* s) { return s->Nq == 0 ? 1 : s->Nq; }
+
 int check_shape(const m2rnn_shape* s) {
   if (s == nullptr) return M2RNN_ERR_INVALID_ARG;
   if (s->B < 1 || s->N < 1 || s->T < 0 || s->ckpt_every < 0) return M2RNN_ERR_INVALID_ARG;
+  if (s->Nq < 0 || s->N % groups(s) != 0) return M2RNN_ERR_INVALID_ARG;
   if (s->in_dtype != M2RNN_F32 && s->in_dtype != M2RNN_BF16) return M2RNN_ERR_INVALID_ARG;
   if (!(s->K == 16 || s->K == 32 || s->K == 64 || s->K == 128)) return M2RNN_ERR_UNSUPPORTED_SHAPE;
   if (!(s->V == 16 || s->V == 32)) return M2RNN_ERR_UNSUPPORTED_SHAPE;
@@ -118,8 +122,9 @@ FwdConfig choose_fwd(const m2rnn_shape* s, int sms) {
   const int WPH = MT == 0 ? s->K / 8 : mtiles / MT;
   const int maxw = m2rnn::fwd_max_consumer_warps(s->V, MT, f32);
   int best = 1;
+  const int hpg = s->N / groups(s);  // a CTA's heads stay inside one q/k group
   for (int G = 1; G <= s->N && G * WPH <= maxw; ++G) {
-    if (s->N % G != 0) continue;
+    if (hpg % G != 0) continue;
     if (m2rnn::fwd_smem_bytes(s->K, s->V, G, WPH, f32, 32) > 200 * 1024) continue;
     const long long ctas = static_cast<long long>(s->B) * (s->N / G);
     if (G == 1 || ctas >= sms) best = G;
@@ -162,7 +167,7 @@ WavePlan plan_full_waves(const m2rnn_shape* s, int sms, const FwdConfig& cfg,
                         (static_cast<long long>(sms) * R)) * R * cfg.G;
   int bestG = 0, bestTc = cfg.tc;
   for (int G = cfg.G - 1; G >= 1; --G) {
-    if (s->N % G != 0) continue;
+    if ((s->N / groups(s)) % G != 0) continue;
     // Shorter ring chunks shrink the per-CTA shared memory so that more of
     // the small CTAs fit on an SM.
     for (int tc = 32; tc >= 8; tc /= 2) {
@@ -195,8 +200,9 @@ struct Gate {
 m2rnn::FwdParams offset_batch(const m2rnn::FwdParams& p, int b0, const m2rnn_shape* s, int es) {
   m2rnn::FwdParams r = p;
   const size_t B0 = static_cast<size_t>(b0), T = s->T, N = s->N, K = s->K, V = s->V;
-  r.q = static_cast<const char*>(p.q) + B0 * T * K * es;
-  r.k = static_cast<const char*>(p.k) + B0 * T * K * es;
+  const size_t Nq = static_cast<size_t>(p.Nq);
+  r.q = static_cast<const char*>(p.q) + B0 * T * Nq * K * es;
+  r.k = static_cast<const char*>(p.k) + B0 * T * Nq * K * es;
   r.v = static_cast<const char*>(p.v) + B0 * T * N * V * es;
   if (p.f) r.f = static_cast<const char*>(p.f) + B0 * T * N * es;
   if (p.a) r.a = static_cast<const char*>(p.a) + B0 * T * N * es;
@@ -239,6 +245,7 @@ int run_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, c
   p.status = status;
   p.wait_limit_ns = static_cast<unsigned long long>(g_wait_limit_ns.load());
   p.inject_stall = g_fault_injection.load();
+  p.Nq = groups(s);
   if (gate != nullptr) {
     p.f = nullptr;
     p.a = gate->a;
@@ -346,7 +353,7 @@ bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
 
 extern "C" {
 
-int m2rnn_version(void) { return 100; }
+int m2rnn_version(void) { return 200; }
 
 const char* m2rnn_status_string(int status) {
   switch (status) {
@@ -425,6 +432,7 @@ int m2rnn_decode(const m2rnn_shape* s, const void* q, const void* k, const void*
   p.B = s->B;
   p.N = s->N;
   p.K = s->K;
+  p.Nq = groups(s);
   return status_from_cuda(m2rnn::launch_decode(p, s->V, s->in_dtype == M2RNN_F32,
                                                static_cast<cudaStream_t>(stream)));
 }
@@ -551,6 +559,7 @@ int bwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, 
     p.dalpha = dalpha;
     p.dbeta = dbeta;
   }
+  p.Nq = groups(s);
   p.dck_ratio = s->ckpt_every / C;
   p.dck_n = static_cast<int>(m2rnn_num_checkpoints(s));
   p.B = s->B;
@@ -565,8 +574,9 @@ int bwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, 
   p.pipe = 0;
   if (!choose_bwd(p, s->V, f32, sms)) return M2RNN_ERR_UNSUPPORTED_SHAPE;
   const size_t BT = static_cast<size_t>(s->B) * s->T;
-  if (cudaMemsetAsync(dq, 0, BT * s->K * sizeof(float), st) != cudaSuccess ||
-      cudaMemsetAsync(dk, 0, BT * s->K * sizeof(float), st) != cudaSuccess)
+  const size_t qk_elems = BT * groups(s) * s->K;
+  if (cudaMemsetAsync(dq, 0, qk_elems * sizeof(float), st) != cudaSuccess ||
+      cudaMemsetAsync(dk, 0, qk_elems * sizeof(float), st) != cudaSuccess)
     return M2RNN_ERR_CUDA;
   if (p.nslices > 1 && (cudaMemsetAsync(dv, 0, BT * NV * sizeof(float), st) != cudaSuccess ||
                         cudaMemsetAsync(dfa, 0, BT * s->N * sizeof(float), st) != cudaSuccess))

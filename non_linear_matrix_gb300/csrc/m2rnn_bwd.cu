@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   const int slice = blockIdx.x % p.nslices;
   const int bn = blockIdx.x / p.nslices;
   const int b = bn / N, n = bn % N;
+  const int Nq = p.Nq, gq = n / (N / Nq);  // query/key group of head n
   const int row0c = slice * RS;            // first row of this CTA
   const int row0 = row0c + 16 * warp;      // first row of this warp
   const BwdLayout L = bwd_layout(V, C, S2, WPC, es);
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
     const int qv = RS * es / 16;  // 16-byte vectors per step
     for (int e = tid; e < Lc * qv; e += nthr) {
       const int s = e / qv, x = e - s * qv;
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(q + (bt0 + s) * K + row0c) + x);
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(q + ((bt0 + s) * Nq + gq) * K + row0c) + x);
       sts_u32x4(sb + L.in_q + static_cast<uint32_t>(s * RS * es + 16 * x), a.x, a.y, a.z, a.w);
     }
     const int vvn = V * es / 16;
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
     const int qv = RS * es / 16;
     for (int e = tid; e < Lc * qv; e += nthr) {
       const int s = e / qv, x = e - s * qv;
-      const uint4 d = __ldg(reinterpret_cast<const uint4*>(kin + (bt0 + s) * K + row0c) + x);
+      const uint4 d = __ldg(reinterpret_cast<const uint4*>(kin + ((bt0 + s) * Nq + gq) * K + row0c) + x);
       sts_u32x4(kb + static_cast<uint32_t>(s * RS * es + 16 * x), d.x, d.y, d.z, d.w);
     }
     const int vvn = V * es / 16;
@@ -486,8 +487,8 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
           const int i = e / r4, x = e - i * r4;
           const float4 a = ptx::lds_f32x4(rq + static_cast<uint32_t>((i * RS + 4 * x) * 4));
           const float4 d = ptx::lds_f32x4(rk + static_cast<uint32_t>((i * RS + 4 * x) * 4));
-          red_add_v4(p.dq + (bt + i) * K + row0c + 4 * x, a.x, a.y, a.z, a.w);
-          red_add_v4(p.dk + (bt + i) * K + row0c + 4 * x, d.x, d.y, d.z, d.w);
+          red_add_v4(p.dq + ((bt + i) * Nq + gq) * K + row0c + 4 * x, a.x, a.y, a.z, a.w);
+          red_add_v4(p.dk + ((bt + i) * Nq + gq) * K + row0c + 4 * x, d.x, d.y, d.z, d.w);
         }
         for (int e = tid; e < Ls * V; e += nthr) {
           const int i = e / V, jj = e - i * V;

@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
   const int slice = blockIdx.x % p.nslices;
   const int bn = blockIdx.x / p.nslices;
   const int b = bn / N, n = bn % N;
+  const int Nq = p.Nq, gq = n / (N / Nq);  // query/key group of head n
   const int row0c = slice * RS;        // first row of this CTA
   const int row0 = row0c + 16 * warp;  // first row of this warp
   constexpr PipeLayout L = pipe_layout(V, S2, WPC, es, GATED);
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
       const bool isR = kind != 2 && kind != 5;
       if (i >= (isR ? sr.nR : sr.nL)) continue;
       const size_t t = (isR ? sr.tR : sr.tL) + i;
-      const TIn* src = kind <= 2 ? (kind == 0 ? q : kin) + t * K + row0c
+      const TIn* src = kind <= 2 ? (kind == 0 ? q : kin) + (t * Nq + gq) * K + row0c
                                  : (kind == 4 ? dy : vin) + (t * N + n) * V;
       ptx::cp_async16(raw + static_cast<uint32_t>((tid + u * nthr) * 16),
                       reinterpret_cast<const uint4*>(src) + x);
@@ -780,9 +781,9 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
       const uint32_t rf = sb + L.r_df + static_cast<uint32_t>(rb * S2 * WPC * 4);
       if (row_ok && i_r < Ls) {
         const uint32_t o = fl_off;
-        red_add_v4(p.dq + (bt + i_r) * K + row0c + r0, ptx::lds_f32(rq + o), ptx::lds_f32(rq + o + 8),
+        red_add_v4(p.dq + ((bt + i_r) * Nq + gq) * K + row0c + r0, ptx::lds_f32(rq + o), ptx::lds_f32(rq + o + 8),
                    ptx::lds_f32(rq + o + 16), ptx::lds_f32(rq + o + 24));
-        red_add_v4(p.dk + (bt + i_r) * K + row0c + r0, ptx::lds_f32(rk + o), ptx::lds_f32(rk + o + 8),
+        red_add_v4(p.dk + ((bt + i_r) * Nq + gq) * K + row0c + r0, ptx::lds_f32(rk + o), ptx::lds_f32(rk + o + 8),
                    ptx::lds_f32(rk + o + 16), ptx::lds_f32(rk + o + 24));
       }
       for (int e = tid; e < Ls * V; e += nthr) {

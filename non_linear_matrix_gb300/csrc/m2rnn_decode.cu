@@ -56,8 +56,10 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
   const int b = static_cast<int>(head / N), n = static_cast<int>(head % N);
   const int row0 = 16 * MT * warp;  // MT 16-row tiles per warp
 
-  const TIn* q = static_cast<const TIn*>(p.q) + static_cast<size_t>(b) * K;
-  const TIn* k = static_cast<const TIn*>(p.k) + static_cast<size_t>(b) * K;
+  // [B,Nq,K]: the row of head n's query/key group
+  const size_t qrow = static_cast<size_t>(b) * p.Nq + n / (N / p.Nq);
+  const TIn* q = static_cast<const TIn*>(p.q) + qrow * K;
+  const TIn* k = static_cast<const TIn*>(p.k) + qrow * K;
   const TIn* v = static_cast<const TIn*>(p.v) + head * V;
   const TIn* Wn = static_cast<const TIn*>(p.W) + static_cast<size_t>(n) * V * V;
   const TIn* wr = static_cast<const TIn*>(p.w_r) + static_cast<size_t>(n) * V;

@@ -155,6 +155,8 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
   const TIn* f = static_cast<const TIn*>(GATED ? p.a : p.f);
   const TIn* galpha = static_cast<const TIn*>(p.alpha);
   const TIn* gbeta = static_cast<const TIn*>(p.beta);
+  // query/key group of this CTA's heads (the host keeps a CTA inside one group)
+  const int Nq = p.Nq, gq = n0 / (N / Nq);
 
   // Waits for a free stage, starts the bulk copies of chunk ch and writes
   // its f (or, gated, f computed from a) as fp32 pairs.
@@ -170,9 +172,18 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
     __syncwarp();
     const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
     const size_t bt0 = static_cast<size_t>(b) * T + t0;
-    if (lane == 0) {
-      ptx::bulk_g2s(st + L.q, q + bt0 * K, qk_bytes, raw);
-      ptx::bulk_g2s(st + L.k, k + bt0 * K, qk_bytes, raw);
+    if (Nq == 1) {  // the chunk's q and k rows are contiguous
+      if (lane == 0) {
+        ptx::bulk_g2s(st + L.q, q + bt0 * K, qk_bytes, raw);
+        ptx::bulk_g2s(st + L.k, k + bt0 * K, qk_bytes, raw);
+      }
+    } else {  // one row per step: [t][Nq][K], group gq
+      const uint32_t row_bytes = static_cast<uint32_t>(K * es);
+      for (int tl = lane; tl < Tc; tl += 32) {
+        const size_t src = ((bt0 + tl) * Nq + gq) * K;
+        ptx::bulk_g2s(st + L.q + tl * row_bytes, q + src, row_bytes, raw);
+        ptx::bulk_g2s(st + L.k + tl * row_bytes, k + src, row_bytes, raw);
+      }
     }
     for (int tl = lane; tl < Tc; tl += 32)
       ptx::bulk_g2s(st + L.v + static_cast<uint32_t>(tl * G * V * es),

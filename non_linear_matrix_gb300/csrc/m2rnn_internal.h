@@ -39,6 +39,7 @@ struct FwdParams {
   int* status;
   unsigned long long wait_limit_ns;
   int inject_stall;  // test hook: 1 = the producer issues nothing
+  int Nq = 1;        // query/key groups: q, k are [B,T,Nq,K], head n reads n / (N / Nq)
   // fused input gate (gated = 1): f = exp(-alpha softplus(a + beta)) from
   // a [B,T,N] and alpha, beta [N] (input dtype) instead of f
   const void* a = nullptr;
@@ -75,6 +76,7 @@ struct BwdParams {
   int S2;       // sub-interval length of the recomputation (= bwd_sub_len)
   int pipe;     // 1: the pipelined kernel (m2rnn_bwd_pipe.cu, V = 16); 0: the
                 // serial one (m2rnn_bwd.cu)
+  int Nq = 1;   // query/key groups (q, k, dq, dk are [B,T,Nq,K])
   // fused input gate (gated = 1): f from a, alpha, beta as in FwdParams; df
   // then receives dL/da, and dalpha, dbeta [N] (zeroed by the caller) are
   // accumulated
@@ -99,8 +101,8 @@ int bwd_sub_len(int V, bool f32_inputs);  // sub-interval length of the variant
 
 // Single-step decode (m2rnn_decode.cu).
 struct DecodeParams {
-  const void* q;      // [B,K]
-  const void* k;      // [B,K]
+  const void* q;      // [B,Nq,K]
+  const void* k;      // [B,Nq,K]
   const void* v;      // [B,N,V]
   const void* f;      // [B,N]
   const void* W;      // [N,V,V]
@@ -109,6 +111,7 @@ struct DecodeParams {
   float* H_out;       // [B,N,K,V], may equal H_in
   void* y;            // [B,N,V]
   int B, N, K;
+  int Nq = 1;         // query/key groups (q, k are [B,Nq,K])
 };
 cudaError_t launch_decode(const DecodeParams& p, int V, bool f32_inputs, cudaStream_t stream);
 

@@ -54,7 +54,7 @@ class M2RNNError(RuntimeError):
 class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("N", ctypes.c_int),
                 ("K", ctypes.c_int), ("V", ctypes.c_int), ("in_dtype", ctypes.c_int),
-                ("ckpt_every", ctypes.c_int)]
+                ("ckpt_every", ctypes.c_int), ("Nq", ctypes.c_int)]
 
 
 def lib() -> ctypes.CDLL:
@@ -108,9 +108,14 @@ def _stream(stream):
 
 
 def make_shape(q, v, ckpt_every: int = 0) -> Shape:
-    B, T, K = q.shape
+    """Shape of a call; q is [B,T,K] (shared by all heads) or [B,T,Nq,K]
+    (Nq query/key groups)."""
+    if q.dim() == 4:
+        B, T, Nq, K = q.shape
+    else:
+        (B, T, K), Nq = q.shape, 1
     N, V = v.shape[2], v.shape[3]
-    return Shape(B, T, N, K, V, _dtype_code(q), int(ckpt_every))
+    return Shape(B, T, N, K, V, _dtype_code(q), int(ckpt_every), Nq)
 
 
 def num_checkpoints(shape: Shape) -> int:
@@ -175,15 +180,19 @@ def fwd_gated(q, k, v, a, alpha, beta, W, w_r, H0=None, *, ckpt_every: int = 0,
 def decode(q, k, v, f, W, w_r, H, *, H_out=None, y=None, stream=None):
     """One decode step for B sequences.  Returns (y, H_out).
 
-    q, k [B,K]; v [B,N,V]; f [B,N]; W [N,V,V]; w_r [N,V], one dtype (bf16 or
-    f32); H [B,N,K,V] fp32 is the state before the step.  H_out defaults to
-    a new tensor; pass ``H_out=H`` to update the state in place."""
-    B, K = q.shape
+    q, k [B,K] (or [B,Nq,K] with Nq query/key groups); v [B,N,V]; f [B,N];
+    W [N,V,V]; w_r [N,V], one dtype (bf16 or f32); H [B,N,K,V] fp32 is the
+    state before the step.  H_out defaults to a new tensor; pass ``H_out=H``
+    to update the state in place."""
+    if q.dim() == 3:
+        B, Nq, K = q.shape
+    else:
+        (B, K), Nq = q.shape, 1
     N, V = v.shape[1], v.shape[2]
     for t in (k, v, f, W, w_r):
         if t.dtype != q.dtype:
             raise TypeError("q, k, v, f, W, w_r must share one dtype")
-    s = Shape(B, 1, N, K, V, _dtype_code(q), 0)
+    s = Shape(B, 1, N, K, V, _dtype_code(q), 0, Nq)
     if H_out is None:
         H_out = torch.empty_like(H)
     if y is None:
@@ -212,7 +221,7 @@ def bwd(q, k, v, f, W, w_r, dy, H0=None, ckpt=None, dHT=None, *, ckpt_every: int
         "dq": out.get("dq"), "dk": out.get("dk"), "dv": out.get("dv"), "df": out.get("df"),
         "dW": out.get("dW"), "dw_r": out.get("dw_r"),
     }
-    shapes = {"dq": (s.B, s.T, s.K), "dk": (s.B, s.T, s.K), "dv": (s.B, s.T, s.N, s.V),
+    shapes = {"dq": tuple(q.shape), "dk": tuple(q.shape), "dv": (s.B, s.T, s.N, s.V),
               "df": (s.B, s.T, s.N), "dW": (s.N, s.V, s.V), "dw_r": (s.N, s.V)}
     for name, shp in shapes.items():
         if g[name] is None:
@@ -248,7 +257,7 @@ def bwd_noalloc(q, k, v, f, W, w_r, dy, H0=None, dHT=None, *, ckpt_every: int = 
     s = make_shape(q, v, ckpt_every)
     f32 = dict(device=q.device, dtype=torch.float32)
     out = dict(out or {})
-    shapes = {"dq": (s.B, s.T, s.K), "dk": (s.B, s.T, s.K), "dv": (s.B, s.T, s.N, s.V),
+    shapes = {"dq": tuple(q.shape), "dk": tuple(q.shape), "dv": (s.B, s.T, s.N, s.V),
               "df": (s.B, s.T, s.N), "dW": (s.N, s.V, s.V), "dw_r": (s.N, s.V)}
     g = {n: out.get(n) if out.get(n) is not None else torch.empty(shp, **f32)
          for n, shp in shapes.items()}
@@ -274,7 +283,7 @@ def bwd_gated(q, k, v, a, alpha, beta, W, w_r, dy, H0=None, ckpt=None, dHT=None,
     s = make_shape(q, v, ckpt_every)
     f32 = dict(device=q.device, dtype=torch.float32)
     out = dict(out or {})
-    shapes = {"dq": (s.B, s.T, s.K), "dk": (s.B, s.T, s.K), "dv": (s.B, s.T, s.N, s.V),
+    shapes = {"dq": tuple(q.shape), "dk": tuple(q.shape), "dv": (s.B, s.T, s.N, s.V),
               "da": (s.B, s.T, s.N), "dalpha": (s.N,), "dbeta": (s.N,),
               "dW": (s.N, s.V, s.V), "dw_r": (s.N, s.V)}
     g = {n: out.get(n) if out.get(n) is not None else torch.empty(shp, **f32)

@@ -105,3 +105,14 @@ def test_gated_entry_points_reject_bad_shapes_before_launch(lib):
     nock = ctypes.byref(Shape(1, 8, 2, 64, 16, 1, 0))  # ckpt_every must be > 0
     assert lib.m2rnn_bwd_gated(nock, *([p] * 8), None, None, p, None, *([p] * 8), None, None, p,
                                ctypes.c_size_t(1 << 20), None) == -1
+
+
+@pytest.mark.parametrize("Nq", [-1, 3, 5])
+def test_groups_must_divide_heads(lib, Nq):
+    """Nq query/key groups must be >= 0 (0 reads as 1) and divide N; checked
+    before any device call."""
+    from non_linear_matrix_gb300.m2rnn import Shape
+    p = ctypes.c_void_p(16)
+    s = ctypes.byref(Shape(1, 8, 4, 64, 16, 1, 0, Nq))
+    assert lib.m2rnn_fwd(s, p, p, p, p, p, p, None, p, None, None, None) == -1
+    assert lib.m2rnn_decode(ctypes.byref(Shape(1, 1, 4, 64, 16, 1, 0, Nq)), *([p] * 10)) == -1

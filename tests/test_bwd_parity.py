@@ -75,13 +75,13 @@ def _restart_parity(m2rnn, oracle_mod, x, C, H0=None, dHT=None, give_ckpt=True, 
     the GPU's dckpt of the next interval (or dH_T) as incoming gradient."""
     gr, ck = _run(m2rnn, x, C, H0, dHT, give_ckpt, with_ckpt=True)
     q, k, v, f, dy = (x[n] for n in ("q", "k", "v", "f", "dy"))
-    B, T, K = q.shape
+    B, T, K = q.shape[0], q.shape[1], q.shape[-1]  # q: [B,T,K] or grouped [B,T,Nq,K]
     N, V = v.shape[2], v.shape[3]
     nck = -(-T // C)
     ckn, dckn = _np64(ck), _np64(gr["dckpt"])
     last = np.zeros((B, N, 1, K, V)) if dHT is None else dHT.double().numpy()[:, :, None]
     nxt = np.concatenate([dckn[:, :, 1:], last], axis=2)
-    ref = {"dq": np.zeros((B, T, K)), "dk": np.zeros((B, T, K)), "dv": np.zeros((B, T, N, V)),
+    ref = {"dq": np.zeros(q.shape), "dk": np.zeros(q.shape), "dv": np.zeros((B, T, N, V)),
            "df": np.zeros((B, T, N)), "dW": np.zeros((N, V, V)), "dw_r": np.zeros((N, V)),
            "dckpt": np.zeros((B, N, nck, K, V))}
     groups = ((0, T // C, C), (T // C, nck, T - (T // C) * C))  # full intervals, ragged tail
@@ -98,8 +98,8 @@ def _restart_parity(m2rnn, oracle_mod, x, C, H0=None, dHT=None, give_ckpt=True, 
             return np.ascontiguousarray(np.moveaxis(a[:, :, c0:c1], 2, 1)).reshape(B * nb, N, K, V)
         r = oracle_mod.bwd(split(q), split(k), split(v), split(f), x["W"], x["w_r"], split(dy),
                            H0=per(ckn), dHT=per(nxt))
-        ref["dq"][:, t0:t1] = r["dq"].reshape(B, nb * L, K)
-        ref["dk"][:, t0:t1] = r["dk"].reshape(B, nb * L, K)
+        ref["dq"][:, t0:t1] = r["dq"].reshape(B, nb * L, *q.shape[2:])
+        ref["dk"][:, t0:t1] = r["dk"].reshape(B, nb * L, *q.shape[2:])
         ref["dv"][:, t0:t1] = r["dv"].reshape(B, nb * L, N, V)
         ref["df"][:, t0:t1] = r["df"].reshape(B, nb * L, N)
         ref["dW"] += r["dW"]
@@ -233,3 +233,25 @@ def test_pipelined_warps_per_cta(m2rnn, oracle_mod, monkeypatch, wpc, dtype):
     H0 = torch.rand(2, 3, 64, 16, generator=gen) - 0.5
     dHT = torch.randn(2, 3, 64, 16, generator=gen)
     _restart_parity(m2rnn, oracle_mod, x, 32, H0=H0, dHT=dHT, label=f"wpc{wpc} {dtype}")
+
+
+@pytest.mark.parametrize("kernel", ["0", "1"])
+@pytest.mark.parametrize("Nq", [2, 4, 8])
+def test_grouped_qk(m2rnn, oracle_mod, monkeypatch, kernel, Nq):
+    """N_q = N_k = Nq query/key groups (head n reads group n // (N/Nq)):
+    dq, dk are [B,T,Nq,K], summed over each group's heads.  Both kernels,
+    ragged last interval, H0 and dH_T given."""
+    monkeypatch.setenv("M2RNN_BWD_KERNEL", kernel)
+    B, T, N = 2, 100, 8
+    x = make_inputs(B, T, N, 64, 16, "bf16", 900 + Nq, with_dy=True, groups=Nq)
+    gen = torch.Generator().manual_seed(Nq)
+    H0 = torch.rand(B, N, 64, 16, generator=gen) - 0.5
+    dHT = torch.randn(B, N, 64, 16, generator=gen)
+    _restart_parity(m2rnn, oracle_mod, x, 24, H0=H0, dHT=dHT, label=f"Nq{Nq} kernel{kernel}")
+
+
+def test_grouped_qk_recomputed_v32_f32(m2rnn, oracle_mod):
+    """Groups with checkpoints recomputed into the workspace (the forward's
+    grouped producer), V = 32, fp32 inputs."""
+    x = make_inputs(2, 70, 4, 64, 32, "f32", 931, with_dy=True, groups=2)
+    _restart_parity(m2rnn, oracle_mod, x, 16, give_ckpt=False, label="Nq2 v32 f32")

@@ -117,3 +117,11 @@ def test_decode_rejects_overlapping_states(m2rnn):
     with pytest.raises(m2rnn.M2RNNError) as e:
         m2rnn.decode(x1["q"], x1["k"], x1["v"], x1["f"], x1["W"], x1["w_r"], H_in, H_out=H_out)
     assert e.value.code == -1
+
+
+@pytest.mark.parametrize("Nq", [2, 6])
+def test_decode_grouped_qk(m2rnn, oracle_mod, Nq):
+    """Nq query/key groups: q, k [B,Nq,K], head n reads group n // (N/Nq)."""
+    B, N, K, V = 4, 6, 64, 16
+    x = make_inputs(B, 1, N, K, V, "bf16", 950 + Nq, groups=Nq)
+    _compare_oracle(m2rnn, oracle_mod, _one_step(x), _state(B, N, K, V, Nq), "bf16")

@@ -74,7 +74,7 @@ def _restart_parity(oracle_mod, x, y, HT, ck, C, tol, label, H0=None):
     """Oracle restarted from the GPU checkpoint of every interval of C steps
     (inputs given for all heads of the batch items in x)."""
     q, k, v, f = (x[n] for n in ("q", "k", "v", "f"))
-    B, T, K = q.shape
+    B, T, K = q.shape[0], q.shape[1], q.shape[-1]  # q: [B,T,K] or grouped [B,T,Nq,K]
     N, V = v.shape[2], v.shape[3]
     ckn = _np(ck)                      # [B,N,nck,K,V]
     yn, HTn = _np(y), _np(HT)
@@ -252,3 +252,29 @@ def test_timeout_path_reports_and_recovers(m2rnn, oracle_mod):
         m2rnn.set_wait_limit_ns(0)
     assert st == -7 and detail in (2, 3), (st, detail)
     _compare(m2rnn, oracle_mod, make_inputs(2, 50, 4, 64, 16, "bf16", 5), "bf16")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("Nq", [2, 4, 32])
+def test_grouped_qk(m2rnn, oracle_mod, dtype, Nq):
+    """N_q = N_k = Nq query/key groups: head n reads q, k of group
+    n // (N / Nq), so a CTA's heads stay inside one group and the producer
+    copies the group's rows one step at a time.  Whole trajectory at T = 40
+    and per 16-step interval at T = 300."""
+    for T in (40, 300):
+        x = make_inputs(3, T, 32, 64, 16, dtype, 700 + Nq + T, groups=Nq)
+        if T <= 40:
+            _compare(m2rnn, oracle_mod, x, dtype, ckpt_every=16, label=f"Nq{Nq} T{T}")
+            continue
+        g = _dev(x)
+        y, HT, ck = m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], ckpt_every=16)
+        torch.cuda.synchronize()
+        _check_status(m2rnn)
+        _restart_parity(oracle_mod, x, y, HT, ck, 16, TOL[dtype], f"Nq{Nq} T{T}")
+
+
+def test_grouped_qk_wave_split(m2rnn, oracle_mod):
+    """A batch large enough for the whole-wave launch plus the tail launch,
+    with 4 groups of 8 heads: both launches' q/k offsets."""
+    x = make_inputs(41, 40, 32, 64, 16, "bf16", 733, groups=4)
+    _compare(m2rnn, oracle_mod, x, "bf16", label="Nq4 wave split")

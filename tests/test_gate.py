@@ -158,13 +158,13 @@ def _gated_restart(m2rnn, oracle_mod, x, C, H0=None, dHT=None, give_ckpt=True, l
     torch.cuda.synchronize()
     _status_ok(m2rnn)
     q, k, v, a, dy = (x[n] for n in ("q", "k", "v", "a", "dy"))
-    B, T, K = q.shape
+    B, T, K = q.shape[0], q.shape[1], q.shape[-1]  # q: [B,T,K] or grouped [B,T,Nq,K]
     N, V = v.shape[2], v.shape[3]
     nck = -(-T // C)
     ckn, dckn = _np(ck), _np(gr["dckpt"])
     last = np.zeros((B, N, 1, K, V)) if dHT is None else dHT.double().numpy()[:, :, None]
     nxt = np.concatenate([dckn[:, :, 1:], last], axis=2)
-    ref = {"dq": np.zeros((B, T, K)), "dk": np.zeros((B, T, K)), "dv": np.zeros((B, T, N, V)),
+    ref = {"dq": np.zeros(q.shape), "dk": np.zeros(q.shape), "dv": np.zeros((B, T, N, V)),
            "da": np.zeros((B, T, N)), "dalpha": np.zeros(N), "dbeta": np.zeros(N),
            "dW": np.zeros((N, V, V)), "dw_r": np.zeros((N, V)),
            "dckpt": np.zeros((B, N, nck, K, V))}
@@ -182,8 +182,8 @@ def _gated_restart(m2rnn, oracle_mod, x, C, H0=None, dHT=None, give_ckpt=True, l
             return np.ascontiguousarray(np.moveaxis(z[:, :, c0:c1], 2, 1)).reshape(B * nb, N, K, V)
         r = oracle_mod.bwd_gated(split(q), split(k), split(v), split(a), x["alpha"], x["beta"],
                                  x["W"], x["w_r"], split(dy), H0=per(ckn), dHT=per(nxt))
-        ref["dq"][:, t0:t1] = r["dq"].reshape(B, nb * L, K)
-        ref["dk"][:, t0:t1] = r["dk"].reshape(B, nb * L, K)
+        ref["dq"][:, t0:t1] = r["dq"].reshape(B, nb * L, *q.shape[2:])
+        ref["dk"][:, t0:t1] = r["dk"].reshape(B, nb * L, *q.shape[2:])
         ref["dv"][:, t0:t1] = r["dv"].reshape(B, nb * L, N, V)
         ref["da"][:, t0:t1] = r["da"].reshape(B, nb * L, N)
         for n in ("dalpha", "dbeta", "dW", "dw_r"):
@@ -280,3 +280,9 @@ def test_gated_zero_steps(m2rnn):
                          x["dy"], ckpt_every=8)
     torch.cuda.synchronize()
     assert torch.count_nonzero(gr["dalpha"]) == 0 and torch.count_nonzero(gr["dbeta"]) == 0
+
+
+def test_gated_grouped_qk(m2rnn, oracle_mod):
+    """The gate together with 4 query/key groups of 2 heads."""
+    x = make_inputs(2, 90, 8, 64, 16, "bf16", 990, with_dy=True, gated=True, groups=4)
+    _gated_restart(m2rnn, oracle_mod, x, 32, label="gated Nq4")
