@@ -19,7 +19,9 @@ share a 100B-token training protocol"; long contexts to 16K and beyond):
     w_r ~ N(0,1) [N,V]
     dy ~ N(0,1) [B,T,N,V]   (only when requested)
     a  ~ N(0,1) [B,T,N], alpha ~ U(0.5, 1.5) [N], beta ~ N(-2, 0.5) [N]
-                            (drawn last, only for the fused input gate)
+                            (only for the fused input gate)
+    g  ~ U(0, 1) [B,T,N,V], w_norm ~ N(1, 0.1) [N,V]
+                            (drawn last, only for the readout epilogue)
   then every tensor is cast to the workload's input dtype (round to nearest
   even for bf16).  H0 = 0 unless a test supplies one.
 
@@ -78,7 +80,7 @@ TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 def make_inputs(B: int, T: int, N: int, K: int, V: int, dtype: str = "bf16",
                 seed: int = 0, f_mean: float = 2.0, with_dy: bool = False,
-                gated: bool = False, groups: int = 1) -> dict:
+                gated: bool = False, groups: int = 1, norm: bool = False) -> dict:
     """Draw one seeded input set on the CPU (see the module docstring)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
@@ -98,6 +100,9 @@ def make_inputs(B: int, T: int, N: int, K: int, V: int, dtype: str = "bf16",
         out["a"] = torch.randn(B, T, N, generator=g)
         out["alpha"] = torch.rand(N, generator=g) + 0.5
         out["beta"] = torch.randn(N, generator=g) * 0.5 - 2.0
+    if norm:
+        out["g"] = torch.rand(B, T, N, V, generator=g)
+        out["w_norm"] = torch.randn(N, V, generator=g) * 0.1 + 1.0
     td = TORCH_DTYPES[dtype]
     return {name: t.to(td).contiguous() for name, t in out.items()}
 

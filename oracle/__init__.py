@@ -24,6 +24,14 @@ per tensor-parallel rank in the deck's topology-aware form), and dq, dk are
 independent problem with N_q = 1, so fwd / bwd run the C routines once per
 group on that group's slices.
 
+The readout epilogue follows the frames "Most of the block can be computed
+before recurrence" (after readout: multiply by the output gate g_t, apply
+RMSNorm) and "Backup: RMSNormTP synchronizes per-token statistics" (the norm
+and its gradient): o = y (.) g over a token's d = N*V features, s =
+(mean_d o^2 + eps)^(-1/2), out = w (.) o s; backward p = w (.) dout,
+r = sum_d p o, do = s p - r s^3 o / d.  eps = 0 is the pages' form (they omit
+it); the functions take it as an argument.
+
 The gated functions follow the frame "The gate preserves a direct path
 through time": f_{t,n} = exp(-alpha_n softplus(a_{t,n} + beta_n)), with a
 [B,T,N] and alpha, beta [N].  They compute f (and the gate's derivatives) in
@@ -201,4 +209,46 @@ def bwd_gated(q, k, v, a, alpha, beta, W, w_r, dy, H0=None, dHT=None):
     r["da"] = da
     r["dalpha"] = (df * (-sp * f)).reshape(-1, df.shape[-1]).sum(axis=0)
     r["dbeta"] = da.reshape(-1, da.shape[-1]).sum(axis=0)
+    return r
+
+
+def readout_norm(y, g, w, eps: float = 0.0):
+    """out = w (.) o s with o = y (.) g and s = (mean over the token's N*V
+    features of o^2 + eps)^(-1/2).  y, g [B,T,N,V]; w [N,V].  Returns
+    dict(out [B,T,N,V], rstd s [B,T]) (float64)."""
+    y, g, w = map(_f64, (y, g, w))
+    o = y * g
+    d = o.shape[2] * o.shape[3]
+    s = 1.0 / np.sqrt((o * o).sum(axis=(2, 3)) / d + eps)
+    return {"out": w[None, None] * o * s[:, :, None, None], "rstd": s}
+
+
+def readout_norm_bwd(y, g, w, dout, eps: float = 0.0):
+    """Gradients of readout_norm for dL/dout = dout: p = w (.) dout,
+    r = sum_d p o, do = s p - r s^3 o / d, then dy = do (.) g, dg = do (.) y
+    and dw = sum over (b, t) of dout (.) o s.  Returns dict(dy, dg, dw)."""
+    y, g, w, dout = map(_f64, (y, g, w, dout))
+    o = y * g
+    d = o.shape[2] * o.shape[3]
+    s = 1.0 / np.sqrt((o * o).sum(axis=(2, 3)) / d + eps)[:, :, None, None]
+    p = w[None, None] * dout
+    r = (p * o).sum(axis=(2, 3))[:, :, None, None]
+    do = s * p - r * s ** 3 * o / d
+    return {"dy": do * g, "dg": do * y, "dw": (dout * o * s).sum(axis=(0, 1))}
+
+
+def fwd_norm(q, k, v, f, W, w_r, g, w_norm, eps: float = 0.0, H0=None):
+    """Forward pass followed by the readout epilogue: dict(y, out, rstd, HT)."""
+    r = fwd(q, k, v, f, W, w_r, H0)
+    r.update(readout_norm(r["y"], g, w_norm, eps))
+    return r
+
+
+def bwd_norm(q, k, v, f, W, w_r, g, w_norm, dout, eps: float = 0.0, H0=None, dHT=None):
+    """Backward pass through the readout epilogue and the recurrence:
+    dict(dq, dk, dv, df, dW, dw_r, dH0, dg, dw_norm) (float64)."""
+    y = fwd(q, k, v, f, W, w_r, H0)["y"]
+    n = readout_norm_bwd(y, g, w_norm, dout, eps)
+    r = bwd(q, k, v, f, W, w_r, n["dy"], H0, dHT)
+    r["dg"], r["dw_norm"] = n["dg"], n["dw"]
     return r

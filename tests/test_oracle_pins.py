@@ -365,3 +365,90 @@ def test_grouped_backward_matches_central_differences(oracle_mod, T):
             fd[idx] = (lp - lm) / (2 * h)
         err = np.abs(g[gname] - fd).max() / max(1.0, np.abs(fd).max())
         assert err <= 1e-6, (gname, err)
+
+
+# --- readout epilogue (frames "Most of the block can be computed before
+# recurrence": x g_t, then RMSNorm; "Backup: RMSNormTP synchronizes per-token
+# statistics": the norm and its gradient) ------------------------------------
+
+def _norm_inputs(seed=3, B=2, T=3, N=2, V=4):
+    x = make_inputs(B, T, N, 8, V, "f32", seed, with_dy=True, norm=True)
+    return _np(x["dy"]) * 0.7, _np(x["g"]), _np(x["w_norm"]), _np(x["dy"])
+
+
+@pytest.mark.parametrize("eps", [0.0, 1e-3])
+def test_readout_norm_matches_library_rms_norm(oracle_mod, eps):
+    """The forward against torch.nn.functional.rms_norm over the token's
+    N*V features (fp64), applied to y (.) g."""
+    y, g, w, _ = _norm_inputs()
+    r = oracle_mod.readout_norm(y, g, w, eps)
+    o = torch.from_numpy(y * g)
+    ref = torch.nn.functional.rms_norm(o, (o.shape[2], o.shape[3]), torch.from_numpy(w), eps=eps)
+    np.testing.assert_allclose(r["out"], ref.numpy(), rtol=1e-13, atol=1e-15)
+
+
+def test_readout_norm_unit_rms_and_scale_invariance(oracle_mod):
+    """eps = 0: every token's (out / w) has mean square exactly 1 over its
+    N*V features, and scaling y by c > 0 leaves out unchanged."""
+    y, g, w, _ = _norm_inputs(seed=5, N=3, V=8)
+    r = oracle_mod.readout_norm(y, g, w)
+    ms = ((r["out"] / w[None, None]) ** 2).mean(axis=(2, 3))
+    np.testing.assert_allclose(ms, 1.0, rtol=1e-13)
+    np.testing.assert_allclose(oracle_mod.readout_norm(3.7 * y, g, w)["out"], r["out"],
+                               rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(r["rstd"], 1 / np.sqrt(((y * g) ** 2).mean(axis=(2, 3))),
+                               rtol=1e-13)
+
+
+@pytest.mark.parametrize("eps", [0.0, 1e-3])
+def test_readout_norm_backward_matches_autograd(oracle_mod, eps):
+    """dy, dg, dw against fp64 torch.autograd through the library rms_norm."""
+    y, g, w, dout = _norm_inputs(seed=9, N=3, V=4)
+    r = oracle_mod.readout_norm_bwd(y, g, w, dout, eps)
+    yt, gt, wt = (torch.from_numpy(a).requires_grad_() for a in (y, g, w))
+    o = yt * gt
+    out = torch.nn.functional.rms_norm(o, (o.shape[2], o.shape[3]), wt, eps=eps)
+    out.backward(torch.from_numpy(dout))
+    for name, t in (("dy", yt), ("dg", gt), ("dw", wt)):
+        np.testing.assert_allclose(r[name], t.grad.numpy(), rtol=1e-11, atol=1e-13)
+
+
+def test_readout_norm_backward_central_differences(oracle_mod):
+    """dy, dg, dw against brute-force central differences of
+    L = sum out (.) dout on every element (fp64, eps = 0)."""
+    y, g, w, dout = _norm_inputs(seed=13, B=1, T=2, N=2, V=3)
+    r = oracle_mod.readout_norm_bwd(y, g, w, dout)
+    arrs = {"dy": y, "dg": g, "dw": w}
+    h = 1e-6
+    for name, arr in arrs.items():
+        fd = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = float((oracle_mod.readout_norm(y, g, w)["out"] * dout).sum())
+            arr[idx] = old - h
+            lm = float((oracle_mod.readout_norm(y, g, w)["out"] * dout).sum())
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * h)
+        assert np.abs(r[name] - fd).max() <= 1e-7 * max(1.0, np.abs(fd).max()), name
+
+
+def test_fwd_bwd_norm_compose(oracle_mod):
+    """fwd_norm / bwd_norm: the recurrence's gradients at dy = the norm's dy
+    (checked against a central difference of the whole block in one
+    direction of W)."""
+    x = make_inputs(1, 4, 2, 8, 4, "f32", 21, with_dy=True, norm=True)
+    args = [_np(x[n]) for n in ("q", "k", "v", "f", "W", "w_r")]
+    g, w, dout = _np(x["g"]), _np(x["w_norm"]), _np(x["dy"])
+    r = oracle_mod.bwd_norm(*args, g, w, dout)
+    dirW = np.random.default_rng(0).normal(size=args[4].shape)
+    h = 1e-6
+
+    def L(W):
+        a = list(args)
+        a[4] = W
+        return float((oracle_mod.fwd_norm(*a, g, w)["out"] * dout).sum())
+    fd = (L(args[4] + h * dirW) - L(args[4] - h * dirW)) / (2 * h)
+    assert abs(fd - float((r["dW"] * dirW).sum())) <= 1e-7 * max(1.0, abs(fd))
