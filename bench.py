@@ -26,6 +26,7 @@ scaling, no collective on the data path); rank 0 prints.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -201,9 +202,15 @@ def _oracle_rate(w, budget_s: float, seed_offset: int = 0):
 
     def run(T_):
         x = make_inputs(1, T_, heads, w.K, w.V, w.dtype, w.seed + seed_offset, w.f_mean,
-                        with_dy=w.backward, gated=w.gated)
+                        with_dy=w.backward, gated=w.gated, norm=w.norm)
         t0 = time.perf_counter()
-        if w.gated:  # the oracle's gated forward (+ backward through the gate)
+        if w.norm:  # the oracle's block: recurrence + readout epilogue (+ backward)
+            oracle.fwd_norm(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], x["g"],
+                            x["w_norm"], 1e-6)
+            if w.backward:
+                oracle.bwd_norm(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], x["g"],
+                                x["w_norm"], x["dy"], 1e-6)
+        elif w.gated:  # the oracle's gated forward (+ backward through the gate)
             gi = (x["a"], x["alpha"], x["beta"])
             oracle.fwd_gated(x["q"], x["k"], x["v"], *gi, x["W"], x["w_r"])
             if w.backward:
@@ -278,12 +285,14 @@ class Runner:
         self.w, self.m = w, m2rnn
         seed = rank_seed(w.seed, rank)
         self.x = make_inputs(w.B, w.T, w.N, w.K, w.V, w.dtype, seed, w.f_mean,
-                             with_dy=w.backward, gated=w.gated)
+                             with_dy=w.backward, gated=w.gated, norm=w.norm)
         self.g = {n: t.cuda() for n, t in self.x.items()}
         g = self.g
         f32 = dict(device="cuda", dtype=torch.float32)
         self.out = {"y": torch.empty_like(g["v"]),
                     "HT": torch.empty(w.B, w.N, w.K, w.V, **f32)}
+        if w.norm:
+            self.out.update(out=torch.empty_like(g["v"]), rstd=torch.empty(w.B, w.T, **f32))
         if w.backward:
             nck = -(-w.T // w.ckpt_every)
             self.out["ckpt"] = torch.empty(w.B, w.N, nck, w.K, w.V, **f32)
@@ -292,19 +301,26 @@ class Runner:
                          "dv": torch.empty(w.B, w.T, w.N, w.V, **f32),
                          "dW": torch.empty(w.N, w.V, w.V, **f32),
                          "dw_r": torch.empty(w.N, w.V, **f32)}
+            if w.norm:
+                self.gout.update(dg=torch.empty(w.B, w.T, w.N, w.V, **f32),
+                                 dw_norm=torch.empty(w.N, w.V, **f32))
             if w.gated:
                 self.gout.update(da=torch.empty(w.B, w.T, w.N, **f32),
                                  dalpha=torch.empty(w.N, **f32), dbeta=torch.empty(w.N, **f32))
             else:
                 self.gout["df"] = torch.empty(w.B, w.T, w.N, **f32)
             shape = m2rnn.make_shape(g["q"], g["v"], w.ckpt_every)
-            self.ws = torch.empty(max(16, m2rnn.bwd_workspace_size(shape, True)),
-                                  device="cuda", dtype=torch.uint8)
+            ws = (m2rnn.lib().m2rnn_bwd_norm_workspace_size(ctypes.byref(shape), 1) if w.norm
+                  else m2rnn.bwd_workspace_size(shape, True))
+            self.ws = torch.empty(max(16, ws), device="cuda", dtype=torch.uint8)
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
 
     def fwd(self):
         g = self.g
-        if self.w.gated:
+        if self.w.norm:
+            self.m.fwd_norm(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], g["g"], g["w_norm"],
+                            1e-6, out=self.out, ckpt_every=self.w.ckpt_every)
+        elif self.w.gated:
             self.m.fwd_gated(g["q"], g["k"], g["v"], g["a"], g["alpha"], g["beta"], g["W"],
                              g["w_r"], out=self.out, ckpt_every=self.w.ckpt_every)
         else:
@@ -313,7 +329,12 @@ class Runner:
 
     def bwd(self):
         g = self.g
-        if self.w.gated:
+        if self.w.norm:
+            o = self.out
+            self.m.bwd_norm(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], g["g"],
+                            g["w_norm"], o["y"], o["rstd"], g["dy"], ckpt=o["ckpt"],
+                            ckpt_every=self.w.ckpt_every, out=self.gout, workspace=self.ws)
+        elif self.w.gated:
             self.m.bwd_gated(g["q"], g["k"], g["v"], g["a"], g["alpha"], g["beta"], g["W"],
                              g["w_r"], g["dy"], ckpt=self.out["ckpt"],
                              ckpt_every=self.w.ckpt_every, out=self.gout, workspace=self.ws)
@@ -556,6 +577,7 @@ def main():
                    "inputs": w.dtype, "state": "f32", "global_batch": w.B * world,
                    "seq_len": w.T, "parallelism": f"replicas{world}" if world > 1 else "1 GPU",
                    "step": ("forward + backward" + (" (fused input gate)" if w.gated else "")
+                            + (" (readout epilogue: x g, RMSNorm)" if w.norm else "")
                             if w.backward else
                             "decode (one step, state updated in place)" if w.decode else
                             "forward"),

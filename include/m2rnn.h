@@ -163,6 +163,56 @@ int m2rnn_bwd_gated(const m2rnn_shape *s, const void *q, const void *k, const vo
                     float *dalpha, float *dbeta, float *dW, float *dw_r, float *dH0,
                     float *dckpt, void *workspace, size_t ws_bytes, void *stream);
 
+/* Forward pass with the readout epilogue of the frame "Most of the block can
+ * be computed before recurrence" (after readout: multiply by the output gate
+ * g_t, apply RMSNorm) in the form of the backup frame "RMSNormTP synchronizes
+ * per-token statistics", over a token's d = N*V features:
+ *     o = y (.) g,   rstd = (sum_d o^2 / d + eps)^(-1/2),   out = w_norm (.) o rstd.
+ * The forward kernel's epilogue adds each CTA's share of sum_d o^2 per token
+ * as it stores y; a second kernel scales.
+ *   f, or the gate (a, alpha, beta): exactly one of the two forms (the other
+ *        pointers NULL), as for m2rnn_fwd / m2rnn_fwd_gated.
+ *   g      : [B,T,N,V] (in_dtype), the output gate (required)
+ *   w_norm : [N,V] (in_dtype), the norm's weight (required)
+ *   eps    : >= 0 (the pages omit it: 0 is their form; then a token whose
+ *            o is all zero gets rstd = inf)
+ *   y      : [B,T,N,V] (in_dtype), the readout of Eq. (12) (required: the
+ *            backward pass needs it)
+ *   out    : [B,T,N,V] (in_dtype), the normalised output (required)
+ *   rstd   : [B,T] float32, rstd per token (required; the backward needs it)
+ *   H_T, ckpt : as for m2rnn_fwd. */
+int m2rnn_fwd_norm(const m2rnn_shape *s, const void *q, const void *k, const void *v,
+                   const void *f, const void *a, const void *alpha, const void *beta,
+                   const void *W, const void *w_r, const float *H0, const void *g,
+                   const void *w_norm, float eps, void *y, void *out, float *rstd, float *H_T,
+                   float *ckpt, void *stream);
+
+/* Bytes of workspace m2rnn_bwd_norm needs: dL/dy ([B,T,N,V] in_dtype, 256-byte
+ * aligned) plus m2rnn_bwd_workspace_size(s, ckpt_given). */
+size_t m2rnn_bwd_norm_workspace_size(const m2rnn_shape *s, int ckpt_given);
+
+/* Backward pass through the readout epilogue and the recurrence, for
+ * dL/dout = dout ([B,T,N,V] in_dtype) and dL/dH_T = dH_T:
+ *     p = w_norm (.) dout,  r = sum_d p o,  do = rstd p - r rstd^3 o / d,
+ *     dL/dy = do (.) g,  dg = do (.) y,  dw_norm = sum over (b, t) of dout (.) o rstd,
+ * then the recurrence's backward pass with that dL/dy (rounded to in_dtype,
+ * the dtype m2rnn_bwd takes dy in).
+ *   y, rstd : from m2rnn_fwd_norm with the same inputs.
+ *   f or (a, alpha, beta) : as for m2rnn_fwd_norm; df receives dL/df, or
+ *            dL/da with dalpha, dbeta ([N] float32, required then, NULL
+ *            otherwise) as for m2rnn_bwd_gated.
+ *   dg      : [B,T,N,V] float32 (required);  dw_norm : [N,V] float32 (required)
+ *   everything else as for m2rnn_bwd; workspace: at least
+ *   m2rnn_bwd_norm_workspace_size(s, ckpt != NULL) bytes. */
+int m2rnn_bwd_norm(const m2rnn_shape *s, const void *q, const void *k, const void *v,
+                   const void *f, const void *a, const void *alpha, const void *beta,
+                   const void *W, const void *w_r, const float *H0, const float *ckpt,
+                   const void *g, const void *w_norm, const void *y, const float *rstd,
+                   const void *dout, const float *dH_T, float *dq, float *dk, float *dv,
+                   float *df, float *dalpha, float *dbeta, float *dW, float *dw_r, float *dg,
+                   float *dw_norm, float *dH0, float *dckpt, void *workspace, size_t ws_bytes,
+                   void *stream);
+
 /* Reads (after synchronising `stream`) and optionally clears the device
  * status word of the current device.  *status receives M2RNN_OK or the code
  * a kernel recorded (M2RNN_ERR_TIMEOUT); *detail receives the location code

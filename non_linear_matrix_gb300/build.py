@@ -19,7 +19,7 @@ LIB = os.path.join(BUILD, "libm2rnn.so")
 MICROBENCH = os.path.join(BUILD, "m2rnn_microbench")
 
 SOURCES = ["m2rnn_api.cu", "m2rnn_fwd.cu", "m2rnn_bwd.cu", "m2rnn_bwd_pipe.cu", "m2rnn_decode.cu",
-           "m2rnn_noalloc.cu"]
+           "m2rnn_noalloc.cu", "m2rnn_norm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

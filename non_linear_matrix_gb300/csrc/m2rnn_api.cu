@@ -196,6 +196,26 @@ struct Gate {
   const void* beta;
 };
 
+// The readout epilogue's arguments: forward (g, w, eps; outputs out and
+// rstd) and backward (g, w, the forward's y and rstd, the upstream dout;
+// outputs dg and dw).  A null pointer to either struct: plain y.
+struct NormFwd {
+  const void* g;
+  const void* w;
+  float eps;
+  void* out;
+  float* rstd;
+};
+struct NormBwd {
+  const void* g;
+  const void* w;
+  const void* y;
+  const float* rstd;
+  const void* dout;
+  float* dg;
+  float* dw;
+};
+
 // Parameters with every per-batch pointer advanced by b0 batch items.
 m2rnn::FwdParams offset_batch(const m2rnn::FwdParams& p, int b0, const m2rnn_shape* s, int es) {
   m2rnn::FwdParams r = p;
@@ -210,6 +230,8 @@ m2rnn::FwdParams offset_batch(const m2rnn::FwdParams& p, int b0, const m2rnn_sha
   if (p.H0) r.H0 = p.H0 + B0 * N * K * V;
   if (p.HT) r.HT = p.HT + B0 * N * K * V;
   if (p.ckpt) r.ckpt = p.ckpt + B0 * N * static_cast<size_t>(p.nck) * K * V;
+  if (p.g) r.g = static_cast<const char*>(p.g) + B0 * T * N * V * es;
+  if (p.ssq) r.ssq = p.ssq + B0 * T;
   return r;
 }
 
@@ -217,7 +239,8 @@ m2rnn::FwdParams offset_batch(const m2rnn::FwdParams& p, int b0, const m2rnn_sha
 // be NULL (checkpoint-only runs for the backward pass).
 int run_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
             const Gate* gate, const void* W, const void* w_r, const float* H0, void* y,
-            float* H_T, float* ckpt, cudaStream_t st, int* status, int sms) {
+            float* H_T, float* ckpt, cudaStream_t st, int* status, int sms,
+            const NormFwd* nf = nullptr) {
   const bool want_ckpt = ckpt != nullptr && s->ckpt_every > 0 && s->T > 0;
   const bool f32 = s->in_dtype == M2RNN_F32;
   const FwdConfig cfg = choose_fwd(s, sms);
@@ -252,6 +275,11 @@ int run_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, c
     p.alpha = gate->alpha;
     p.beta = gate->beta;
     p.gated = 1;
+  }
+  if (nf != nullptr) {  // the epilogue adds sum (y g)^2 per token into rstd
+    p.g = nf->g;
+    p.ssq = nf->rstd;
+    p.norm = 1;
   }
 
   // Wave planning.  All CTAs of a launch run equally long, so when the heads
@@ -297,6 +325,12 @@ int bwd_interval(const m2rnn_shape* s, bool ckpt_given, bool* own_ckpt) {
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Workspace bytes of the readout epilogue's dy (input dtype, [B,T,N,V]).
+size_t norm_dy_bytes(const m2rnn_shape* s) {
+  return align256(static_cast<size_t>(s->B) * s->T * s->N * s->V *
+                  (s->in_dtype == M2RNN_F32 ? 4 : 2));
+}
 
 // Picks the kernel (pipelined where it exists for V, else serial) and the
 // warps per CTA (16 rows each) for the fewest waves; ties go to the
@@ -444,7 +478,7 @@ namespace {
 // Forward entry: validation, then run_fwd.  gate = NULL: f is given.
 int fwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
              const Gate* gate, const void* W, const void* w_r, const float* H0, void* y,
-             float* H_T, float* ckpt, void* stream) {
+             float* H_T, float* ckpt, void* stream, const NormFwd* nf = nullptr) {
   int rc = check_shape(s);
   if (rc != M2RNN_OK) return rc;
   int dev, sms;
@@ -458,6 +492,10 @@ int fwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, 
     if ((rc = check_ptr(gate->alpha, dev, true)) != M2RNN_OK) return rc;
     if ((rc = check_ptr(gate->beta, dev, true)) != M2RNN_OK) return rc;
   }
+  if (nf != nullptr) {
+    if (!(nf->eps >= 0.f)) return M2RNN_ERR_INVALID_ARG;  // also rejects NaN
+    if ((rc = check_ptr(nf->w, dev, true)) != M2RNN_OK) return rc;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t state_bytes = static_cast<size_t>(s->B) * s->N * s->K * s->V * sizeof(float);
   if (s->T == 0) {  // empty sequences: the [B,0,...] tensors may have no storage
@@ -469,8 +507,31 @@ int fwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, 
   for (const void* p : req)
     if ((rc = check_ptr(p, dev, true)) != M2RNN_OK) return rc;
   if ((rc = check_ptr(ckpt, dev, false)) != M2RNN_OK) return rc;
-  return run_fwd(s, q, k, v, f, gate, W, w_r, H0, y, H_T, want_ckpt ? ckpt : nullptr, st, status,
-                 sms);
+  if (nf == nullptr)
+    return run_fwd(s, q, k, v, f, gate, W, w_r, H0, y, H_T, want_ckpt ? ckpt : nullptr, st,
+                   status, sms);
+  const void* nreq[] = {nf->g, nf->out, nf->rstd};
+  for (const void* p : nreq)
+    if ((rc = check_ptr(p, dev, true)) != M2RNN_OK) return rc;
+  const long long rows = static_cast<long long>(s->B) * s->T;
+  if (cudaMemsetAsync(nf->rstd, 0, rows * sizeof(float), st) != cudaSuccess) return M2RNN_ERR_CUDA;
+  rc = run_fwd(s, q, k, v, f, gate, W, w_r, H0, y, H_T, want_ckpt ? ckpt : nullptr, st, status,
+               sms, nf);
+  if (rc != M2RNN_OK) return rc;
+  m2rnn::NormParams np;
+  np.rows = rows;
+  np.d = s->N * s->V;
+  np.eps = nf->eps;
+  np.y = y;
+  np.g = nf->g;
+  np.w = nf->w;
+  np.rstd = nf->rstd;
+  np.out = nf->out;
+  np.dout = nullptr;
+  np.dy = nullptr;
+  np.dg = nullptr;
+  np.dw = nullptr;
+  return status_from_cuda(m2rnn::launch_norm_fwd(np, s->in_dtype == M2RNN_F32, sms, st));
 }
 
 // Backward entry.  gate = NULL: f is given and dfa receives dL/df; otherwise
@@ -479,7 +540,7 @@ int bwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, 
              const Gate* gate, const void* W, const void* w_r, const float* H0, const float* ckpt,
              const void* dy, const float* dH_T, float* dq, float* dk, float* dv, float* dfa,
              float* dalpha, float* dbeta, float* dW, float* dw_r, float* dH0, float* dckpt,
-             void* workspace, size_t ws_bytes, void* stream) {
+             void* workspace, size_t ws_bytes, void* stream, const NormBwd* nb = nullptr) {
   int rc = check_shape(s);
   if (rc != M2RNN_OK) return rc;
   if (s->ckpt_every <= 0) return M2RNN_ERR_INVALID_ARG;
@@ -508,10 +569,40 @@ int bwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, 
   if (gate != nullptr && (cudaMemsetAsync(dalpha, 0, s->N * sizeof(float), st) != cudaSuccess ||
                           cudaMemsetAsync(dbeta, 0, s->N * sizeof(float), st) != cudaSuccess))
     return M2RNN_ERR_CUDA;
+  if (nb != nullptr) {
+    if ((rc = check_ptr(nb->w, dev, true)) != M2RNN_OK) return rc;
+    if ((rc = check_ptr(nb->dw, dev, true)) != M2RNN_OK) return rc;
+    if (cudaMemsetAsync(nb->dw, 0, NV * sizeof(float), st) != cudaSuccess) return M2RNN_ERR_CUDA;
+  }
   if (s->T == 0) {  // no steps: dH0 = dH_T
     if (dH0 == nullptr) return M2RNN_OK;
     return status_from_cuda(dH_T ? cudaMemcpyAsync(dH0, dH_T, state_bytes, cudaMemcpyDeviceToDevice, st)
                                  : cudaMemsetAsync(dH0, 0, state_bytes, st));
+  }
+  if (nb != nullptr) {  // dy from the readout epilogue's gradient, into the workspace
+    const void* nreq[] = {nb->g, nb->y, nb->rstd, nb->dout, nb->dg};
+    for (const void* x : nreq)
+      if ((rc = check_ptr(x, dev, true)) != M2RNN_OK) return rc;
+    const size_t dy_bytes = norm_dy_bytes(s);
+    if (workspace == nullptr || ws_bytes < dy_bytes) return M2RNN_ERR_WORKSPACE;
+    if ((rc = check_ptr(workspace, dev, true)) != M2RNN_OK) return rc;
+    m2rnn::NormParams np;
+    np.rows = static_cast<long long>(s->B) * s->T;
+    np.d = s->N * s->V;
+    np.eps = 0.f;
+    np.y = nb->y;
+    np.g = nb->g;
+    np.w = nb->w;
+    np.rstd = const_cast<float*>(nb->rstd);  // read only in the backward kernel
+    np.out = nullptr;
+    np.dout = nb->dout;
+    np.dy = workspace;
+    np.dg = nb->dg;
+    np.dw = nb->dw;
+    if (m2rnn::launch_norm_bwd(np, f32, sms, st) != cudaSuccess) return M2RNN_ERR_CUDA;
+    dy = workspace;
+    workspace = static_cast<char*>(workspace) + dy_bytes;
+    ws_bytes -= dy_bytes;
   }
   const void* req[] = {q, k, v, gate ? gate->a : f, dy, dq, dk, dv, dfa};
   for (const void* x : req)
@@ -522,7 +613,7 @@ int bwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, 
   const size_t need = m2rnn_bwd_workspace_size(s, ckpt != nullptr);
   if (need > 0) {
     if (workspace == nullptr || ws_bytes < need) return M2RNN_ERR_WORKSPACE;
-    if ((rc = check_ptr(workspace, dev, true)) != M2RNN_OK) return rc;
+    if (nb == nullptr && (rc = check_ptr(workspace, dev, true)) != M2RNN_OK) return rc;
   }
   const float* ck = ckpt;
   if (own) {  // checkpoints at interval C into the workspace (no y written)
@@ -585,6 +676,21 @@ int bwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, 
                                 : m2rnn::launch_bwd(p, s->V, f32, st));
 }
 
+// f or the gate (exactly one of the two forms).
+int pick_f(const void* f, const void* a, const void* alpha, const void* beta, Gate* gate,
+           const Gate** gp) {
+  if (f != nullptr && a == nullptr && alpha == nullptr && beta == nullptr) {
+    *gp = nullptr;
+    return M2RNN_OK;
+  }
+  if (f == nullptr && a != nullptr && alpha != nullptr && beta != nullptr) {
+    *gate = Gate{a, alpha, beta};
+    *gp = gate;
+    return M2RNN_OK;
+  }
+  return M2RNN_ERR_INVALID_ARG;
+}
+
 }  // namespace
 
 extern "C" {
@@ -629,6 +735,41 @@ int m2rnn_bwd_gated(const m2rnn_shape* s, const void* q, const void* k, const vo
   const Gate gate{a, alpha, beta};
   return bwd_impl(s, q, k, v, nullptr, &gate, W, w_r, H0, ckpt, dy, dH_T, dq, dk, dv, da, dalpha,
                   dbeta, dW, dw_r, dH0, dckpt, workspace, ws_bytes, stream);
+}
+
+int m2rnn_fwd_norm(const m2rnn_shape* s, const void* q, const void* k, const void* v,
+                   const void* f, const void* a, const void* alpha, const void* beta,
+                   const void* W, const void* w_r, const float* H0, const void* g,
+                   const void* w_norm, float eps, void* y, void* out, float* rstd, float* H_T,
+                   float* ckpt, void* stream) {
+  Gate gate;
+  const Gate* gp = nullptr;
+  int rc = pick_f(f, a, alpha, beta, &gate, &gp);
+  if (rc != M2RNN_OK) return rc;
+  const NormFwd nf{g, w_norm, eps, out, rstd};
+  return fwd_impl(s, q, k, v, f, gp, W, w_r, H0, y, H_T, ckpt, stream, &nf);
+}
+
+size_t m2rnn_bwd_norm_workspace_size(const m2rnn_shape* s, int ckpt_given) {
+  if (check_shape(s) != M2RNN_OK || s->ckpt_every <= 0 || s->T == 0) return 0;
+  return norm_dy_bytes(s) + m2rnn_bwd_workspace_size(s, ckpt_given);
+}
+
+int m2rnn_bwd_norm(const m2rnn_shape* s, const void* q, const void* k, const void* v,
+                   const void* f, const void* a, const void* alpha, const void* beta,
+                   const void* W, const void* w_r, const float* H0, const float* ckpt,
+                   const void* g, const void* w_norm, const void* y, const float* rstd,
+                   const void* dout, const float* dH_T, float* dq, float* dk, float* dv,
+                   float* df, float* dalpha, float* dbeta, float* dW, float* dw_r, float* dg,
+                   float* dw_norm, float* dH0, float* dckpt, void* workspace, size_t ws_bytes,
+                   void* stream) {
+  Gate gate;
+  const Gate* gp = nullptr;
+  int rc = pick_f(f, a, alpha, beta, &gate, &gp);
+  if (rc != M2RNN_OK) return rc;
+  const NormBwd nb{g, w_norm, y, rstd, dout, dg, dw_norm};
+  return bwd_impl(s, q, k, v, f, gp, W, w_r, H0, ckpt, nullptr, dH_T, dq, dk, dv, df, dalpha,
+                  dbeta, dW, dw_r, dH0, dckpt, workspace, ws_bytes, stream, &nb);
 }
 
 }  // extern "C"

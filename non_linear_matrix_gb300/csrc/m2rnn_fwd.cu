@@ -306,7 +306,28 @@ __device__ __forceinline__ void load8(uint32_t addr, float (&o)[8]) {
   }
 }
 
-template <int V, bool F32>
+// 8 consecutive input-dtype values from global memory (16-byte aligned).
+template <bool F32>
+__device__ __forceinline__ void ldg8(const void* src, float (&o)[8]) {
+  if (F32) {
+    const float4 a = __ldg(static_cast<const float4*>(src)), c = __ldg(static_cast<const float4*>(src) + 1);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = c.x; o[5] = c.y; o[6] = c.z; o[7] = c.w;
+  } else {
+    const uint4 u = __ldg(static_cast<const uint4*>(src));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = ptx::bf16x2_lo(w[i]);
+      o[2 * i + 1] = ptx::bf16x2_hi(w[i]);
+    }
+  }
+}
+
+// Sums the per-warp readout partials, adds w_r (.) v and stores y.  NORM
+// (the readout epilogue): also adds this CTA's share of sum (y (.) g)^2 of
+// every token into p.ssq[b, t] (the normalisation kernel finishes the norm).
+template <int V, bool F32, bool NORM>
 __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout& L, uint32_t sbase,
                                              int b, int n0, int Geff) {
   using TIn = typename InType<F32>::T;
@@ -357,6 +378,18 @@ __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i] = fmaf(wr[i], vv[i], o[i]);
       store8(y + static_cast<size_t>(tl) * N * V + r, o);
+      if constexpr (NORM) {
+        float gg[8];
+        ldg8<F32>(static_cast<const TIn*>(p.g) +
+                      ((static_cast<size_t>(b) * T + t0 + tl) * N + n0) * V + r, gg);
+        float part = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float og = o[i] * gg[i];
+          part = fmaf(og, og, part);
+        }
+        atomicAdd(p.ssq + static_cast<size_t>(b) * T + t0 + tl, part);
+      }
     }
     __syncwarp();
     if (lane == 0) {
@@ -682,7 +715,7 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
   if (p.HT != nullptr) store_state<V, MT, HALF>(p.HT + hoff, S.H, row0, g, c);
 }
 
-template <int V, int MT, bool F32, bool GATED>
+template <int V, int MT, bool F32, bool GATED, bool NORM>
 __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1)
     fwd_kernel(const FwdParams p) {
   using TIn = typename InType<F32>::T;
@@ -713,16 +746,24 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
     // the other warps runs into its time limit (tests of the time-out path).
     if (p.inject_stall == 0) fwd_producer<V, F32, GATED>(p, L, sbase, b, n0, Geff);
   } else if (warp == 1) {
-    fwd_epilogue<V, F32>(p, L, sbase, b, n0, Geff);
+    fwd_epilogue<V, F32, NORM>(p, L, sbase, b, n0, Geff);
   } else if (warp - 2 < ncons) {
     fwd_consumer<V, MT, F32>(p, L, sbase, b, n0, warp - 2);
   }
 }
 
+// The kernel instance for p's fused parts (gate, readout epilogue).
+template <int V, int MT, bool F32>
+auto select_kernel(const FwdParams& p) {
+  if (p.norm)
+    return p.gated ? fwd_kernel<V, MT, F32, true, true> : fwd_kernel<V, MT, F32, false, true>;
+  return p.gated ? fwd_kernel<V, MT, F32, true, false> : fwd_kernel<V, MT, F32, false, false>;
+}
+
 template <int V, int MT, bool F32>
 int ctas_per_sm_t(const FwdParams& p) {
   const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc);
-  auto kern = p.gated ? fwd_kernel<V, MT, F32, true> : fwd_kernel<V, MT, F32, false>;
+  auto kern = select_kernel<V, MT, F32>(p);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(L.total)) != cudaSuccess)
     return 0;
@@ -738,7 +779,7 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
   const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc);
   if (p.tc < 2 || p.tc > 32) return cudaErrorInvalidValue;
   if (p.G * p.WPH > max_consumer_warps<V, MT, F32>()) return cudaErrorInvalidConfiguration;
-  auto kern = p.gated ? fwd_kernel<V, MT, F32, true> : fwd_kernel<V, MT, F32, false>;
+  auto kern = select_kernel<V, MT, F32>(p);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L.total));
   if (e != cudaSuccess) return e;

@@ -46,6 +46,11 @@ struct FwdParams {
   const void* alpha = nullptr;
   const void* beta = nullptr;
   int gated = 0;
+  // readout epilogue (norm = 1): the epilogue adds sum (y (.) g)^2 of its
+  // heads for every token into ssq [B,T] (zeroed by the caller); g is [B,T,N,V]
+  const void* g = nullptr;
+  float* ssq = nullptr;
+  int norm = 0;
 };
 
 struct BwdParams {
@@ -114,6 +119,29 @@ struct DecodeParams {
   int Nq = 1;         // query/key groups (q, k are [B,Nq,K])
 };
 cudaError_t launch_decode(const DecodeParams& p, int V, bool f32_inputs, cudaStream_t stream);
+
+// Readout epilogue kernels (m2rnn_norm.cu).  Forward: turns the per-token
+// sums of squares ssq [T_all] into rstd = (ssq / d + eps)^(-1/2) in place and
+// writes out = w (.) y (.) g rstd.  Backward: from dout, y, g, w and rstd,
+// writes dy (input dtype) and dg (fp32) and adds sum dout (.) y (.) g rstd into
+// dw (fp32, zeroed by the caller).  Tokens are rows of d features.
+struct NormParams {
+  long long rows;   // B * T
+  int d;            // N * V features per token
+  float eps;
+  const void* y;    // [rows][d] input dtype
+  const void* g;    // [rows][d]
+  const void* w;    // [d]
+  float* rstd;      // [rows] (forward: holds ssq on entry)
+  void* out;        // forward: [rows][d] input dtype
+  const void* dout; // backward: [rows][d] input dtype
+  void* dy;         // backward: [rows][d] input dtype
+  float* dg;        // backward: [rows][d]
+  float* dw;        // backward: [d]
+};
+cudaError_t launch_norm_fwd(const NormParams& p, bool f32_inputs, int sms, cudaStream_t stream);
+cudaError_t launch_norm_bwd(const NormParams& p, bool f32_inputs, int sms, cudaStream_t stream);
+size_t norm_bwd_smem_bytes(int d);
 
 // Launches the forward kernel variant for (V, input dtype, MT m-tiles/warp).
 cudaError_t launch_fwd(const FwdParams& p, int V, bool f32_inputs, int MT, cudaStream_t stream);

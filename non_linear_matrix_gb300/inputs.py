@@ -51,6 +51,7 @@ class Workload:
     ckpt_every: int = 0  # checkpoint interval C for the backward (0 = none)
     decode: bool = False  # single-step decode (T = 1, state carried in HBM)
     gated: bool = False   # f computed from a, alpha, beta by the fused input gate
+    norm: bool = False    # readout epilogue: out = RMSNorm(y (.) g)
 
     @property
     def th(self) -> int:
@@ -71,6 +72,8 @@ WORKLOADS = {
                  backward=True, ckpt_every=64),
         Workload("fwdbwd_gated_bf16_b8_t4096_n32", 8, 4096, 32, 64, 16, "bf16", 4,
                  backward=True, ckpt_every=64, gated=True),
+        Workload("fwdbwd_norm_bf16_b8_t4096_n32", 8, 4096, 32, 64, 16, "bf16", 4,
+                 backward=True, ckpt_every=64, norm=True),
         Workload("decode_bf16_b2048_n32", 2048, 1, 32, 64, 16, "bf16", 6, decode=True),
     )
 }
@@ -116,4 +119,5 @@ def decode_state(B: int, N: int, K: int, V: int, seed: int) -> torch.Tensor:
 
 def workload_inputs(w: Workload, with_dy: bool | None = None) -> dict:
     return make_inputs(w.B, w.T, w.N, w.K, w.V, w.dtype, w.seed, w.f_mean,
-                       with_dy=w.backward if with_dy is None else with_dy, gated=w.gated)
+                       with_dy=w.backward if with_dy is None else with_dy, gated=w.gated,
+                       norm=w.norm)

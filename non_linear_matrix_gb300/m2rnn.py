@@ -42,6 +42,9 @@ _EXPORTS = {
     "m2rnn_decode": (ctypes.c_int, [_VP] * 11),
     "m2rnn_fwd_gated": (ctypes.c_int, [_VP] * 14),
     "m2rnn_bwd_gated": (ctypes.c_int, [_VP] * 24 + [ctypes.c_size_t, _VP]),
+    "m2rnn_fwd_norm": (ctypes.c_int, [_VP] * 13 + [ctypes.c_float] + [_VP] * 6),
+    "m2rnn_bwd_norm_workspace_size": (ctypes.c_size_t, [_VP, ctypes.c_int]),
+    "m2rnn_bwd_norm": (ctypes.c_int, [_VP] * 31 + [ctypes.c_size_t, _VP]),
 }
 
 
@@ -309,6 +312,81 @@ def bwd_gated(q, k, v, a, alpha, beta, W, w_r, dy, H0=None, ckpt=None, dHT=None,
     if dck is not None:
         g["dckpt"] = dck
     return g
+
+
+def fwd_norm(q, k, v, f, W, w_r, g, w_norm, eps: float = 0.0, H0=None, *, gate=None,
+             ckpt_every: int = 0, want_HT: bool = True, out=None, stream=None):
+    """Forward pass with the readout epilogue out = w_norm (.) (y (.) g) rstd,
+    rstd = (mean over the token's N*V features of (y (.) g)^2 + eps)^(-1/2).
+    ``gate=(a, alpha, beta)`` replaces f (pass f=None).  Returns dict(y, out,
+    rstd, HT, ckpt)."""
+    s = make_shape(q, v, ckpt_every)
+    a, alpha, beta = gate if gate is not None else (None, None, None)
+    out = dict(out or {})
+    r = {"y": out.get("y"), "out": out.get("out"), "rstd": out.get("rstd"),
+         "HT": out.get("HT"), "ckpt": out.get("ckpt")}
+    if r["y"] is None:
+        r["y"] = torch.empty_like(v)
+    if r["out"] is None:
+        r["out"] = torch.empty_like(v)
+    if r["rstd"] is None:
+        r["rstd"] = torch.empty(s.B, s.T, device=q.device, dtype=torch.float32)
+    if r["HT"] is None and want_HT:
+        r["HT"] = torch.empty(s.B, s.N, s.K, s.V, device=q.device, dtype=torch.float32)
+    nck = num_checkpoints(s)
+    if r["ckpt"] is None and nck > 0:
+        r["ckpt"] = torch.empty(s.B, s.N, nck, s.K, s.V, device=q.device, dtype=torch.float32)
+    rc = lib().m2rnn_fwd_norm(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(a),
+                              _ptr(alpha), _ptr(beta), _ptr(W), _ptr(w_r), _ptr(H0), _ptr(g),
+                              _ptr(w_norm), ctypes.c_float(eps), _ptr(r["y"]), _ptr(r["out"]),
+                              _ptr(r["rstd"]), _ptr(r["HT"]), _ptr(r["ckpt"]), _stream(stream))
+    _check(rc, "m2rnn_fwd_norm")
+    return r
+
+
+def bwd_norm(q, k, v, f, W, w_r, g, w_norm, y, rstd, dout, H0=None, ckpt=None, dHT=None, *,
+             gate=None, ckpt_every: int = 64, want_dH0: bool = False, want_dckpt: bool = False,
+             workspace=None, out=None, stream=None):
+    """Backward pass through the readout epilogue and the recurrence.
+    Returns dict(dq, dk, dv, df | da+dalpha+dbeta, dW, dw_r, dg, dw_norm
+    [, dH0][, dckpt]) (fp32)."""
+    s = make_shape(q, v, ckpt_every)
+    a, alpha, beta = gate if gate is not None else (None, None, None)
+    f32 = dict(device=q.device, dtype=torch.float32)
+    out = dict(out or {})
+    shapes = {"dq": tuple(q.shape), "dk": tuple(q.shape), "dv": (s.B, s.T, s.N, s.V),
+              "dW": (s.N, s.V, s.V), "dw_r": (s.N, s.V), "dg": (s.B, s.T, s.N, s.V),
+              "dw_norm": (s.N, s.V)}
+    if gate is None:
+        shapes["df"] = (s.B, s.T, s.N)
+    else:
+        shapes.update(da=(s.B, s.T, s.N), dalpha=(s.N,), dbeta=(s.N,))
+    gr = {n: out.get(n) if out.get(n) is not None else torch.empty(shp, **f32)
+          for n, shp in shapes.items()}
+    dH0 = out.get("dH0")
+    if dH0 is None and want_dH0:
+        dH0 = torch.empty(s.B, s.N, s.K, s.V, **f32)
+    dck = out.get("dckpt")
+    if dck is None and want_dckpt:
+        dck = torch.empty(s.B, s.N, num_checkpoints(s), s.K, s.V, **f32)
+    need = int(lib().m2rnn_bwd_norm_workspace_size(ctypes.byref(s), int(ckpt is not None)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    dfa = gr["df"] if gate is None else gr["da"]
+    rc = lib().m2rnn_bwd_norm(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(a),
+                              _ptr(alpha), _ptr(beta), _ptr(W), _ptr(w_r), _ptr(H0), _ptr(ckpt),
+                              _ptr(g), _ptr(w_norm), _ptr(y), _ptr(rstd), _ptr(dout), _ptr(dHT),
+                              _ptr(gr["dq"]), _ptr(gr["dk"]), _ptr(gr["dv"]), _ptr(dfa),
+                              _ptr(gr.get("dalpha")), _ptr(gr.get("dbeta")), _ptr(gr["dW"]),
+                              _ptr(gr["dw_r"]), _ptr(gr["dg"]), _ptr(gr["dw_norm"]), _ptr(dH0),
+                              _ptr(dck), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                              _stream(stream))
+    _check(rc, "m2rnn_bwd_norm")
+    if dH0 is not None:
+        gr["dH0"] = dH0
+    if dck is not None:
+        gr["dckpt"] = dck
+    return gr
 
 
 def device_status(clear: bool = True, stream=None):

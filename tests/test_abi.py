@@ -116,3 +116,20 @@ def test_groups_must_divide_heads(lib, Nq):
     s = ctypes.byref(Shape(1, 8, 4, 64, 16, 1, 0, Nq))
     assert lib.m2rnn_fwd(s, p, p, p, p, p, p, None, p, None, None, None) == -1
     assert lib.m2rnn_decode(ctypes.byref(Shape(1, 1, 4, 64, 16, 1, 0, Nq)), *([p] * 10)) == -1
+
+
+def test_norm_entry_points_take_f_or_gate(lib):
+    """m2rnn_fwd_norm / m2rnn_bwd_norm take f or (a, alpha, beta), exactly
+    one form; the choice is checked before anything else."""
+    from non_linear_matrix_gb300.m2rnn import Shape
+    p = ctypes.c_void_p(16)
+    s = ctypes.byref(Shape(1, 8, 2, 64, 16, 1, 4))
+    eps = ctypes.c_float(0.0)
+    both = [p, p, p, p]      # f and the gate
+    neither = [None] * 4
+    for fa in (both, neither, [p, p, None, p]):
+        assert lib.m2rnn_fwd_norm(s, p, p, p, *fa, p, p, None, p, p, eps, p, p, p, None, None,
+                                  None) == -1
+        assert lib.m2rnn_bwd_norm(s, p, p, p, *fa, p, p, None, None, *([p] * 5), None,
+                                  *([p] * 10), None, None, p, ctypes.c_size_t(1 << 20),
+                                  None) == -1
