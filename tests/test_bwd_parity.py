@@ -202,12 +202,14 @@ def test_workload_fwd_bwd(m2rnn, oracle_mod):
 
 @pytest.mark.parametrize("kernel", ["0", "1"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("T,C", [(100, 12), (61, 7), (130, 64), (64, 64)])
+@pytest.mark.parametrize("T,C", [(100, 12), (61, 7), (130, 64), (64, 64), (1, 4), (9, 8), (24, 8)])
 def test_kernel_variants(m2rnn, oracle_mod, monkeypatch, kernel, dtype, T, C):
     """Both backward kernels: serial (0) and pipelined (1).  C = 12 and 7
     are not multiples of the sub-interval length, and the ragged last
     interval leaves part of the next interval's recompute to run after its
-    sub-intervals in the pipelined kernel."""
+    sub-intervals in the pipelined kernel; T = 1 and 9 are one and two
+    intervals, T = 24 with C = 8 three intervals of one sub-interval each
+    (every slot then reads and rewrites the same sub-checkpoint slot)."""
     monkeypatch.setenv("M2RNN_BWD_KERNEL", kernel)
     x = make_inputs(2, T, 3, 64, 16, dtype, 300 + T + C, with_dy=True)
     gen = torch.Generator().manual_seed(C)
@@ -255,3 +257,4 @@ def test_grouped_qk_recomputed_v32_f32(m2rnn, oracle_mod):
     grouped producer), V = 32, fp32 inputs."""
     x = make_inputs(2, 70, 4, 64, 32, "f32", 931, with_dy=True, groups=2)
     _restart_parity(m2rnn, oracle_mod, x, 16, give_ckpt=False, label="Nq2 v32 f32")
+
