@@ -56,8 +56,9 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
   const int b = static_cast<int>(head / N), n = static_cast<int>(head % N);
   const int row0 = 16 * MT * warp;  // MT 16-row tiles per warp
 
-  // [B,Nq,K]: the row of head n's query/key group
-  const size_t qrow = static_cast<size_t>(b) * p.Nq + n / (N / p.Nq);
+  // [B,Nq,K]: the row of head n's query/key group (no division when shared)
+  const size_t qrow = p.Nq == 1 ? static_cast<size_t>(b)
+                                : static_cast<size_t>(b) * p.Nq + n / (N / p.Nq);
   const TIn* q = static_cast<const TIn*>(p.q) + qrow * K;
   const TIn* k = static_cast<const TIn*>(p.k) + qrow * K;
   const TIn* v = static_cast<const TIn*>(p.v) + head * V;
