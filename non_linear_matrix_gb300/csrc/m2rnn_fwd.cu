@@ -715,9 +715,18 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
   if (p.HT != nullptr) store_state<V, MT, HALF>(p.HT + hoff, S.H, row0, g, c);
 }
 
-template <int V, int MT, bool F32, bool GATED, bool NORM>
+// KC, GC (0 = taken from the parameters): K and heads per CTA fixed at
+// compile time, so that every shared-memory stride of the step loops is an
+// immediate (instances for the common K = 64 launches).
+template <int V, int MT, bool F32, bool GATED, bool NORM, int KC = 0, int GC = 0>
 __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1)
-    fwd_kernel(const FwdParams p) {
+    fwd_kernel(const FwdParams prm) {
+  FwdParams p = prm;
+  if constexpr (KC > 0) {
+    p.K = KC;
+    p.WPH = MT == 0 ? KC / 8 : KC / (16 * MT);
+  }
+  if constexpr (GC > 0) p.G = GC;
   using TIn = typename InType<F32>::T;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
@@ -755,6 +764,14 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
 // The kernel instance for p's fused parts (gate, readout epilogue).
 template <int V, int MT, bool F32>
 auto select_kernel(const FwdParams& p) {
+  // the instances with compile-time K and G (the K = 64 launches of large
+  // batches; a G = 1, MT = 1 instance measured slower than the generic one)
+  if constexpr (V == 16 && MT == 2 && !F32) {
+    if (!p.norm && !p.gated && p.K == 64 && p.WPH == 2) {
+      if (p.G == 8) return fwd_kernel<16, 2, false, false, false, 64, 8>;
+      if (p.G == 2) return fwd_kernel<16, 2, false, false, false, 64, 2>;
+    }
+  }
   if (p.norm)
     return p.gated ? fwd_kernel<V, MT, F32, true, true> : fwd_kernel<V, MT, F32, false, true>;
   return p.gated ? fwd_kernel<V, MT, F32, true, false> : fwd_kernel<V, MT, F32, false, false>;
