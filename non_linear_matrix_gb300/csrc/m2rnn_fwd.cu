@@ -86,8 +86,8 @@ __host__ __device__ inline FwdLayout fwd_layout(int K, int V, int G, int WPH, in
   o = align_up(o + TC * K * es, 128);
   L.v = o;
   o = align_up(o + TC * G * V * es, 128);
-  L.kd = o;
-  o = align_up(o + TC * K * 8, 128);
+  L.kd = o;  // fp32-input path only (the bf16 path reads k raw)
+  o = align_up(o + (es == 4 ? TC * K * 8 : 0), 128);
   L.fd = o;
   o = align_up(o + TC * G * 8, 128);
   L.stage = o;
@@ -223,7 +223,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
     if (!warp_wait(bar_raw_full(bars, s), (ch / NSTAGE) & 1, p.wait_limit_ns)) return false;
     const int Tc = min(TC, T - ch * TC);
     const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
-    const int n8 = Tc * K / 8;
+    const int n8 = F32 ? Tc * K / 8 : 0;  // the bf16 path uses k as copied
     for (int i = lane; i < n8; i += 32) {
       float x[8];
       if (F32) {
@@ -450,27 +450,43 @@ __device__ __forceinline__ void pack_a_lo(const float (&H)[V / 8][4], const uint
 // Rank-1 inputs of one step, read one step ahead of their use:
 // k as fp32 pairs (k_i, k_i) at rows 16mt+g and 16mt+8+g, and v at columns
 // 8nt+2c, 8nt+2c+1 (bf16x2 in the bf16 path, fp32 pair in the fp32 path).
+// bf16 path: the rank-1 term as an MMA of two one-column operands, k as
+// (k_i, 0) A-operand words at rows 16mt+g and 16mt+8+g and v as (v_j, 0)
+// B-operand words at columns 8nt+g, on the lanes with c == 0 (zero on the
+// others).
 template <int MT, int NT, bool F32>
 struct StepIn {
   float2 k0[MT], k1[MT];
   uint32_t vb[NT];
   float2 vf[NT];
+  float kv[MT][NT][4];  // bf16 path: k v^T of the step, formed while the previous step runs
 };
 
+// kdb: the step's k (fp32 pairs in the fp32 path, raw bf16 otherwise) at
+// this warp's first row; vb: its v (raw) at this head.
 template <int V, int MT, bool F32, bool HALF = false>
 __device__ __forceinline__ void load_step(StepIn<MT, V / 8, F32>& in, uint32_t kdb, uint32_t vb,
                                           int g, int c) {
+  if constexpr (F32) {
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    in.k0[mt] = ptx::lds_f32x2(kdb + 8 * (16 * mt + g));
-    in.k1[mt] = HALF ? make_float2(0.f, 0.f) : ptx::lds_f32x2(kdb + 8 * (16 * mt + 8 + g));
-  }
+    for (int mt = 0; mt < MT; ++mt) {
+      in.k0[mt] = ptx::lds_f32x2(kdb + 8 * (16 * mt + g));
+      in.k1[mt] = HALF ? make_float2(0.f, 0.f) : ptx::lds_f32x2(kdb + 8 * (16 * mt + 8 + g));
+    }
 #pragma unroll
-  for (int nt = 0; nt < V / 8; ++nt) {
-    if (F32)
-      in.vf[nt] = ptx::lds_f32x2(vb + 4 * (8 * nt + 2 * c));
-    else
-      in.vb[nt] = ptx::lds_u32(vb + 2 * (8 * nt + 2 * c));
+    for (int nt = 0; nt < V / 8; ++nt) in.vf[nt] = ptx::lds_f32x2(vb + 4 * (8 * nt + 2 * c));
+  } else {
+    uint32_t vz[V / 8];
+#pragma unroll
+    for (int nt = 0; nt < V / 8; ++nt) vz[nt] = c == 0 ? ptx::lds_u16(vb + 2 * (8 * nt + g)) : 0u;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const uint32_t Ak[4] = {c == 0 ? ptx::lds_u16(kdb + 2 * (16 * mt + g)) : 0u,
+                              (c == 0 && !HALF) ? ptx::lds_u16(kdb + 2 * (16 * mt + 8 + g)) : 0u,
+                              0u, 0u};
+#pragma unroll
+      for (int nt = 0; nt < V / 8; ++nt) ptx::mma_bf16_16816_zero(in.kv[mt][nt], Ak, vz[nt], 0u);
+    }
   }
 }
 
@@ -506,23 +522,25 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
   }
   const float2 f2 = ptx::lds_f32x2(fdaddr);
   const float2 m1 = make_float2(-1.f, -1.f);
-  float2 vv[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-    vv[nt] = F32 ? in.vf[nt] : make_float2(ptx::bf16x2_lo(in.vb[nt]), ptx::bf16x2_hi(in.vb[nt]));
   float ya[NT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
-    // acc = k v^T (exact fp32 products), then acc += bf16(H) W on the tensor core.
+    // acc = k v^T (exact fp32 products: one nonzero product per element in
+    // the bf16 path's MMA), then acc += bf16(H) W on the tensor core.
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float2 lo = __fmul2_rn(in.k0[mt], vv[nt]);
-      const float2 hi = HALF ? make_float2(0.f, 0.f) : __fmul2_rn(in.k1[mt], vv[nt]);
-      acc[nt][0] = lo.x;
-      acc[nt][1] = lo.y;
-      acc[nt][2] = hi.x;
-      acc[nt][3] = hi.y;
+      if constexpr (F32) {
+        const float2 lo = __fmul2_rn(in.k0[mt], in.vf[nt]);
+        const float2 hi = HALF ? make_float2(0.f, 0.f) : __fmul2_rn(in.k1[mt], in.vf[nt]);
+        acc[nt][0] = lo.x;
+        acc[nt][1] = lo.y;
+        acc[nt][2] = hi.x;
+        acc[nt][3] = hi.y;
+      } else {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[nt][r] = in.kv[mt][nt][r];
+      }
     }
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks)
@@ -649,7 +667,7 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
   const int nchunks = (T + TC - 1) / TC;
   // Per-time-step strides of this lane's shared-memory reads.
   const uint32_t q_stride = static_cast<uint32_t>(K * es);
-  const uint32_t kd_stride = static_cast<uint32_t>(K * 8);
+  const uint32_t kd_stride = static_cast<uint32_t>(F32 ? K * 8 : K * 2);
   const uint32_t v_stride = static_cast<uint32_t>(G * V * es);
   const uint32_t fd_stride = static_cast<uint32_t>(G * 8);
   const uint32_t yp_stride = static_cast<uint32_t>(G * WPH * V * 4);
@@ -666,7 +684,8 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
     const int Tc = min(TC, T - t0);
     const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
     const uint32_t qb = st + L.q + static_cast<uint32_t>(row0 * es);
-    const uint32_t kdb = st + L.kd + static_cast<uint32_t>(row0 * 8);
+    const uint32_t kdb = F32 ? st + L.kd + static_cast<uint32_t>(row0 * 8)
+                             : st + L.k + static_cast<uint32_t>(row0 * 2);
     const uint32_t vb = st + L.v + static_cast<uint32_t>(hl * V * es);
     const uint32_t fdb = st + L.fd + static_cast<uint32_t>(hl * 8);
     const uint32_t yb = sbase + L.yp_base + static_cast<uint32_t>(ys) * L.yp_stage +

@@ -85,9 +85,11 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 
 // ---- shared memory (explicit state space, 32-bit shared addresses) -------
 
+// 16-bit shared-memory load, zero-extended into a 32-bit register (a bf16
+// value in the low half).
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
