@@ -500,34 +500,77 @@ struct WarpState {
   uint32_t Al[MT][V / 16][4];      // residual of bf16(H) (fp32-input path)
 };
 
-// One recurrence step for this warp's MT slices; writes the slices' readout
-// partial (columns 8nt+2c, +1, on lanes with g == 0) to ypaddr.
+// Readout partial y^T = q^T H of this warp's MT slices on the tensor core
+// (bf16 path): A = q in every row, B = the slices of bf16(H) transposed
+// 8x8-blockwise; columns 8nt+2c, +1 are stored to ypaddr by lanes g == 0.
+template <int V, int MT, bool HALF>
+__device__ __forceinline__ void readout_bf16(const uint32_t (&A)[MT][V / 16][4], uint32_t qb,
+                                             uint32_t ypaddr, int g, int c) {
+  constexpr int NT = V / 8, KS = V / 16;
+  float ya[NT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const uint32_t q0 = ptx::lds_u32(qb + 2 * (16 * mt + 2 * c));
+    const uint32_t q1 = ptx::lds_u32(qb + 2 * (16 * mt + 8 + 2 * c));
+    const uint32_t Aq[4] = {q0, q0, q1, q1};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const uint32_t b0 = ptx::movmatrix_trans(A[mt][ks][2 * h2]);
+        const uint32_t b1 = HALF ? 0u : ptx::movmatrix_trans(A[mt][ks][2 * h2 + 1]);
+        if (mt == 0)
+          ptx::mma_bf16_16816_zero(ya[2 * ks + h2], Aq, b0, b1);
+        else
+          ptx::mma_bf16_16816(ya[2 * ks + h2], Aq, b0, b1);
+      }
+  }
+  if (g == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) ptx::sts_f32x2(ypaddr + 4 * (8 * nt + 2 * c), ya[nt][0], ya[nt][1]);
+  }
+}
+
+// Whether a step writes the previous step's readout (bf16, one 16-row slice
+// per warp: the readout's transposes and MMA then fill the latency of the
+// state products) instead of its own (measured slower with two slices per
+// warp, where the two slices' chains already overlap).
+template <int MT, bool F32>
+__host__ __device__ constexpr bool defer_readout() {
+  return !F32 && MT == 1;
+}
+
+// One recurrence step for this warp's MT slices.  Writes a readout partial
+// (columns 8nt+2c, +1, on lanes with g == 0) to ypaddr from q at qb: the
+// step's own, or with defer_readout() the previous step's, formed from the
+// bf16(H) operand of this step's H W products before they are used (the last
+// step of a run then needs readout_bf16 afterwards).
 template <int V, int MT, bool F32, bool HALF = false>
 __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V / 8, F32>& in,
                                          uint32_t qb, uint32_t fdaddr, uint32_t ypaddr, int g,
                                          int c) {
   constexpr int NT = V / 8, KS = V / 16;
+  constexpr bool DEFER = defer_readout<MT, F32>();
   // q (for the readout) and f are read here; their use is tens of cycles on.
   uint32_t qa[MT][2];
   float qf[MT][2];
+  if constexpr (!DEFER) {
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    if (F32) {
-      qf[mt][0] = ptx::lds_f32(qb + 4 * (16 * mt + g));
-      qf[mt][1] = ptx::lds_f32(qb + 4 * (16 * mt + 8 + g));
-    } else {
-      qa[mt][0] = ptx::lds_u32(qb + 2 * (16 * mt + 2 * c));
-      qa[mt][1] = ptx::lds_u32(qb + 2 * (16 * mt + 8 + 2 * c));
+    for (int mt = 0; mt < MT; ++mt) {
+      if (F32) {
+        qf[mt][0] = ptx::lds_f32(qb + 4 * (16 * mt + g));
+        qf[mt][1] = ptx::lds_f32(qb + 4 * (16 * mt + 8 + g));
+      } else {
+        qa[mt][0] = ptx::lds_u32(qb + 2 * (16 * mt + 2 * c));
+        qa[mt][1] = ptx::lds_u32(qb + 2 * (16 * mt + 8 + 2 * c));
+      }
     }
   }
   const float2 f2 = ptx::lds_f32x2(fdaddr);
   const float2 m1 = make_float2(-1.f, -1.f);
-  float ya[NT][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    // acc = k v^T (exact fp32 products: one nonzero product per element in
-    // the bf16 path's MMA), then acc += bf16(H) W on the tensor core.
-    float acc[NT][4];
+  // acc = k v^T (exact fp32 products: one nonzero product per element in
+  // the bf16 path's MMA), then acc += bf16(H) W on the tensor core.
+  auto products = [&](int mt, float (&acc)[NT][4]) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       if constexpr (F32) {
@@ -552,7 +595,9 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
           ptx::mma_bf16_16816(acc[nt], S.Al[mt][ks], S.Bw[ks][nt][0], S.Bw[ks][nt][1]);
         }
       }
-    // Z = tanh(acc); H = Z + f (H - Z)
+  };
+  // Z = tanh(acc); H = Z + f (H - Z); the next step's A operand
+  auto update = [&](int mt, const float (&acc)[NT][4]) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -567,8 +612,24 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
         S.H[mt][nt][2 * h + 1] = hn.y;
       }
     pack_a<V, HALF>(S.H[mt], S.A[mt]);
+    if (F32) pack_a_lo<V>(S.H[mt], S.A[mt], S.Al[mt]);
+  };
+  if constexpr (DEFER) {
+    float acc[MT][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) products(mt, acc[mt]);
+    readout_bf16<V, MT, HALF>(S.A, qb, ypaddr, g, c);  // the previous step's, in the MMAs' shadow
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) update(mt, acc[mt]);
+    return;
+  }
+  float ya[NT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    float acc[NT][4];
+    products(mt, acc);
+    update(mt, acc);
     if constexpr (F32) {
-      pack_a_lo<V>(S.H[mt], S.A[mt], S.Al[mt]);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const float p0 = fmaf(qf[mt][0], S.H[mt][nt][0], qf[mt][1] * S.H[mt][nt][2]);
@@ -702,24 +763,34 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
         next_ck += p.C;
       }
       const int seg_end = min(Tc, next_ck - t0);  // no checkpoint inside [tl, seg_end)
+      // The readout a step writes: its own, or with defer_readout() the
+      // previous step's (at the chunk's first step a placeholder for step 0,
+      // overwritten by step 0's readout before the chunk is released).
+      auto ro = [](uint32_t u) -> uint32_t {
+        return defer_readout<MT, F32>() ? (u > 0 ? u - 1 : 0) : u;
+      };
 #pragma unroll 1
       for (; tl + 1 < seg_end; tl += 2) {
         const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1, u2 = u0 + 2;
         load_step<V, MT, F32, HALF>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
-        fwd_step<V, MT, F32, HALF>(S, in0, qb + u0 * q_stride, fdb + u0 * fd_stride,
-                             yb + u0 * yp_stride, g, c);
+        fwd_step<V, MT, F32, HALF>(S, in0, qb + ro(u0) * q_stride, fdb + u0 * fd_stride,
+                             yb + ro(u0) * yp_stride, g, c);
         load_step<V, MT, F32, HALF>(in0, kdb + u2 * kd_stride, vb + u2 * v_stride, g, c);
-        fwd_step<V, MT, F32, HALF>(S, in1, qb + u1 * q_stride, fdb + u1 * fd_stride,
-                             yb + u1 * yp_stride, g, c);
+        fwd_step<V, MT, F32, HALF>(S, in1, qb + ro(u1) * q_stride, fdb + u1 * fd_stride,
+                             yb + ro(u1) * yp_stride, g, c);
       }
       if (tl < seg_end) {  // odd remainder of the segment
         const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1;
         load_step<V, MT, F32, HALF>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
-        fwd_step<V, MT, F32, HALF>(S, in0, qb + u0 * q_stride, fdb + u0 * fd_stride,
-                             yb + u0 * yp_stride, g, c);
+        fwd_step<V, MT, F32, HALF>(S, in0, qb + ro(u0) * q_stride, fdb + u0 * fd_stride,
+                             yb + ro(u0) * yp_stride, g, c);
         in0 = in1;
         ++tl;
       }
+    }
+    if constexpr (defer_readout<MT, F32>()) {  // the chunk's last step's readout
+      const uint32_t ul = static_cast<uint32_t>(Tc - 1);
+      readout_bf16<V, MT, HALF>(S.A, qb + ul * q_stride, yb + ul * yp_stride, g, c);
     }
     __syncwarp();
     if (lane == 0) {
