@@ -64,6 +64,15 @@ constexpr int max_consumer_warps() {
   return (V == 16 && MT <= 2 && !F32) || (V == 16 && MT == 1) ? 16 : 8;
 }
 
+// The rank-1 term k v^T from fp32 (k, k) pairs the producer writes and a
+// packed fp32 multiply (fp32 inputs, and V = 32, where the tensor-core form's
+// prefetched products need 32 more registers per thread and measured
+// slower); otherwise from an MMA of two one-column bf16 operands.
+template <int V, bool F32>
+__host__ __device__ constexpr bool rank1_pairs() {
+  return F32 || V != 16;
+}
+
 struct FwdLayout {
   uint32_t q, k, v;    // raw bulk-copied inputs (input dtype)
   uint32_t kd, fd;     // k as fp32 pairs [TC][K][2], f as fp32 pairs [TC][G][2]
@@ -86,8 +95,8 @@ __host__ __device__ inline FwdLayout fwd_layout(int K, int V, int G, int WPH, in
   o = align_up(o + TC * K * es, 128);
   L.v = o;
   o = align_up(o + TC * G * V * es, 128);
-  L.kd = o;  // fp32-input path only (the bf16 path reads k raw)
-  o = align_up(o + (es == 4 ? TC * K * 8 : 0), 128);
+  L.kd = o;  // fp32 pairs of k, except for bf16 inputs at V = 16 (k read raw)
+  o = align_up(o + ((es == 4 || V != 16) ? TC * K * 8 : 0), 128);
   L.fd = o;
   o = align_up(o + TC * G * 8, 128);
   L.stage = o;
@@ -223,7 +232,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
     if (!warp_wait(bar_raw_full(bars, s), (ch / NSTAGE) & 1, p.wait_limit_ns)) return false;
     const int Tc = min(TC, T - ch * TC);
     const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
-    const int n8 = F32 ? Tc * K / 8 : 0;  // the bf16 path uses k as copied
+    const int n8 = rank1_pairs<V, F32>() ? Tc * K / 8 : 0;  // else k is used as copied
     for (int i = lane; i < n8; i += 32) {
       float x[8];
       if (F32) {
@@ -467,14 +476,19 @@ struct StepIn {
 template <int V, int MT, bool F32, bool HALF = false>
 __device__ __forceinline__ void load_step(StepIn<MT, V / 8, F32>& in, uint32_t kdb, uint32_t vb,
                                           int g, int c) {
-  if constexpr (F32) {
+  if constexpr (rank1_pairs<V, F32>()) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       in.k0[mt] = ptx::lds_f32x2(kdb + 8 * (16 * mt + g));
       in.k1[mt] = HALF ? make_float2(0.f, 0.f) : ptx::lds_f32x2(kdb + 8 * (16 * mt + 8 + g));
     }
 #pragma unroll
-    for (int nt = 0; nt < V / 8; ++nt) in.vf[nt] = ptx::lds_f32x2(vb + 4 * (8 * nt + 2 * c));
+    for (int nt = 0; nt < V / 8; ++nt) {
+      if (F32)
+        in.vf[nt] = ptx::lds_f32x2(vb + 4 * (8 * nt + 2 * c));
+      else
+        in.vb[nt] = ptx::lds_u32(vb + 2 * (8 * nt + 2 * c));
+    }
   } else {
     uint32_t vz[V / 8];
 #pragma unroll
@@ -573,9 +587,11 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
   auto products = [&](int mt, float (&acc)[NT][4]) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      if constexpr (F32) {
-        const float2 lo = __fmul2_rn(in.k0[mt], in.vf[nt]);
-        const float2 hi = HALF ? make_float2(0.f, 0.f) : __fmul2_rn(in.k1[mt], in.vf[nt]);
+      if constexpr (rank1_pairs<V, F32>()) {
+        const float2 vv =
+            F32 ? in.vf[nt] : make_float2(ptx::bf16x2_lo(in.vb[nt]), ptx::bf16x2_hi(in.vb[nt]));
+        const float2 lo = __fmul2_rn(in.k0[mt], vv);
+        const float2 hi = HALF ? make_float2(0.f, 0.f) : __fmul2_rn(in.k1[mt], vv);
         acc[nt][0] = lo.x;
         acc[nt][1] = lo.y;
         acc[nt][2] = hi.x;
@@ -728,7 +744,7 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
   const int nchunks = (T + TC - 1) / TC;
   // Per-time-step strides of this lane's shared-memory reads.
   const uint32_t q_stride = static_cast<uint32_t>(K * es);
-  const uint32_t kd_stride = static_cast<uint32_t>(F32 ? K * 8 : K * 2);
+  const uint32_t kd_stride = static_cast<uint32_t>(rank1_pairs<V, F32>() ? K * 8 : K * 2);
   const uint32_t v_stride = static_cast<uint32_t>(G * V * es);
   const uint32_t fd_stride = static_cast<uint32_t>(G * 8);
   const uint32_t yp_stride = static_cast<uint32_t>(G * WPH * V * 4);
@@ -745,8 +761,8 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
     const int Tc = min(TC, T - t0);
     const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
     const uint32_t qb = st + L.q + static_cast<uint32_t>(row0 * es);
-    const uint32_t kdb = F32 ? st + L.kd + static_cast<uint32_t>(row0 * 8)
-                             : st + L.k + static_cast<uint32_t>(row0 * 2);
+    const uint32_t kdb = rank1_pairs<V, F32>() ? st + L.kd + static_cast<uint32_t>(row0 * 8)
+                                               : st + L.k + static_cast<uint32_t>(row0 * 2);
     const uint32_t vb = st + L.v + static_cast<uint32_t>(hl * V * es);
     const uint32_t fdb = st + L.fd + static_cast<uint32_t>(hl * 8);
     const uint32_t yb = sbase + L.yp_base + static_cast<uint32_t>(ys) * L.yp_stage +
