@@ -278,3 +278,27 @@ def test_grouped_qk_wave_split(m2rnn, oracle_mod):
     with 4 groups of 8 heads: both launches' q/k offsets."""
     x = make_inputs(41, 40, 32, 64, 16, "bf16", 733, groups=4)
     _compare(m2rnn, oracle_mod, x, "bf16", label="Nq4 wave split")
+
+
+def test_state_bitwise_across_launch_variants(m2rnn, monkeypatch):
+    """The state update is the same per element whatever the launch shape:
+    the whole-wave and tail launches with compile-time K and heads per CTA
+    (two slices per warp), the generic instance with one slice per warp
+    (previous step's readout deferred) and a single launch all give the same
+    H_T bit for bit (y may differ in the last bits: its row sums are grouped
+    by warp)."""
+    x = _dev(make_inputs(41, 96, 32, 64, 16, "bf16", 733))
+    runs = {}
+    for name, env in (("planned", {}), ("one_slice", {"M2RNN_FWD_MT": "1"}),
+                      ("one_launch", {"M2RNN_FWD_ONE_LAUNCH": "1"})):
+        for k in ("M2RNN_FWD_MT", "M2RNN_FWD_ONE_LAUNCH"):
+            monkeypatch.delenv(k, raising=False)
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        y, HT, _ = m2rnn.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"])
+        torch.cuda.synchronize()
+        runs[name] = (y.float(), HT)
+    _check_status(m2rnn)
+    for name in ("one_slice", "one_launch"):
+        assert torch.equal(runs[name][1], runs["planned"][1]), name
+        assert (runs[name][0] - runs["planned"][0]).abs().max().item() <= 2e-2, name
