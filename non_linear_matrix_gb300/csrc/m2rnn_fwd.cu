@@ -637,56 +637,56 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
     readout_bf16<V, MT, HALF>(S.A, qb, ypaddr, g, c);  // the previous step's, in the MMAs' shadow
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) update(mt, acc[mt]);
-    return;
-  }
-  float ya[NT][4];
+  } else {
+    float ya[NT][4];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    float acc[NT][4];
-    products(mt, acc);
-    update(mt, acc);
-    if constexpr (F32) {
+    for (int mt = 0; mt < MT; ++mt) {
+      float acc[NT][4];
+      products(mt, acc);
+      update(mt, acc);
+      if constexpr (F32) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float p0 = fmaf(qf[mt][0], S.H[mt][nt][0], qf[mt][1] * S.H[mt][nt][2]);
-        const float p1 = fmaf(qf[mt][0], S.H[mt][nt][1], qf[mt][1] * S.H[mt][nt][3]);
-        ya[nt][0] = mt == 0 ? p0 : ya[nt][0] + p0;
-        ya[nt][1] = mt == 0 ? p1 : ya[nt][1] + p1;
+        for (int nt = 0; nt < NT; ++nt) {
+          const float p0 = fmaf(qf[mt][0], S.H[mt][nt][0], qf[mt][1] * S.H[mt][nt][2]);
+          const float p1 = fmaf(qf[mt][0], S.H[mt][nt][1], qf[mt][1] * S.H[mt][nt][3]);
+          ya[nt][0] = mt == 0 ? p0 : ya[nt][0] + p0;
+          ya[nt][1] = mt == 0 ? p1 : ya[nt][1] + p1;
+        }
+      } else {
+        // Readout y^T += q^T H on the tensor core: A = q in every row,
+        // B = this slice of bf16(H_t) transposed 8x8-blockwise.
+        const uint32_t Aq[4] = {qa[mt][0], qa[mt][0], qa[mt][1], qa[mt][1]};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const uint32_t b0 = ptx::movmatrix_trans(S.A[mt][ks][2 * h2]);
+            const uint32_t b1 = HALF ? 0u : ptx::movmatrix_trans(S.A[mt][ks][2 * h2 + 1]);
+            if (mt == 0)
+              ptx::mma_bf16_16816_zero(ya[2 * ks + h2], Aq, b0, b1);
+            else
+              ptx::mma_bf16_16816(ya[2 * ks + h2], Aq, b0, b1);
+          }
       }
-    } else {
-      // Readout y^T += q^T H on the tensor core: A = q in every row,
-      // B = this slice of bf16(H_t) transposed 8x8-blockwise.
-      const uint32_t Aq[4] = {qa[mt][0], qa[mt][0], qa[mt][1], qa[mt][1]};
+    }
+    if constexpr (F32) {
+      // Sum the fp32 partials over the 8 lanes of each column group.
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const uint32_t b0 = ptx::movmatrix_trans(S.A[mt][ks][2 * h2]);
-          const uint32_t b1 = HALF ? 0u : ptx::movmatrix_trans(S.A[mt][ks][2 * h2 + 1]);
-          if (mt == 0)
-            ptx::mma_bf16_16816_zero(ya[2 * ks + h2], Aq, b0, b1);
-          else
-            ptx::mma_bf16_16816(ya[2 * ks + h2], Aq, b0, b1);
+        for (int e = 0; e < 2; ++e) {
+          float x = ya[nt][e];
+          x += __shfl_xor_sync(0xffffffffu, x, 4);
+          x += __shfl_xor_sync(0xffffffffu, x, 8);
+          x += __shfl_xor_sync(0xffffffffu, x, 16);
+          ya[nt][e] = x;
         }
     }
-  }
-  if constexpr (F32) {
-    // Sum the fp32 partials over the 8 lanes of each column group.
+    if (g == 0) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float x = ya[nt][e];
-        x += __shfl_xor_sync(0xffffffffu, x, 4);
-        x += __shfl_xor_sync(0xffffffffu, x, 8);
-        x += __shfl_xor_sync(0xffffffffu, x, 16);
-        ya[nt][e] = x;
-      }
-  }
-  if (g == 0) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) ptx::sts_f32x2(ypaddr + 4 * (8 * nt + 2 * c), ya[nt][0], ya[nt][1]);
-  }
+      for (int nt = 0; nt < NT; ++nt) ptx::sts_f32x2(ypaddr + 4 * (8 * nt + 2 * c), ya[nt][0], ya[nt][1]);
+    }
+  }  // !DEFER
 }
 
 template <int V, int MT_, bool F32>

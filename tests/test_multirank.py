@@ -41,7 +41,7 @@ def _worker(rank, world, port, results):
 
 def test_two_gloo_ranks_aggregate_like_the_bench():
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.start_processes(_worker, args=(world, port, results), nprocs=world, join=True,
                            start_method="spawn")
