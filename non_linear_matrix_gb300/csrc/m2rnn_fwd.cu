@@ -65,12 +65,15 @@ constexpr int max_consumer_warps() {
 }
 
 // The rank-1 term k v^T from fp32 (k, k) pairs the producer writes and a
-// packed fp32 multiply (fp32 inputs, and V = 32, where the tensor-core form's
-// prefetched products need 32 more registers per thread and measured
-// slower); otherwise from an MMA of two one-column bf16 operands.
-template <int V, bool F32>
+// packed fp32 multiply, or (false) from an MMA of two one-column bf16
+// operands.  Pairs for fp32 inputs; for V = 32, where the tensor-core form's
+// prefetched products need 32 more registers per thread; and for the dense
+// 8-head full-wave launch (GC = 8), where the extra MMAs contend for the
+// tensor pipe (measured 1.496 ms against 1.569 ms for one full wave, while
+// the sparser launches gain from the MMA form).
+template <int V, bool F32, int GC = 0>
 __host__ __device__ constexpr bool rank1_pairs() {
-  return F32 || V != 16;
+  return F32 || V != 16 || GC >= 8;
 }
 
 struct FwdLayout {
@@ -86,7 +89,9 @@ struct FwdLayout {
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 // TC: time steps per ring chunk (<= 32).
-__host__ __device__ inline FwdLayout fwd_layout(int K, int V, int G, int WPH, int es, int TC) {
+// pairs: k also as fp32 (k, k) pairs (rank1_pairs).
+__host__ __device__ inline FwdLayout fwd_layout(int K, int V, int G, int WPH, int es, int TC,
+                                                bool pairs = true) {
   FwdLayout L;
   uint32_t o = 0;
   L.q = o;
@@ -95,8 +100,8 @@ __host__ __device__ inline FwdLayout fwd_layout(int K, int V, int G, int WPH, in
   o = align_up(o + TC * K * es, 128);
   L.v = o;
   o = align_up(o + TC * G * V * es, 128);
-  L.kd = o;  // fp32 pairs of k, except for bf16 inputs at V = 16 (k read raw)
-  o = align_up(o + ((es == 4 || V != 16) ? TC * K * 8 : 0), 128);
+  L.kd = o;  // fp32 pairs of k (otherwise the consumers read k as copied)
+  o = align_up(o + (pairs ? TC * K * 8 : 0), 128);
   L.fd = o;
   o = align_up(o + TC * G * 8, 128);
   L.stage = o;
@@ -147,7 +152,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
 // ---------------------------------------------------------------------------
 // producer warp
 // ---------------------------------------------------------------------------
-template <int V, bool F32, bool GATED>
+template <int V, bool F32, bool GATED, bool PAIRS>
 __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout& L, uint32_t sbase,
                                              int b, int n0, int Geff) {
   using TIn = typename InType<F32>::T;
@@ -232,7 +237,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
     if (!warp_wait(bar_raw_full(bars, s), (ch / NSTAGE) & 1, p.wait_limit_ns)) return false;
     const int Tc = min(TC, T - ch * TC);
     const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
-    const int n8 = rank1_pairs<V, F32>() ? Tc * K / 8 : 0;  // else k is used as copied
+    const int n8 = PAIRS ? Tc * K / 8 : 0;  // else k is used as copied
     for (int i = lane; i < n8; i += 32) {
       float x[8];
       if (F32) {
@@ -473,10 +478,10 @@ struct StepIn {
 
 // kdb: the step's k (fp32 pairs in the fp32 path, raw bf16 otherwise) at
 // this warp's first row; vb: its v (raw) at this head.
-template <int V, int MT, bool F32, bool HALF = false>
+template <int V, int MT, bool F32, bool HALF, bool PAIRS>
 __device__ __forceinline__ void load_step(StepIn<MT, V / 8, F32>& in, uint32_t kdb, uint32_t vb,
                                           int g, int c) {
-  if constexpr (rank1_pairs<V, F32>()) {
+  if constexpr (PAIRS) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       in.k0[mt] = ptx::lds_f32x2(kdb + 8 * (16 * mt + g));
@@ -559,7 +564,7 @@ __host__ __device__ constexpr bool defer_readout() {
 // step's own, or with defer_readout() the previous step's, formed from the
 // bf16(H) operand of this step's H W products before they are used (the last
 // step of a run then needs readout_bf16 afterwards).
-template <int V, int MT, bool F32, bool HALF = false>
+template <int V, int MT, bool F32, bool HALF, bool PAIRS>
 __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V / 8, F32>& in,
                                          uint32_t qb, uint32_t fdaddr, uint32_t ypaddr, int g,
                                          int c) {
@@ -587,7 +592,7 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
   auto products = [&](int mt, float (&acc)[NT][4]) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      if constexpr (rank1_pairs<V, F32>()) {
+      if constexpr (PAIRS) {
         const float2 vv =
             F32 ? in.vf[nt] : make_float2(ptx::bf16x2_lo(in.vb[nt]), ptx::bf16x2_hi(in.vb[nt]));
         const float2 lo = __fmul2_rn(in.k0[mt], vv);
@@ -689,7 +694,7 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
   }  // !DEFER
 }
 
-template <int V, int MT_, bool F32>
+template <int V, int MT_, bool F32, bool PAIRS>
 __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout& L, uint32_t sbase,
                                              int b, int n0, int ci) {
   using TIn = typename InType<F32>::T;
@@ -744,7 +749,7 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
   const int nchunks = (T + TC - 1) / TC;
   // Per-time-step strides of this lane's shared-memory reads.
   const uint32_t q_stride = static_cast<uint32_t>(K * es);
-  const uint32_t kd_stride = static_cast<uint32_t>(rank1_pairs<V, F32>() ? K * 8 : K * 2);
+  const uint32_t kd_stride = static_cast<uint32_t>(PAIRS ? K * 8 : K * 2);
   const uint32_t v_stride = static_cast<uint32_t>(G * V * es);
   const uint32_t fd_stride = static_cast<uint32_t>(G * 8);
   const uint32_t yp_stride = static_cast<uint32_t>(G * WPH * V * 4);
@@ -761,7 +766,7 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
     const int Tc = min(TC, T - t0);
     const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
     const uint32_t qb = st + L.q + static_cast<uint32_t>(row0 * es);
-    const uint32_t kdb = rank1_pairs<V, F32>() ? st + L.kd + static_cast<uint32_t>(row0 * 8)
+    const uint32_t kdb = PAIRS ? st + L.kd + static_cast<uint32_t>(row0 * 8)
                                                : st + L.k + static_cast<uint32_t>(row0 * 2);
     const uint32_t vb = st + L.v + static_cast<uint32_t>(hl * V * es);
     const uint32_t fdb = st + L.fd + static_cast<uint32_t>(hl * 8);
@@ -770,7 +775,7 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
     // The rank-1 inputs of step tl+1 are read while step tl computes.  The
     // read past the chunk's last step (slot Tc <= TC) stays inside this
     // stage's shared memory and its values are never used.
-    load_step<V, MT, F32, HALF>(in0, kdb, vb, g, c);
+    load_step<V, MT, F32, HALF, PAIRS>(in0, kdb, vb, g, c);
     int tl = 0;
     while (tl < Tc) {
       if (t0 + tl == next_ck) {
@@ -788,17 +793,17 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
 #pragma unroll 1
       for (; tl + 1 < seg_end; tl += 2) {
         const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1, u2 = u0 + 2;
-        load_step<V, MT, F32, HALF>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
-        fwd_step<V, MT, F32, HALF>(S, in0, qb + ro(u0) * q_stride, fdb + u0 * fd_stride,
+        load_step<V, MT, F32, HALF, PAIRS>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
+        fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, qb + ro(u0) * q_stride, fdb + u0 * fd_stride,
                              yb + ro(u0) * yp_stride, g, c);
-        load_step<V, MT, F32, HALF>(in0, kdb + u2 * kd_stride, vb + u2 * v_stride, g, c);
-        fwd_step<V, MT, F32, HALF>(S, in1, qb + ro(u1) * q_stride, fdb + u1 * fd_stride,
+        load_step<V, MT, F32, HALF, PAIRS>(in0, kdb + u2 * kd_stride, vb + u2 * v_stride, g, c);
+        fwd_step<V, MT, F32, HALF, PAIRS>(S, in1, qb + ro(u1) * q_stride, fdb + u1 * fd_stride,
                              yb + ro(u1) * yp_stride, g, c);
       }
       if (tl < seg_end) {  // odd remainder of the segment
         const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1;
-        load_step<V, MT, F32, HALF>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
-        fwd_step<V, MT, F32, HALF>(S, in0, qb + ro(u0) * q_stride, fdb + u0 * fd_stride,
+        load_step<V, MT, F32, HALF, PAIRS>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
+        fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, qb + ro(u0) * q_stride, fdb + u0 * fd_stride,
                              yb + ro(u0) * yp_stride, g, c);
         in0 = in1;
         ++tl;
@@ -840,7 +845,8 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
   const int n0 = (blockIdx.x % p.ngroups) * p.G;
   const int Geff = min(p.G, p.N - n0);
   const int ncons = Geff * p.WPH;
-  const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, sizeof(TIn), p.tc);
+  constexpr bool PAIRS = rank1_pairs<V, F32, GC>();
+  const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, sizeof(TIn), p.tc, PAIRS);
   const uint32_t sbase = ptx::smem_addr(smem);
   const uint32_t bars = sbase + L.bars;
   if (threadIdx.x == 0) {
@@ -859,34 +865,48 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
   if (warp == 0) {
     // With fault injection on, the producer issues nothing, so every wait of
     // the other warps runs into its time limit (tests of the time-out path).
-    if (p.inject_stall == 0) fwd_producer<V, F32, GATED>(p, L, sbase, b, n0, Geff);
+    if (p.inject_stall == 0) fwd_producer<V, F32, GATED, PAIRS>(p, L, sbase, b, n0, Geff);
   } else if (warp == 1) {
     fwd_epilogue<V, F32, NORM>(p, L, sbase, b, n0, Geff);
   } else if (warp - 2 < ncons) {
-    fwd_consumer<V, MT, F32>(p, L, sbase, b, n0, warp - 2);
+    fwd_consumer<V, MT, F32, PAIRS>(p, L, sbase, b, n0, warp - 2);
   }
 }
 
-// The kernel instance for p's fused parts (gate, readout epilogue).
+// The kernel instance for p (fused gate, readout epilogue, compile-time K
+// and heads per CTA), with the rank1_pairs choice it was compiled with (the
+// launch's shared-memory layout depends on it).
 template <int V, int MT, bool F32>
-auto select_kernel(const FwdParams& p) {
+struct Selected {
+  decltype(&fwd_kernel<V, MT, F32, false, false>) kern;
+  bool pairs;
+};
+
+template <int V, int MT, bool F32>
+Selected<V, MT, F32> select_kernel(const FwdParams& p) {
   // the instances with compile-time K and G (the K = 64 launches of large
   // batches; a G = 1, MT = 1 instance measured slower than the generic one)
   if constexpr (V == 16 && MT == 2 && !F32) {
     if (!p.norm && !p.gated && p.K == 64 && p.WPH == 2) {
-      if (p.G == 8) return fwd_kernel<16, 2, false, false, false, 64, 8>;
-      if (p.G == 2) return fwd_kernel<16, 2, false, false, false, 64, 2>;
+      if (p.G == 8)
+        return {fwd_kernel<16, 2, false, false, false, 64, 8>, rank1_pairs<16, false, 8>()};
+      if (p.G == 2)
+        return {fwd_kernel<16, 2, false, false, false, 64, 2>, rank1_pairs<16, false, 2>()};
     }
   }
+  constexpr bool pairs = rank1_pairs<V, F32>();
   if (p.norm)
-    return p.gated ? fwd_kernel<V, MT, F32, true, true> : fwd_kernel<V, MT, F32, false, true>;
-  return p.gated ? fwd_kernel<V, MT, F32, true, false> : fwd_kernel<V, MT, F32, false, false>;
+    return {p.gated ? fwd_kernel<V, MT, F32, true, true> : fwd_kernel<V, MT, F32, false, true>,
+            pairs};
+  return {p.gated ? fwd_kernel<V, MT, F32, true, false> : fwd_kernel<V, MT, F32, false, false>,
+          pairs};
 }
 
 template <int V, int MT, bool F32>
 int ctas_per_sm_t(const FwdParams& p) {
-  const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc);
-  auto kern = select_kernel<V, MT, F32>(p);
+  const auto sel = select_kernel<V, MT, F32>(p);
+  const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc, sel.pairs);
+  auto kern = sel.kern;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(L.total)) != cudaSuccess)
     return 0;
@@ -899,10 +919,11 @@ int ctas_per_sm_t(const FwdParams& p) {
 
 template <int V, int MT, bool F32>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
-  const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc);
+  const auto sel = select_kernel<V, MT, F32>(p);
+  const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc, sel.pairs);
   if (p.tc < 2 || p.tc > 32) return cudaErrorInvalidValue;
   if (p.G * p.WPH > max_consumer_warps<V, MT, F32>()) return cudaErrorInvalidConfiguration;
-  auto kern = select_kernel<V, MT, F32>(p);
+  auto kern = sel.kern;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(L.total));
   if (e != cudaSuccess) return e;
@@ -913,8 +934,9 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+// (with k's fp32 pairs: an upper bound for the planner)
 size_t fwd_smem_bytes(int K, int V, int G, int WPH, bool f32_inputs, int tc) {
-  return fwd_layout(K, V, G, WPH, f32_inputs ? 4 : 2, tc).total;
+  return fwd_layout(K, V, G, WPH, f32_inputs ? 4 : 2, tc, true).total;
 }
 
 int fwd_max_consumer_warps(int V, int MT, bool f32_inputs) {
