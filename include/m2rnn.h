@@ -280,6 +280,15 @@ int m2rnn_decode(const m2rnn_shape *s, const void *q, const void *k, const void 
                  const void *f, const void *W, const void *w_r, const float *H_in,
                  float *H_out, void *y, void *stream);
 
+/* Single-step decode with the fused input gate of Eq. (13): as m2rnn_decode,
+ * with f = exp(-alpha softplus(a + beta)) computed in the kernel from
+ * a [B,N] (in_dtype) and alpha, beta [N] (in_dtype) instead of f.  T such
+ * calls reproduce m2rnn_fwd_gated's H_T for the same inputs bit for bit. */
+int m2rnn_decode_gated(const m2rnn_shape *s, const void *q, const void *k, const void *v,
+                       const void *a, const void *alpha, const void *beta, const void *W,
+                       const void *w_r, const float *H_in, float *H_out, void *y,
+                       void *stream);
+
 /* Test hook for the time-out path.  mode 1: kernels launched afterwards
  * from this process start no input transfers, so every internal wait runs
  * into the wait limit, the kernel stops early (outputs unspecified) and

@@ -383,6 +383,53 @@ bool choose_bwd(m2rnn::BwdParams& p, int V, bool f32, int sms) {
   return true;
 }
 
+// Decode entry: validation, then the decode kernel.  gate = NULL: f is given.
+int decode_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
+                const Gate* gate, const void* W, const void* w_r, const float* H_in, float* H_out,
+                void* y, void* stream) {
+  int rc = check_shape(s);
+  if (rc != M2RNN_OK) return rc;
+  if (s->T != 1) return M2RNN_ERR_INVALID_ARG;
+  int dev, sms;
+  int* status;
+  rc = device_info(&dev, &status, &sms);
+  if (rc != M2RNN_OK) return rc;
+  const void* req[] = {q, k, v, gate ? gate->a : f, W, w_r, H_in, H_out, y};
+  for (const void* p : req)
+    if ((rc = check_ptr(p, dev, true)) != M2RNN_OK) return rc;
+  if (gate != nullptr) {
+    if ((rc = check_ptr(gate->alpha, dev, true)) != M2RNN_OK) return rc;
+    if ((rc = check_ptr(gate->beta, dev, true)) != M2RNN_OK) return rc;
+  }
+  if (H_out != H_in) {  // distinct state buffers must not overlap
+    const size_t bytes = static_cast<size_t>(s->B) * s->N * s->K * s->V * sizeof(float);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(H_in), b = reinterpret_cast<uintptr_t>(H_out);
+    if (a < b + bytes && b < a + bytes) return M2RNN_ERR_INVALID_ARG;
+  }
+  m2rnn::DecodeParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.f = f;
+  p.W = W;
+  p.w_r = w_r;
+  p.H_in = H_in;
+  p.H_out = H_out;
+  p.y = y;
+  p.B = s->B;
+  p.N = s->N;
+  p.K = s->K;
+  p.Nq = groups(s);
+  if (gate != nullptr) {
+    p.a = gate->a;
+    p.alpha = gate->alpha;
+    p.beta = gate->beta;
+    p.gated = 1;
+  }
+  return status_from_cuda(m2rnn::launch_decode(p, s->V, s->in_dtype == M2RNN_F32,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -438,37 +485,14 @@ int m2rnn_device_status(int* status, int* detail, int clear, void* stream) {
 int m2rnn_decode(const m2rnn_shape* s, const void* q, const void* k, const void* v, const void* f,
                  const void* W, const void* w_r, const float* H_in, float* H_out, void* y,
                  void* stream) {
-  int rc = check_shape(s);
-  if (rc != M2RNN_OK) return rc;
-  if (s->T != 1) return M2RNN_ERR_INVALID_ARG;
-  int dev, sms;
-  int* status;
-  rc = device_info(&dev, &status, &sms);
-  if (rc != M2RNN_OK) return rc;
-  const void* req[] = {q, k, v, f, W, w_r, H_in, H_out, y};
-  for (const void* p : req)
-    if ((rc = check_ptr(p, dev, true)) != M2RNN_OK) return rc;
-  if (H_out != H_in) {  // distinct state buffers must not overlap
-    const size_t bytes = static_cast<size_t>(s->B) * s->N * s->K * s->V * sizeof(float);
-    const uintptr_t a = reinterpret_cast<uintptr_t>(H_in), b = reinterpret_cast<uintptr_t>(H_out);
-    if (a < b + bytes && b < a + bytes) return M2RNN_ERR_INVALID_ARG;
-  }
-  m2rnn::DecodeParams p;
-  p.q = q;
-  p.k = k;
-  p.v = v;
-  p.f = f;
-  p.W = W;
-  p.w_r = w_r;
-  p.H_in = H_in;
-  p.H_out = H_out;
-  p.y = y;
-  p.B = s->B;
-  p.N = s->N;
-  p.K = s->K;
-  p.Nq = groups(s);
-  return status_from_cuda(m2rnn::launch_decode(p, s->V, s->in_dtype == M2RNN_F32,
-                                               static_cast<cudaStream_t>(stream)));
+  return decode_impl(s, q, k, v, f, nullptr, W, w_r, H_in, H_out, y, stream);
+}
+
+int m2rnn_decode_gated(const m2rnn_shape* s, const void* q, const void* k, const void* v,
+                       const void* a, const void* alpha, const void* beta, const void* W,
+                       const void* w_r, const float* H_in, float* H_out, void* y, void* stream) {
+  const Gate gate{a, alpha, beta};
+  return decode_impl(s, q, k, v, nullptr, &gate, W, w_r, H_in, H_out, y, stream);
 }
 
 }  // extern "C"

@@ -24,6 +24,7 @@
 
 #include "m2rnn.h"
 #include "m2rnn_internal.h"
+#include "m2rnn_gate.cuh"
 #include "ptx.cuh"
 
 namespace m2rnn {
@@ -100,7 +101,12 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
     vv[nt] = make_float2(dtof(v[8 * nt + 2 * c]), dtof(v[8 * nt + 2 * c + 1]));
-  const float fg = dtof(static_cast<const TIn*>(p.f)[head]);
+  // f, or with the fused input gate exp(-alpha softplus(a + beta)) (the
+  // forward kernel's function, so decode steps stay bitwise equal to it)
+  const float fg = p.gated ? gate_f(dtof(static_cast<const TIn*>(p.a)[head]),
+                                    dtof(static_cast<const TIn*>(p.alpha)[n]),
+                                    dtof(static_cast<const TIn*>(p.beta)[n]))
+                           : dtof(static_cast<const TIn*>(p.f)[head]);
   const float2 f2 = make_float2(fg, fg), m1 = make_float2(-1.f, -1.f);
 
   float ypart[NT][2];

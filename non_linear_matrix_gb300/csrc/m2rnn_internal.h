@@ -117,6 +117,11 @@ struct DecodeParams {
   void* y;            // [B,N,V]
   int B, N, K;
   int Nq = 1;         // query/key groups (q, k are [B,Nq,K])
+  // fused input gate (gated = 1): f from a [B,N] and alpha, beta [N]
+  const void* a = nullptr;
+  const void* alpha = nullptr;
+  const void* beta = nullptr;
+  int gated = 0;
 };
 cudaError_t launch_decode(const DecodeParams& p, int V, bool f32_inputs, cudaStream_t stream);
 

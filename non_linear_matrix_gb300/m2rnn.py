@@ -40,6 +40,7 @@ _EXPORTS = {
     "m2rnn_set_fault_injection": (ctypes.c_int, [ctypes.c_int]),
     "m2rnn_bwd_noalloc": (ctypes.c_int, [_VP] * 18),
     "m2rnn_decode": (ctypes.c_int, [_VP] * 11),
+    "m2rnn_decode_gated": (ctypes.c_int, [_VP] * 13),
     "m2rnn_fwd_gated": (ctypes.c_int, [_VP] * 14),
     "m2rnn_bwd_gated": (ctypes.c_int, [_VP] * 24 + [ctypes.c_size_t, _VP]),
     "m2rnn_fwd_norm": (ctypes.c_int, [_VP] * 13 + [ctypes.c_float] + [_VP] * 6),
@@ -203,6 +204,29 @@ def decode(q, k, v, f, W, w_r, H, *, H_out=None, y=None, stream=None):
     rc = lib().m2rnn_decode(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(f), _ptr(W),
                             _ptr(w_r), _ptr(H), _ptr(H_out), _ptr(y), _stream(stream))
     _check(rc, "m2rnn_decode")
+    return y, H_out
+
+
+def decode_gated(q, k, v, a, alpha, beta, W, w_r, H, *, H_out=None, y=None, stream=None):
+    """One decode step with the fused input gate: a [B,N], alpha and beta
+    [N] replace f; otherwise as ``decode``.  Returns (y, H_out)."""
+    if q.dim() == 3:
+        B, Nq, K = q.shape
+    else:
+        (B, K), Nq = q.shape, 1
+    N, V = v.shape[1], v.shape[2]
+    for t in (k, v, a, alpha, beta, W, w_r):
+        if t.dtype != q.dtype:
+            raise TypeError("q, k, v, a, alpha, beta, W, w_r must share one dtype")
+    s = Shape(B, 1, N, K, V, _dtype_code(q), 0, Nq)
+    if H_out is None:
+        H_out = torch.empty_like(H)
+    if y is None:
+        y = torch.empty_like(v)
+    rc = lib().m2rnn_decode_gated(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(alpha),
+                                  _ptr(beta), _ptr(W), _ptr(w_r), _ptr(H), _ptr(H_out), _ptr(y),
+                                  _stream(stream))
+    _check(rc, "m2rnn_decode_gated")
     return y, H_out
 
 

@@ -125,3 +125,30 @@ def test_decode_grouped_qk(m2rnn, oracle_mod, Nq):
     B, N, K, V = 4, 6, 64, 16
     x = make_inputs(B, 1, N, K, V, "bf16", 950 + Nq, groups=Nq)
     _compare_oracle(m2rnn, oracle_mod, _one_step(x), _state(B, N, K, V, Nq), "bf16")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_gated(m2rnn, oracle_mod, dtype):
+    """The fused gate in decode: one step against the oracle's gated forward
+    at T = 1, and T steps against m2rnn_fwd_gated's H_T bit for bit."""
+    B, T, N, K, V = 3, 12, 4, 64, 16
+    x = make_inputs(B, T, N, K, V, dtype, 971, gated=True)
+    H0 = _state(B, N, K, V, 19)
+    g = {n: t.cuda() for n, t in x.items()}
+    y1, H1 = m2rnn.decode_gated(g["q"][:, 0].contiguous(), g["k"][:, 0].contiguous(),
+                                g["v"][:, 0].contiguous(), g["a"][:, 0].contiguous(), g["alpha"],
+                                g["beta"], g["W"], g["w_r"], H0.cuda())
+    torch.cuda.synchronize()
+    ref = oracle_mod.fwd_gated(x["q"][:, :1], x["k"][:, :1], x["v"][:, :1], x["a"][:, :1],
+                               x["alpha"], x["beta"], x["W"], x["w_r"], H0=H0)
+    assert np.abs(y1.float().cpu().numpy() - ref["y"][:, 0]).max() <= TOL[dtype]
+    assert np.abs(H1.cpu().double().numpy() - ref["HT"]).max() <= TOL[dtype]
+    _, HT, _ = m2rnn.fwd_gated(g["q"], g["k"], g["v"], g["a"], g["alpha"], g["beta"], g["W"],
+                               g["w_r"], H0.cuda())
+    H = H0.cuda()
+    for t in range(T):
+        _, H = m2rnn.decode_gated(g["q"][:, t].contiguous(), g["k"][:, t].contiguous(),
+                                  g["v"][:, t].contiguous(), g["a"][:, t].contiguous(),
+                                  g["alpha"], g["beta"], g["W"], g["w_r"], H, H_out=H)
+    torch.cuda.synchronize()
+    assert torch.equal(H, HT)
