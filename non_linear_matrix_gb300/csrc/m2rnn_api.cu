@@ -226,7 +226,7 @@ m2rnn::FwdParams offset_batch(const m2rnn::FwdParams& p, int b0, const m2rnn_sha
   r.v = static_cast<const char*>(p.v) + B0 * T * N * V * es;
   if (p.f) r.f = static_cast<const char*>(p.f) + B0 * T * N * es;
   if (p.a) r.a = static_cast<const char*>(p.a) + B0 * T * N * es;
-  r.y = static_cast<char*>(p.y) + B0 * T * N * V * es;
+  if (p.y) r.y = static_cast<char*>(p.y) + B0 * T * N * V * es;  // NULL: checkpoint-only run
   if (p.H0) r.H0 = p.H0 + B0 * N * K * V;
   if (p.HT) r.HT = p.HT + B0 * N * K * V;
   if (p.ckpt) r.ckpt = p.ckpt + B0 * N * static_cast<size_t>(p.nck) * K * V;
