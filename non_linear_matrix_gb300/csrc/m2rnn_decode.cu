@@ -45,7 +45,7 @@ __device__ __forceinline__ float dtof(__nv_bfloat16 x) { return __bfloat162float
 __device__ __forceinline__ void dstore(float* p, float x) { *p = x; }
 __device__ __forceinline__ void dstore(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-template <int V, bool F32, int MT>
+template <int V, bool F32, int MT, bool GATED>
 __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
   using TIn = typename DecIn<F32>::T;
   constexpr int NT = V / 8, KS = V / 16;
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
     vv[nt] = make_float2(dtof(v[8 * nt + 2 * c]), dtof(v[8 * nt + 2 * c + 1]));
   // f, or with the fused input gate exp(-alpha softplus(a + beta)) (the
   // forward kernel's function, so decode steps stay bitwise equal to it)
-  const float fg = p.gated ? gate_f(dtof(static_cast<const TIn*>(p.a)[head]),
+  const float fg = GATED ? gate_f(dtof(static_cast<const TIn*>(p.a)[head]),
                                     dtof(static_cast<const TIn*>(p.alpha)[n]),
                                     dtof(static_cast<const TIn*>(p.beta)[n]))
                            : dtof(static_cast<const TIn*>(p.f)[head]);
@@ -194,14 +194,19 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
   }
 }
 
-template <int V, bool F32>
-cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
+template <int V, bool F32, bool GATED>
+cudaError_t launch_decode_g(const DecodeParams& p, cudaStream_t stream) {
   const size_t heads = static_cast<size_t>(p.B) * p.N;
   if (p.K >= 32)  // two 16-row tiles per warp: twice the state bytes in flight per warp
-    decode_kernel<V, F32, 2><<<static_cast<unsigned>(heads), 32 * (p.K / 32), 0, stream>>>(p);
+    decode_kernel<V, F32, 2, GATED><<<static_cast<unsigned>(heads), 32 * (p.K / 32), 0, stream>>>(p);
   else
-    decode_kernel<V, F32, 1><<<static_cast<unsigned>(heads), 32 * (p.K / 16), 0, stream>>>(p);
+    decode_kernel<V, F32, 1, GATED><<<static_cast<unsigned>(heads), 32 * (p.K / 16), 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int V, bool F32>
+cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
+  return p.gated ? launch_decode_g<V, F32, true>(p, stream) : launch_decode_g<V, F32, false>(p, stream);
 }
 
 }  // namespace

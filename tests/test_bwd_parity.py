@@ -159,6 +159,15 @@ def test_checkpoints_recomputed(m2rnn, oracle_mod, C):
         _restart_parity(m2rnn, oracle_mod, x, C, give_ckpt=True, label=f"given C{C}")
 
 
+def test_checkpoints_recomputed_split_forward(m2rnn, oracle_mod):
+    """ckpt = NULL at a batch (41 items x 32 heads) that the forward splits
+    into a whole-wave launch and a tail launch; the recompute writes no y.
+    Grouped q/k (4 groups); at this many (b, n) pairs the serial kernel
+    with one warp per CTA is the automatic choice."""
+    x = make_inputs(41, 40, 32, 64, 16, "bf16", 4141, with_dy=True, groups=4)
+    _restart_parity(m2rnn, oracle_mod, x, 16, give_ckpt=False, label="recompute split")
+
+
 def test_restart_parity_with_H0_dHT(m2rnn, oracle_mod):
     """Interval parity with a ragged last interval, H0 and dH_T."""
     B, T, N = 2, 700, 5
@@ -235,6 +244,22 @@ def test_pipelined_warps_per_cta(m2rnn, oracle_mod, monkeypatch, wpc, dtype):
     H0 = torch.rand(2, 3, 64, 16, generator=gen) - 0.5
     dHT = torch.randn(2, 3, 64, 16, generator=gen)
     _restart_parity(m2rnn, oracle_mod, x, 32, H0=H0, dHT=dHT, label=f"wpc{wpc} {dtype}")
+
+
+@pytest.mark.parametrize("wpc,dtype,V", [("1", "bf16", 16), ("2", "bf16", 16), ("1", "f32", 16),
+                                          ("2", "f32", 16), ("1", "bf16", 32), ("2", "f32", 32)])
+def test_serial_warps_per_cta(m2rnn, oracle_mod, monkeypatch, wpc, dtype, V):
+    """The serial kernel with 1 and 2 warps per CTA (4 or 2 row slices per
+    head, cross-slice atomic sums of dv and df).  The automatic choice takes
+    it at large batches, where it fits more CTAs per SM than the pipelined
+    kernel; here it is forced on the same inputs as the pipelined test."""
+    monkeypatch.setenv("M2RNN_BWD_KERNEL", "0")
+    monkeypatch.setenv("M2RNN_BWD_WPC", wpc)
+    x = make_inputs(2, 150, 3, 64, V, dtype, 600, with_dy=True)
+    gen = torch.Generator().manual_seed(11)
+    H0 = torch.rand(2, 3, 64, V, generator=gen) - 0.5
+    dHT = torch.randn(2, 3, 64, V, generator=gen)
+    _restart_parity(m2rnn, oracle_mod, x, 32, H0=H0, dHT=dHT, label=f"serial wpc{wpc} {dtype} V{V}")
 
 
 @pytest.mark.parametrize("kernel", ["0", "1"])
