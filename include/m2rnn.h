@@ -74,7 +74,9 @@ typedef enum {
     M2RNN_ERR_POINTER = -4,           /* a pointer is not device memory of the current device */
     M2RNN_ERR_WORKSPACE = -5,         /* workspace missing or smaller than required */
     M2RNN_ERR_CUDA = -6,              /* a CUDA runtime call or launch failed */
-    M2RNN_ERR_TIMEOUT = -7            /* a kernel wait exceeded its limit (device status) */
+    M2RNN_ERR_TIMEOUT = -7,           /* a kernel wait exceeded its limit (device status) */
+    M2RNN_ERR_BOUNDS = -8             /* checked build only: a kernel computed an index outside
+                                         its array and skipped the access (device status) */
 } m2rnn_status;
 
 typedef enum {
@@ -91,7 +93,15 @@ typedef struct {
 } m2rnn_shape;
 
 /* Library version (major*10000 + minor*100 + patch). */
-int m2rnn_version(void);  /* 200 and later: m2rnn_shape carries Nq */
+int m2rnn_version(void);  /* 200 and later: m2rnn_shape carries Nq; 201: M2RNN_ERR_BOUNDS */
+
+/* 1 for the checked build (libm2rnn_check.so), 0 for the normal one.  The
+ * checked build compiles the same kernels with an index check in front of
+ * every global-memory access whose index a kernel computes: an index outside
+ * the extent that the call's shape gives its array records M2RNN_ERR_BOUNDS
+ * and the location code of the access in the device status word, and the
+ * access is skipped (no trap).  The normal build has no such checks. */
+int m2rnn_checked(void);
 
 /* Human-readable text for a status code; never NULL. */
 const char *m2rnn_status_string(int status);
@@ -214,10 +224,11 @@ int m2rnn_bwd_norm(const m2rnn_shape *s, const void *q, const void *k, const voi
                    void *stream);
 
 /* Reads (after synchronising `stream`) and optionally clears the device
- * status word of the current device.  *status receives M2RNN_OK or the code
- * a kernel recorded (M2RNN_ERR_TIMEOUT); *detail receives the location code
- * of the wait that gave up (may be NULL).  Returns M2RNN_OK or
- * M2RNN_ERR_CUDA. */
+ * status word of the current device.  *status receives M2RNN_OK or the
+ * first code a kernel recorded (M2RNN_ERR_TIMEOUT, or in the checked build
+ * M2RNN_ERR_BOUNDS); *detail receives the location code of the wait that
+ * gave up or of the access that was skipped (may be NULL).  Returns
+ * M2RNN_OK or M2RNN_ERR_CUDA. */
 int m2rnn_device_status(int *status, int *detail, int clear, void *stream);
 
 /* Sets the time limit, in nanoseconds, of every internal wait of kernels

@@ -3,6 +3,12 @@
 Each translation unit is compiled in parallel into ``_build/`` and linked
 into ``_build/libm2rnn.so``; the CUDA runtime is linked statically so the
 library has no run-time dependency beyond the driver.
+
+``build(checked=True)`` (``python -m non_linear_matrix_gb300.build checked``)
+compiles the same sources with ``-DM2RNN_CHECK=1`` into
+``_build/check/libm2rnn_check.so``: every computed global-memory index is
+tested against its array's extent and a violation is reported through the
+device status word (M2RNN_ERR_BOUNDS) instead of being performed.
 """
 from __future__ import annotations
 
@@ -16,6 +22,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libm2rnn.so")
+BUILD_CHECKED = os.path.join(BUILD, "check")
+LIB_CHECKED = os.path.join(BUILD_CHECKED, "libm2rnn_check.so")
 MICROBENCH = os.path.join(BUILD, "m2rnn_microbench")
 
 SOURCES = ["m2rnn_api.cu", "m2rnn_fwd.cu", "m2rnn_bwd.cu", "m2rnn_bwd_pipe.cu", "m2rnn_decode.cu",
@@ -36,18 +44,21 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libm2rnn.so; returns its path.  Raises on failure."""
-    os.makedirs(BUILD, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile and link libm2rnn.so (or, checked=True, libm2rnn_check.so);
+    returns its path.  Raises on failure."""
+    out_dir, lib = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    defs = ["-DM2RNN_CHECK=1"] if checked else []
+    os.makedirs(out_dir, exist_ok=True)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime():
+        return lib
     nvcc = _nvcc()
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         objs.append(obj)
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *ARCH, *FLAGS, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.append("-Xptxas=-v")
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -60,10 +71,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
             failed.append(" ".join(cmd))
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 def build_microbench() -> str:
@@ -77,5 +88,7 @@ def build_microbench() -> str:
 if __name__ == "__main__":
     if len(sys.argv) > 1 and sys.argv[1] == "microbench":
         print(build_microbench())
+    elif len(sys.argv) > 1 and sys.argv[1] == "checked":
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked=True))
     else:
         print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

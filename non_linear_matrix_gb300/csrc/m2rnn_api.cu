@@ -12,6 +12,7 @@
 
 #include "m2rnn.h"
 #include "m2rnn_internal.h"
+#include "m2rnn_check.cuh"
 
 namespace m2rnn {
 int fwd_max_consumer_warps(int V, int MT, bool f32_inputs);
@@ -420,6 +421,7 @@ int decode_impl(const m2rnn_shape* s, const void* q, const void* k, const void* 
   p.N = s->N;
   p.K = s->K;
   p.Nq = groups(s);
+  p.status = status;
   if (gate != nullptr) {
     p.a = gate->a;
     p.alpha = gate->alpha;
@@ -434,7 +436,9 @@ int decode_impl(const m2rnn_shape* s, const void* q, const void* k, const void* 
 
 extern "C" {
 
-int m2rnn_version(void) { return 200; }
+int m2rnn_version(void) { return 201; }
+
+int m2rnn_checked(void) { return M2RNN_CHECK ? 1 : 0; }
 
 const char* m2rnn_status_string(int status) {
   switch (status) {
@@ -446,6 +450,7 @@ const char* m2rnn_status_string(int status) {
     case M2RNN_ERR_WORKSPACE: return "workspace missing or too small";
     case M2RNN_ERR_CUDA: return "CUDA runtime error";
     case M2RNN_ERR_TIMEOUT: return "a kernel wait exceeded its time limit";
+    case M2RNN_ERR_BOUNDS: return "a kernel index was outside its array (checked build; access skipped)";
     default: return "unknown status";
   }
 }
@@ -555,6 +560,7 @@ int fwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, 
   np.dy = nullptr;
   np.dg = nullptr;
   np.dw = nullptr;
+  np.status = status;
   return status_from_cuda(m2rnn::launch_norm_fwd(np, s->in_dtype == M2RNN_F32, sms, st));
 }
 
@@ -623,6 +629,7 @@ int bwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, 
     np.dy = workspace;
     np.dg = nb->dg;
     np.dw = nb->dw;
+    np.status = status;
     if (m2rnn::launch_norm_bwd(np, f32, sms, st) != cudaSuccess) return M2RNN_ERR_CUDA;
     dy = workspace;
     workspace = static_cast<char*>(workspace) + dy_bytes;
@@ -666,6 +673,7 @@ int bwd_impl(const m2rnn_shape* s, const void* q, const void* k, const void* v, 
   p.dw_r = dw_r;
   p.dH0 = dH0;
   p.dckpt = dckpt;
+  p.status = status;
   if (gate != nullptr) {
     p.a = gate->a;
     p.alpha = gate->alpha;

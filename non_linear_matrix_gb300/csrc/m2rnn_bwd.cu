@@ -46,6 +46,7 @@
 #include "ptx.cuh"
 #include "m2rnn_bwd_common.cuh"
 #include "m2rnn_gate.cuh"
+#include "m2rnn_check.cuh"
 
 namespace m2rnn {
 namespace {
@@ -130,8 +131,13 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
   // f, or with the fused input gate its input a (same layout and dtype)
   constexpr bool gated = GATED;
   const TIn* fin = static_cast<const TIn*>(gated ? p.a : p.f);
-  const float g_alpha = gated ? tof(static_cast<const TIn*>(p.alpha)[n]) : 0.f;
-  const float g_beta = gated ? tof(static_cast<const TIn*>(p.beta)[n]) : 0.f;
+  // array extents in elements (index checks of the checked build)
+  const size_t BT = static_cast<size_t>(p.B) * T;
+  const size_t qk_ext = BT * Nq * K, v_ext = BT * N * V, f_ext = BT * N;
+  const size_t s_ext = static_cast<size_t>(p.B) * N * K * V;  // dH_T, dH0
+  const bool n_ok = in_range(p.status, n, 1, N, CHK_BWD_PARAM);
+  const float g_alpha = gated && n_ok ? tof(static_cast<const TIn*>(p.alpha)[n]) : 0.f;
+  const float g_beta = gated && n_ok ? tof(static_cast<const TIn*>(p.beta)[n]) : 0.f;
   float dalpha_acc = 0.f, dbeta_acc = 0.f;  // gate parameter sums of this thread's steps
   const TIn* dy = static_cast<const TIn*>(p.dy);
   const TIn* Wn = static_cast<const TIn*>(p.W) + static_cast<size_t>(n) * V * V;
@@ -146,12 +152,12 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int kk = 16 * ks + 8 * h + 2 * c, nn = 8 * nt + g;
-        const float w0 = tof(Wn[kk * V + nn]), w1 = tof(Wn[(kk + 1) * V + nn]);
+        const float w0 = n_ok ? tof(Wn[kk * V + nn]) : 0.f, w1 = n_ok ? tof(Wn[(kk + 1) * V + nn]) : 0.f;
         Bw[ks][nt][h] = ptx::pack_bf16x2(w0, w1);
         Bwl[ks][nt][h] = F32 ? ptx::pack_bf16x2(w0 - ptx::bf16x2_lo(Bw[ks][nt][h]),
                                                 w1 - ptx::bf16x2_hi(Bw[ks][nt][h]))
                              : 0u;
-        const float t0 = tof(Wn[nn * V + kk]), t1 = tof(Wn[nn * V + kk + 1]);
+        const float t0 = n_ok ? tof(Wn[nn * V + kk]) : 0.f, t1 = n_ok ? tof(Wn[nn * V + kk + 1]) : 0.f;
         Bt[ks][nt][h] = ptx::pack_bf16x2(t0, t1);
         Btl[ks][nt][h] = F32 ? ptx::pack_bf16x2(t0 - ptx::bf16x2_lo(Bt[ks][nt][h]),
                                                 t1 - ptx::bf16x2_hi(Bt[ks][nt][h]))
@@ -166,7 +172,8 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int row = row0 + g + 8 * (r >> 1), col = 8 * nt + 2 * c + (r & 1);
-      Cg[nt][r] = p.dHT ? p.dHT[sidx + row * V + col] : 0.f;
+      const size_t o = sidx + row * V + col;
+      Cg[nt][r] = p.dHT && in_range(p.status, o, 1, s_ext, CHK_BWD_DHT) ? p.dHT[o] : 0.f;
     }
   float dW[KS][NT][4];
 #pragma unroll
@@ -200,13 +207,17 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
     const int qv = RS * es / 16;  // 16-byte vectors per step
     for (int e = tid; e < Lc * qv; e += nthr) {
       const int s = e / qv, x = e - s * qv;
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(q + ((bt0 + s) * Nq + gq) * K + row0c) + x);
+      const size_t so = ((bt0 + s) * Nq + gq) * K + row0c;
+      if (!in_range(p.status, so + x * (16 / es), 16 / es, qk_ext, CHK_BWD_IN)) continue;
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(q + so) + x);
       sts_u32x4(sb + L.in_q + static_cast<uint32_t>(s * RS * es + 16 * x), a.x, a.y, a.z, a.w);
     }
     const int vvn = V * es / 16;
     for (int e = tid; e < Lc * vvn; e += nthr) {
       const int s = e / vvn, x = e - s * vvn;
-      const uint4 d = __ldg(reinterpret_cast<const uint4*>(dy + ((bt0 + s) * N + n) * V) + x);
+      const size_t so = ((bt0 + s) * N + n) * V;
+      if (!in_range(p.status, so + x * (16 / es), 16 / es, v_ext, CHK_BWD_IN)) continue;
+      const uint4 d = __ldg(reinterpret_cast<const uint4*>(dy + so) + x);
       sts_u32x4(sb + L.in_dy + static_cast<uint32_t>(s * V * es + 16 * x), d.x, d.y, d.z, d.w);
     }
   };
@@ -216,28 +227,37 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
     const int qv = RS * es / 16;
     for (int e = tid; e < Lc * qv; e += nthr) {
       const int s = e / qv, x = e - s * qv;
-      const uint4 d = __ldg(reinterpret_cast<const uint4*>(kin + ((bt0 + s) * Nq + gq) * K + row0c) + x);
+      const size_t so = ((bt0 + s) * Nq + gq) * K + row0c;
+      if (!in_range(p.status, so + x * (16 / es), 16 / es, qk_ext, CHK_BWD_IN)) continue;
+      const uint4 d = __ldg(reinterpret_cast<const uint4*>(kin + so) + x);
       sts_u32x4(kb + static_cast<uint32_t>(s * RS * es + 16 * x), d.x, d.y, d.z, d.w);
     }
     const int vvn = V * es / 16;
     for (int e = tid; e < Lc * vvn; e += nthr) {
       const int s = e / vvn, x = e - s * vvn;
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(vin + ((bt0 + s) * N + n) * V) + x);
+      const size_t so = ((bt0 + s) * N + n) * V;
+      if (!in_range(p.status, so + x * (16 / es), 16 / es, v_ext, CHK_BWD_IN)) continue;
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(vin + so) + x);
       sts_u32x4(vb + static_cast<uint32_t>(s * V * es + 16 * x), a.x, a.y, a.z, a.w);
     }
     for (int s = tid; s < Lc; s += nthr) {
+      if (!in_range(p.status, (bt0 + s) * N + n, 1, f_ext, CHK_BWD_IN)) continue;
       const float x = tof(fin[(bt0 + s) * N + n]);
       ptx::sts_f32(sb + L.in_f + buf * L.fbuf + 4 * s, gated ? gate_f(x, g_alpha, g_beta) : x);
     }
   };
   // checkpoint H_{ci C} of this thread's elements
   auto load_ckpt = [&](int ci, float (&H)[NT][4]) {
-    const float* ck = p.ckpt + ((static_cast<size_t>(b) * N + n) * p.nck + ci) * K * V;
+    const size_t ck0 = ((static_cast<size_t>(b) * N + n) * p.nck + ci) * K * V;
+    const float* ck = p.ckpt + ck0;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const float2 x = *reinterpret_cast<const float2*>(ck + (row0 + g + 8 * h) * V + 8 * nt + 2 * c);
+        const int o = (row0 + g + 8 * h) * V + 8 * nt + 2 * c;
+        const float2 x = in_range(p.status, ck0 + o, 2, s_ext * p.nck, CHK_BWD_CKPT)
+                             ? *reinterpret_cast<const float2*>(ck + o)
+                             : make_float2(0.f, 0.f);
         H[nt][2 * h] = x.x;
         H[nt][2 * h + 1] = x.y;
       }
@@ -487,8 +507,10 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
           const int i = e / r4, x = e - i * r4;
           const float4 a = ptx::lds_f32x4(rq + static_cast<uint32_t>((i * RS + 4 * x) * 4));
           const float4 d = ptx::lds_f32x4(rk + static_cast<uint32_t>((i * RS + 4 * x) * 4));
-          red_add_v4(p.dq + ((bt + i) * Nq + gq) * K + row0c + 4 * x, a.x, a.y, a.z, a.w);
-          red_add_v4(p.dk + ((bt + i) * Nq + gq) * K + row0c + 4 * x, d.x, d.y, d.z, d.w);
+          const size_t qo = ((bt + i) * Nq + gq) * K + row0c + 4 * x;
+          if (!in_range(p.status, qo, 4, qk_ext, CHK_BWD_DQK)) continue;
+          red_add_v4(p.dq + qo, a.x, a.y, a.z, a.w);
+          red_add_v4(p.dk + qo, d.x, d.y, d.z, d.w);
         }
         for (int e = tid; e < Ls * V; e += nthr) {
           const int i = e / V, jj = e - i * V;
@@ -498,7 +520,12 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
           const int s = s0 + i;
           const float uu = one_f32<F32>(sb + L.in_dy + static_cast<uint32_t>((s * V + jj) * es));
           const float vv = one_f32<F32>(sb + L.in_v + buf * L.vbuf + static_cast<uint32_t>((s * V + jj) * es));
-          float* dst = p.dv + ((bt + i) * N + n) * V + jj;
+          const size_t vo = ((bt + i) * N + n) * V + jj;
+          float* dst = p.dv + vo;
+          if (!in_range(p.status, vo, 1, v_ext, CHK_BWD_DV) ||
+              !in_range(p.status, static_cast<size_t>(n) * V + jj, 1, static_cast<size_t>(N) * V,
+                        CHK_BWD_PARAM))
+            continue;
           if (p.nslices == 1) {
             *dst = fmaf(tof(wr[jj]), uu, acc);
           } else {
@@ -509,6 +536,7 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
         for (int i = tid; i < Ls; i += nthr) {
           float acc = 0.f;
           for (int w = 0; w < WPC; ++w) acc += ptx::lds_f32(rf + static_cast<uint32_t>((i * WPC + w) * 4));
+          if (!in_range(p.status, (bt + i) * N + n, 1, f_ext, CHK_BWD_DF)) continue;
           if (gated) {  // chain rule through the gate: this slice's share of da, dalpha, dbeta
             float gf, gda, gdal;
             gate_f_grads(tof(fin[(bt + i) * N + n]), g_alpha, g_beta, gf, gda, gdal);
@@ -526,13 +554,16 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
     }
     // C now holds dL/dH_{t0}: the gradient of this interval's checkpoint.
     if (p.dckpt != nullptr && ci % p.dck_ratio == 0) {
-      float* dst = p.dckpt + ((static_cast<size_t>(b) * N + n) * p.dck_n + ci / p.dck_ratio) * K * V;
+      const size_t d0 = ((static_cast<size_t>(b) * N + n) * p.dck_n + ci / p.dck_ratio) * K * V;
+      float* dst = p.dckpt + d0;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          *reinterpret_cast<float2*>(dst + (row0 + g + 8 * h) * V + 8 * nt + 2 * c) =
-              make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
+        for (int h = 0; h < 2; ++h) {
+          const int o = (row0 + g + 8 * h) * V + 8 * nt + 2 * c;
+          if (in_range(p.status, d0 + o, 2, s_ext * p.dck_n, CHK_BWD_DCKPT))
+            *reinterpret_cast<float2*>(dst + o) = make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
+        }
     }
   }
 
@@ -541,9 +572,11 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        *reinterpret_cast<float2*>(p.dH0 + sidx + (row0 + g + 8 * h) * V + 8 * nt + 2 * c) =
-            make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
+      for (int h = 0; h < 2; ++h) {
+        const size_t o = sidx + (row0 + g + 8 * h) * V + 8 * nt + 2 * c;
+        if (in_range(p.status, o, 2, s_ext, CHK_BWD_DH0))
+          *reinterpret_cast<float2*>(p.dH0 + o) = make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
+      }
   }
   // dW: this warp's [V][V] sum -> shared memory (over the sub-checkpoints,
   // no longer read) -> CTA sum -> global
@@ -565,11 +598,11 @@ __global__ void __launch_bounds__(256) bwd_kernel(const BwdParams p) {
     float acc = 0.f;
     for (int w = 0; w < WPC; ++w)
       acc += ptx::lds_f32(sb + L.dwsum + static_cast<uint32_t>((w * V * V + e) * 4));
-    red_add(p.dW + static_cast<size_t>(n) * V * V + e, acc);
+    if (n_ok) red_add(p.dW + static_cast<size_t>(n) * V * V + e, acc);
   }
   // each thread holds the u (.) v sum of column tid % V over the steps it flushed
-  if (slice == 0) red_add(p.dw_r + static_cast<size_t>(n) * V + tid % V, dwr_acc);
-  if (gated && tid < S2) {  // the threads that flushed df
+  if (slice == 0 && n_ok) red_add(p.dw_r + static_cast<size_t>(n) * V + tid % V, dwr_acc);
+  if (gated && tid < S2 && n_ok) {  // the threads that flushed df
     red_add(p.dalpha + n, dalpha_acc);
     red_add(p.dbeta + n, dbeta_acc);
   }

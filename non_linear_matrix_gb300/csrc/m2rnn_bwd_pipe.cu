@@ -43,6 +43,7 @@
 #include "m2rnn.h"
 #include "m2rnn_bwd_common.cuh"
 #include "m2rnn_gate.cuh"
+#include "m2rnn_check.cuh"
 #include "m2rnn_internal.h"
 #include "ptx.cuh"
 
@@ -245,8 +246,13 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
   // f, or with the fused input gate its input a (same layout and dtype)
   constexpr bool gated = GATED;
   const TIn* fin = static_cast<const TIn*>(gated ? p.a : p.f);
-  const float g_alpha = gated ? tof(static_cast<const TIn*>(p.alpha)[n]) : 0.f;
-  const float g_beta = gated ? tof(static_cast<const TIn*>(p.beta)[n]) : 0.f;
+  // array extents in elements (index checks of the checked build)
+  const size_t BT = static_cast<size_t>(p.B) * T;
+  const size_t qk_ext = BT * Nq * K, v_ext = BT * N * V, f_ext = BT * N;
+  const size_t s_ext = static_cast<size_t>(p.B) * N * K * V;  // dH_T, dH0
+  const bool n_ok = in_range(p.status, n, 1, N, CHK_BWD_PARAM);
+  const float g_alpha = gated && n_ok ? tof(static_cast<const TIn*>(p.alpha)[n]) : 0.f;
+  const float g_beta = gated && n_ok ? tof(static_cast<const TIn*>(p.beta)[n]) : 0.f;
   float dalpha_acc = 0.f, dbeta_acc = 0.f;  // gate parameter sums of this thread's steps
   const TIn* dy = static_cast<const TIn*>(p.dy);
   const TIn* Wn = static_cast<const TIn*>(p.W) + static_cast<size_t>(n) * V * V;
@@ -261,12 +267,12 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int kk = 16 * ks + 8 * h + 2 * c, nn = 8 * nt + g;
-        const float w0 = tof(Wn[kk * V + nn]), w1 = tof(Wn[(kk + 1) * V + nn]);
+        const float w0 = n_ok ? tof(Wn[kk * V + nn]) : 0.f, w1 = n_ok ? tof(Wn[(kk + 1) * V + nn]) : 0.f;
         Bw[ks][nt][h] = ptx::pack_bf16x2(w0, w1);
         Bwl[ks][nt][h] = F32 ? ptx::pack_bf16x2(w0 - ptx::bf16x2_lo(Bw[ks][nt][h]),
                                                 w1 - ptx::bf16x2_hi(Bw[ks][nt][h]))
                              : 0u;
-        const float t0 = tof(Wn[nn * V + kk]), t1 = tof(Wn[nn * V + kk + 1]);
+        const float t0 = n_ok ? tof(Wn[nn * V + kk]) : 0.f, t1 = n_ok ? tof(Wn[nn * V + kk + 1]) : 0.f;
         Bt[ks][nt][h] = ptx::pack_bf16x2(t0, t1);
         Btl[ks][nt][h] = F32 ? ptx::pack_bf16x2(t0 - ptx::bf16x2_lo(Bt[ks][nt][h]),
                                                 t1 - ptx::bf16x2_hi(Bt[ks][nt][h]))
@@ -280,7 +286,8 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int row = row0 + g + 8 * (r >> 1), col = 8 * nt + 2 * c + (r & 1);
-      Cg[nt][r] = p.dHT ? p.dHT[sidx + row * V + col] : 0.f;
+      const size_t o = sidx + row * V + col;
+      Cg[nt][r] = p.dHT && in_range(p.status, o, 1, s_ext, CHK_BWD_DHT) ? p.dHT[o] : 0.f;
     }
   float dW[KS][NT][4];
 #pragma unroll
@@ -300,12 +307,16 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
   };
   auto phys = [&](int ci2, int m) { return (ci2 & 1) ? NS1 - 1 - m : m; };
   auto load_ckpt = [&](int ci2, float (&Hc)[NT][4]) {
-    const float* ck = p.ckpt + ((static_cast<size_t>(b) * N + n) * nck + ci2) * K * V;
+    const size_t ck0 = ((static_cast<size_t>(b) * N + n) * nck + ci2) * K * V;
+    const float* ck = p.ckpt + ck0;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const float2 x = *reinterpret_cast<const float2*>(ck + (row0 + g + 8 * h) * V + 8 * nt + 2 * c);
+        const int o = (row0 + g + 8 * h) * V + 8 * nt + 2 * c;
+        const float2 x = in_range(p.status, ck0 + o, 2, s_ext * nck, CHK_BWD_CKPT)
+                             ? *reinterpret_cast<const float2*>(ck + o)
+                             : make_float2(0.f, 0.f);
         Hc[nt][2 * h] = x.x;
         Hc[nt][2 * h + 1] = x.y;
       }
@@ -396,10 +407,11 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
       const bool isR = kind != 2 && kind != 5;
       if (i >= (isR ? sr.nR : sr.nL)) continue;
       const size_t t = (isR ? sr.tR : sr.tL) + i;
-      const TIn* src = kind <= 2 ? (kind == 0 ? q : kin) + (t * Nq + gq) * K + row0c
-                                 : (kind == 4 ? dy : vin) + (t * N + n) * V;
-      ptx::cp_async16(raw + static_cast<uint32_t>((tid + u * nthr) * 16),
-                      reinterpret_cast<const uint4*>(src) + x);
+      const size_t so = kind <= 2 ? (t * Nq + gq) * K + row0c : (t * N + n) * V;
+      const TIn* src = (kind <= 2 ? (kind == 0 ? q : kin) : (kind == 4 ? dy : vin)) + so;
+      if (in_range(p.status, so + x * (16 / es), 16 / es, kind <= 2 ? qk_ext : v_ext, CHK_BWD_IN))
+        ptx::cp_async16(raw + static_cast<uint32_t>((tid + u * nthr) * 16),
+                        reinterpret_cast<const uint4*>(src) + x);
     }
     if (ft >= 0 && ft < 2 * S2) {  // f of R (ft < S2) and of L: the aligned 32-bit word holding it
       const bool isR = ft < S2;
@@ -407,7 +419,9 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
       if (i < (isR ? sr.nR : sr.nL)) {
         const size_t idx = ((isR ? sr.tR : sr.tL) + i) * N + n;
         const uint32_t dst = raw_f + 4 * ft;
-        if (es == 4 || (idx | 1) < f_total) {
+        if (!in_range(p.status, idx, 1, f_ext, CHK_BWD_IN)) {
+          // (checked build: skipped)
+        } else if (es == 4 || (idx | 1) < f_total) {
           ptx::cp_async4(dst, fin + (es == 4 ? idx : (idx & ~static_cast<size_t>(1))));
         } else {  // the last element of an odd-length bf16 array: its word would overrun
           const uint32_t bits = __bfloat16_as_ushort(*reinterpret_cast<const __nv_bfloat16*>(fin + idx));
@@ -779,11 +793,12 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
       const uint32_t rk = sb + L.r_dk + static_cast<uint32_t>(rb * S2 * WPC * 64);
       const uint32_t rv = sb + L.r_dv + static_cast<uint32_t>(rb * S2 * WPC * KS * 64);
       const uint32_t rf = sb + L.r_df + static_cast<uint32_t>(rb * S2 * WPC * 4);
-      if (row_ok && i_r < Ls) {
+      const size_t qo = ((bt + i_r) * Nq + gq) * K + row0c + r0;
+      if (row_ok && i_r < Ls && in_range(p.status, qo, 4, qk_ext, CHK_BWD_DQK)) {
         const uint32_t o = fl_off;
-        red_add_v4(p.dq + ((bt + i_r) * Nq + gq) * K + row0c + r0, ptx::lds_f32(rq + o), ptx::lds_f32(rq + o + 8),
+        red_add_v4(p.dq + qo, ptx::lds_f32(rq + o), ptx::lds_f32(rq + o + 8),
                    ptx::lds_f32(rq + o + 16), ptx::lds_f32(rq + o + 24));
-        red_add_v4(p.dk + ((bt + i_r) * Nq + gq) * K + row0c + r0, ptx::lds_f32(rk + o), ptx::lds_f32(rk + o + 8),
+        red_add_v4(p.dk + qo, ptx::lds_f32(rk + o), ptx::lds_f32(rk + o + 8),
                    ptx::lds_f32(rk + o + 16), ptx::lds_f32(rk + o + 24));
       }
       for (int e = tid; e < Ls * V; e += nthr) {
@@ -796,7 +811,11 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
         const uint32_t fo = static_cast<uint32_t>(((i * 4 + ((jc & 7) >> 1)) * NT + (jc >> 3)) * 8 + (jc & 1) * 4);
         const float uu = ptx::lds_f32(B0 + L.uf + fo);
         const float vv = ptx::lds_f32(B0 + L.vf + fo);
-        float* dst = p.dv + ((bt + i) * N + n) * V + jc;
+        const size_t vo = ((bt + i) * N + n) * V + jc;
+        float* dst = p.dv + vo;
+        if (!in_range(p.status, vo, 1, v_ext, CHK_BWD_DV) ||
+            !in_range(p.status, static_cast<size_t>(n) * V + jc, 1, static_cast<size_t>(N) * V, CHK_BWD_PARAM))
+          continue;
         if (p.nslices == 1)
           *dst = fmaf(tof(wr[jc]), uu, acc);
         else
@@ -814,11 +833,14 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
           acc *= gda;
           dbeta_acc += acc;
         }
-        float* dst = p.df + (bt + i) * N + n;
-        if (p.nslices == 1)
-          *dst = acc;
-        else
-          red_add(dst, acc);
+        const size_t fo = (bt + i) * N + n;
+        float* dst = p.df + fo;
+        if (in_range(p.status, fo, 1, f_ext, CHK_BWD_DF)) {
+          if (p.nslices == 1)
+            *dst = acc;
+          else
+            red_add(dst, acc);
+        }
       }
     }
     if (nci >= 0) convert(nci, njj, true, bufi ^ 1);
@@ -830,13 +852,16 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
       if (have_l1 && nsub < NS1) serial_chunks(ci, nsub, NS1, bufi);
       // C now holds dL/dH at the interval start: the checkpoint's gradient
       if (p.dckpt != nullptr && ci % p.dck_ratio == 0) {
-        float* dst = p.dckpt + ((static_cast<size_t>(b) * N + n) * p.dck_n + ci / p.dck_ratio) * K * V;
+        const size_t d0 = ((static_cast<size_t>(b) * N + n) * p.dck_n + ci / p.dck_ratio) * K * V;
+        float* dst = p.dckpt + d0;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            *reinterpret_cast<float2*>(dst + (row0 + g + 8 * h) * V + 8 * nt + 2 * c) =
-                make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
+          for (int h = 0; h < 2; ++h) {
+            const int o = (row0 + g + 8 * h) * V + 8 * nt + 2 * c;
+            if (in_range(p.status, d0 + o, 2, s_ext * p.dck_n, CHK_BWD_DCKPT))
+              *reinterpret_cast<float2*>(dst + o) = make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
+          }
       }
       if (ci == 0) break;
       --ci;
@@ -854,9 +879,11 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        *reinterpret_cast<float2*>(p.dH0 + sidx + (row0 + g + 8 * h) * V + 8 * nt + 2 * c) =
-            make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
+      for (int h = 0; h < 2; ++h) {
+        const size_t o = sidx + (row0 + g + 8 * h) * V + 8 * nt + 2 * c;
+        if (in_range(p.status, o, 2, s_ext, CHK_BWD_DH0))
+          *reinterpret_cast<float2*>(p.dH0 + o) = make_float2(Cg[nt][2 * h], Cg[nt][2 * h + 1]);
+      }
   }
   // dW: this warp's [V][V] sum -> shared memory (over the sub-checkpoints, no
   // longer read after the last barrier) -> CTA sum -> global
@@ -877,11 +904,11 @@ __global__ void __launch_bounds__(32 * WPC) bwd_pipe_kernel(const BwdParams p) {
     float acc = 0.f;
     for (int w = 0; w < WPC; ++w)
       acc += ptx::lds_f32(sb + L.subck + static_cast<uint32_t>((w * V * V + e) * 4));
-    red_add(p.dW + static_cast<size_t>(n) * V * V + e, acc);
+    if (n_ok) red_add(p.dW + static_cast<size_t>(n) * V * V + e, acc);
   }
   // each thread holds the u (.) v sum of column tid % V over the steps it flushed
-  if (slice == 0) red_add(p.dw_r + static_cast<size_t>(n) * V + tid % V, dwr_acc);
-  if (gated && dt >= 0 && dt < S2) {
+  if (slice == 0 && n_ok) red_add(p.dw_r + static_cast<size_t>(n) * V + tid % V, dwr_acc);
+  if (gated && dt >= 0 && dt < S2 && n_ok) {
     red_add(p.dalpha + n, dalpha_acc);
     red_add(p.dbeta + n, dbeta_acc);
   }

@@ -25,6 +25,7 @@
 #include "m2rnn.h"
 #include "m2rnn_internal.h"
 #include "m2rnn_gate.cuh"
+#include "m2rnn_check.cuh"
 #include "ptx.cuh"
 
 namespace m2rnn {
@@ -67,6 +68,14 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
   const TIn* wr = static_cast<const TIn*>(p.w_r) + static_cast<size_t>(n) * V;
   const float* Hin = p.H_in + head * K * V;
   float* Hout = p.H_out + head * K * V;
+  // index checks of the checked build (uniform over the CTA, before any barrier)
+  const size_t BN = static_cast<size_t>(p.B) * N, s_ext = BN * K * V;
+  if (!in_range(p.status, qrow * K, K, static_cast<size_t>(p.B) * p.Nq * K, CHK_DEC_IN) ||
+      !in_range(p.status, head * V, V, BN * V, CHK_DEC_IN) ||
+      !in_range(p.status, head, 1, BN, CHK_DEC_IN) ||
+      !in_range(p.status, static_cast<size_t>(n) * V * V, V * V, static_cast<size_t>(N) * V * V, CHK_DEC_IN) ||
+      !in_range(p.status, head * V, V, BN * V, CHK_DEC_Y))
+    return;
 
   // the state first: the loads that decide the kernel's time, all in flight
   // before any use
@@ -77,8 +86,10 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const float2 x = __ldcs(reinterpret_cast<const float2*>(
-            Hin + (row0 + 16 * m + g + 8 * h) * V + 8 * nt + 2 * c));
+        const int o = (row0 + 16 * m + g + 8 * h) * V + 8 * nt + 2 * c;
+        const float2 x = in_range(p.status, head * K * V + o, 2, s_ext, CHK_DEC_STATE)
+                             ? __ldcs(reinterpret_cast<const float2*>(Hin + o))
+                             : make_float2(0.f, 0.f);
         H[m][nt][2 * h] = x.x;
         H[m][nt][2 * h + 1] = x.y;
       }
@@ -167,7 +178,9 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
         const float2 r = __ffma2_rn(f2, d, z);
         hn[2 * h] = r.x;
         hn[2 * h + 1] = r.y;
-        __stcs(reinterpret_cast<float2*>(Hout + (r0 + g + 8 * h) * V + 8 * nt + 2 * c), r);
+        const int o = (r0 + g + 8 * h) * V + 8 * nt + 2 * c;
+        if (in_range(p.status, head * K * V + o, 2, s_ext, CHK_DEC_STATE))
+          __stcs(reinterpret_cast<float2*>(Hout + o), r);
       }
       // this lane's two rows of the readout for columns 8nt + 2c, 8nt + 2c + 1
       ypart[nt][0] += fmaf(hn[0], q0, hn[2] * q1);

@@ -46,6 +46,7 @@
 #include "m2rnn_internal.h"
 #include "ptx.cuh"
 #include "m2rnn_gate.cuh"
+#include "m2rnn_check.cuh"
 
 namespace m2rnn {
 namespace {
@@ -171,6 +172,9 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
   const TIn* gbeta = static_cast<const TIn*>(p.beta);
   // query/key group of this CTA's heads (the host keeps a CTA inside one group)
   const int Nq = p.Nq, gq = n0 / (N / Nq);
+  // array extents in elements (index checks of the checked build)
+  const size_t qk_ext = static_cast<size_t>(p.B) * T * Nq * K;
+  const size_t v_ext = static_cast<size_t>(p.B) * T * N * V, f_ext = static_cast<size_t>(p.B) * T * N;
 
   // Waits for a free stage, starts the bulk copies of chunk ch and writes
   // its f (or, gated, f computed from a) as fp32 pairs.
@@ -186,22 +190,35 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
     __syncwarp();
     const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
     const size_t bt0 = static_cast<size_t>(b) * T + t0;
+    // (a copy the checked build skips still counts its bytes as arrived)
     if (Nq == 1) {  // the chunk's q and k rows are contiguous
       if (lane == 0) {
-        ptx::bulk_g2s(st + L.q, q + bt0 * K, qk_bytes, raw);
-        ptx::bulk_g2s(st + L.k, k + bt0 * K, qk_bytes, raw);
+        if (in_range(p.status, bt0 * K, static_cast<size_t>(Tc) * K, qk_ext, CHK_FWD_QK)) {
+          ptx::bulk_g2s(st + L.q, q + bt0 * K, qk_bytes, raw);
+          ptx::bulk_g2s(st + L.k, k + bt0 * K, qk_bytes, raw);
+        } else {
+          ptx::mbar_complete_tx(raw, 2 * qk_bytes);
+        }
       }
     } else {  // one row per step: [t][Nq][K], group gq
       const uint32_t row_bytes = static_cast<uint32_t>(K * es);
       for (int tl = lane; tl < Tc; tl += 32) {
         const size_t src = ((bt0 + tl) * Nq + gq) * K;
-        ptx::bulk_g2s(st + L.q + tl * row_bytes, q + src, row_bytes, raw);
-        ptx::bulk_g2s(st + L.k + tl * row_bytes, k + src, row_bytes, raw);
+        if (in_range(p.status, src, K, qk_ext, CHK_FWD_QK)) {
+          ptx::bulk_g2s(st + L.q + tl * row_bytes, q + src, row_bytes, raw);
+          ptx::bulk_g2s(st + L.k + tl * row_bytes, k + src, row_bytes, raw);
+        } else {
+          ptx::mbar_complete_tx(raw, 2 * row_bytes);
+        }
       }
     }
-    for (int tl = lane; tl < Tc; tl += 32)
-      ptx::bulk_g2s(st + L.v + static_cast<uint32_t>(tl * G * V * es),
-                    v + ((bt0 + tl) * N + n0) * V, v_bytes, raw);
+    for (int tl = lane; tl < Tc; tl += 32) {
+      const size_t src = ((bt0 + tl) * N + n0) * V;
+      if (in_range(p.status, src, static_cast<size_t>(Geff) * V, v_ext, CHK_FWD_V))
+        ptx::bulk_g2s(st + L.v + static_cast<uint32_t>(tl * G * V * es), v + src, v_bytes, raw);
+      else
+        ptx::mbar_complete_tx(raw, v_bytes);
+    }
     // f[b, t0:t0+Tc, n0:n0+Geff] -> fp32 pairs [TC][G][2]; loads batched.
     const int nf = Tc * Geff;
     for (int base = 0; base < nf; base += 256) {
@@ -210,12 +227,14 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
       for (int i = 0; i < 8; ++i) {
         const int e = base + lane + 32 * i;
         const int tl = e / Geff, h = e - tl * Geff;
+        const size_t fi = (bt0 + tl) * N + n0 + h;
+        const bool use = e < nf && in_range(p.status, fi, 1, f_ext, CHK_FWD_F);
         if constexpr (GATED)
-          fv[i] = e < nf ? gate_f(to_f(f[(bt0 + tl) * N + n0 + h]), to_f(galpha[n0 + h]),
-                                  to_f(gbeta[n0 + h]))
-                         : 0.f;
+          fv[i] = use && in_range(p.status, n0 + h, 1, N, CHK_FWD_PARAM)
+                      ? gate_f(to_f(f[fi]), to_f(galpha[n0 + h]), to_f(gbeta[n0 + h]))
+                      : 0.f;
         else
-          fv[i] = e < nf ? to_f(f[(bt0 + tl) * N + n0 + h]) : 0.f;
+          fv[i] = use ? to_f(f[fi]) : 0.f;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -353,7 +372,10 @@ __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout
   const int nchunks = (T + TC - 1) / TC;
   const TIn* w_r = static_cast<const TIn*>(p.w_r) + static_cast<size_t>(n0) * V;
   const int GV = Geff * V;
-  for (int e = lane; e < GV; e += 32) ptx::sts_f32(sbase + L.wr + 4 * e, to_f(w_r[e]));
+  const size_t y_ext = static_cast<size_t>(p.B) * T * N * V;  // y and g (index checks)
+  for (int e = lane; e < GV; e += 32)
+    if (in_range(p.status, static_cast<size_t>(n0) * V + e, 1, static_cast<size_t>(N) * V, CHK_FWD_PARAM))
+      ptx::sts_f32(sbase + L.wr + 4 * e, to_f(w_r[e]));
   __syncwarp();
   const int R8 = GV / 8;  // 8-element groups per time step
   for (int ch = 0; ch < nchunks; ++ch) {
@@ -391,18 +413,19 @@ __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout
       const float wr[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i] = fmaf(wr[i], vv[i], o[i]);
-      store8(y + static_cast<size_t>(tl) * N * V + r, o);
+      const size_t yo = ((static_cast<size_t>(b) * T + t0 + tl) * N + n0) * V + r;  // = y + tl N V + r
+      if (in_range(p.status, yo, 8, y_ext, CHK_FWD_Y)) store8(y + static_cast<size_t>(tl) * N * V + r, o);
       if constexpr (NORM) {
-        float gg[8];
-        ldg8<F32>(static_cast<const TIn*>(p.g) +
-                      ((static_cast<size_t>(b) * T + t0 + tl) * N + n0) * V + r, gg);
+        float gg[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (in_range(p.status, yo, 8, y_ext, CHK_FWD_G)) ldg8<F32>(static_cast<const TIn*>(p.g) + yo, gg);
         float part = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float og = o[i] * gg[i];
           part = fmaf(og, og, part);
         }
-        atomicAdd(p.ssq + static_cast<size_t>(b) * T + t0 + tl, part);
+        const size_t so = static_cast<size_t>(b) * T + t0 + tl;
+        if (in_range(p.status, so, 1, static_cast<size_t>(p.B) * T, CHK_FWD_SSQ)) atomicAdd(p.ssq + so, part);
       }
     }
     __syncwarp();
@@ -418,10 +441,12 @@ __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout
 // ---------------------------------------------------------------------------
 
 // Stores the thread's part of the state (rows row0 + 16*mt + g (+8), columns
-// 8*nt + 2c (+1)) to a [K][V] fp32 array.
+// 8*nt + 2c (+1)) to a [K][V] fp32 array.  dst is element off0 of an array
+// of `extent` elements (index checks of the checked build, at `site`).
 template <int V, int MT, bool HALF = false>
 __device__ __forceinline__ void store_state(float* dst, const float (&H)[MT][V / 8][4], int row0,
-                                            int g, int c) {
+                                            int g, int c, int* status, size_t off0, size_t extent,
+                                            int site) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -429,8 +454,9 @@ __device__ __forceinline__ void store_state(float* dst, const float (&H)[MT][V /
 #pragma unroll
       for (int h = 0; h < (HALF ? 1 : 2); ++h) {
         const int row = row0 + 16 * mt + g + 8 * h;
-        *reinterpret_cast<float2*>(dst + row * V + 8 * nt + 2 * c) =
-            make_float2(H[mt][nt][2 * h], H[mt][nt][2 * h + 1]);
+        const int o = row * V + 8 * nt + 2 * c;
+        if (in_range(status, off0 + o, 2, extent, site))
+          *reinterpret_cast<float2*>(dst + o) = make_float2(H[mt][nt][2 * h], H[mt][nt][2 * h + 1]);
       }
 }
 
@@ -712,6 +738,8 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
   WarpState<V, MT> S;
   // W as B operands (k = row l of W, n = column j), bf16 hi (+ lo residual).
   const TIn* Wn = static_cast<const TIn*>(p.W) + static_cast<size_t>(n) * V * V;
+  const bool w_ok = in_range(p.status, static_cast<size_t>(n) * V * V, V * V,
+                             static_cast<size_t>(N) * V * V, CHK_FWD_PARAM);
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
@@ -719,13 +747,15 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int r0 = 16 * ks + 8 * h + 2 * c, col = 8 * nt + g;
-        const float w0 = to_f(Wn[r0 * V + col]), w1 = to_f(Wn[(r0 + 1) * V + col]);
+        const float w0 = w_ok ? to_f(Wn[r0 * V + col]) : 0.f;
+        const float w1 = w_ok ? to_f(Wn[(r0 + 1) * V + col]) : 0.f;
         S.Bw[ks][nt][h] = ptx::pack_bf16x2(w0, w1);
         S.Bwl[ks][nt][h] = F32 ? ptx::pack_bf16x2(w0 - ptx::bf16x2_lo(S.Bw[ks][nt][h]),
                                                   w1 - ptx::bf16x2_hi(S.Bw[ks][nt][h]))
                                : 0u;
       }
   const size_t hoff = (static_cast<size_t>(b) * N + n) * K * V;
+  const size_t h_ext = static_cast<size_t>(p.B) * N * K * V;  // H0, H_T (index checks)
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -733,7 +763,10 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int row = row0 + 16 * mt + g + 8 * (r >> 1), col = 8 * nt + 2 * c + (r & 1);
-        S.H[mt][nt][r] = (p.H0 && (!HALF || r < 2)) ? p.H0[hoff + row * V + col] : 0.f;
+        const size_t o = hoff + row * V + col;
+        S.H[mt][nt][r] = (p.H0 && (!HALF || r < 2) && in_range(p.status, o, 1, h_ext, CHK_FWD_H0))
+                             ? p.H0[o]
+                             : 0.f;
       }
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
@@ -742,6 +775,8 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
   }
 
   float* ckpt = p.ckpt ? p.ckpt + (static_cast<size_t>(b) * N + n) * p.nck * K * V : nullptr;
+  size_t ck_off = (static_cast<size_t>(b) * N + n) * p.nck * K * V;  // element offset of ckpt
+  const size_t ck_ext = static_cast<size_t>(p.B) * N * p.nck * K * V;
   // Absolute step before which the next checkpoint is stored (the state
   // after next_ck steps); beyond T when no checkpoints are written.
   int next_ck = ckpt != nullptr ? 0 : T + 1;
@@ -779,8 +814,9 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
     int tl = 0;
     while (tl < Tc) {
       if (t0 + tl == next_ck) {
-        store_state<V, MT, HALF>(ckpt, S.H, row0, g, c);
+        store_state<V, MT, HALF>(ckpt, S.H, row0, g, c, p.status, ck_off, ck_ext, CHK_FWD_CKPT);
         ckpt += K * V;
+        ck_off += static_cast<size_t>(K) * V;
         next_ck += p.C;
       }
       const int seg_end = min(Tc, next_ck - t0);  // no checkpoint inside [tl, seg_end)
@@ -823,7 +859,8 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
     if (lane == 0) record_timeout(p.status, SITE_FWD_CONSUMER);
     return;
   }
-  if (p.HT != nullptr) store_state<V, MT, HALF>(p.HT + hoff, S.H, row0, g, c);
+  if (p.HT != nullptr)
+    store_state<V, MT, HALF>(p.HT + hoff, S.H, row0, g, c, p.status, hoff, h_ext, CHK_FWD_HT);
 }
 
 // KC, GC (0 = taken from the parameters): K and heads per CTA fixed at

@@ -17,6 +17,36 @@ enum WaitSite : int {
 };
 
 constexpr int kStatusTimeout = -7;  // == M2RNN_ERR_TIMEOUT
+constexpr int kStatusBounds = -8;   // == M2RNN_ERR_BOUNDS (checked build only)
+
+// Location codes of the checked build's index checks (status word [1]).
+enum CheckSite : int {
+  CHK_FWD_QK = 101,     // q, k staging copies
+  CHK_FWD_V = 102,      // v staging copies
+  CHK_FWD_F = 103,      // f (or the gate's a) loads
+  CHK_FWD_Y = 104,      // y stores
+  CHK_FWD_G = 105,      // readout epilogue: g loads
+  CHK_FWD_SSQ = 106,    // readout epilogue: sum-of-squares atomics
+  CHK_FWD_H0 = 107,     // H0 loads
+  CHK_FWD_HT = 108,     // H_T stores
+  CHK_FWD_CKPT = 109,   // checkpoint stores
+  CHK_FWD_PARAM = 110,  // W, w_r, alpha, beta loads
+  CHK_BWD_IN = 201,     // q, k, v, dy, f (or a) loads
+  CHK_BWD_CKPT = 202,   // checkpoint loads
+  CHK_BWD_DQK = 203,    // dq, dk reductions
+  CHK_BWD_DV = 204,     // dv stores / reductions
+  CHK_BWD_DF = 205,     // df (or da) stores / reductions
+  CHK_BWD_DCKPT = 206,  // dckpt stores
+  CHK_BWD_DH0 = 207,    // dH0 stores
+  CHK_BWD_DPARAM = 208, // dW, dw_r, dalpha, dbeta reductions
+  CHK_BWD_DHT = 209,    // dH_T loads
+  CHK_BWD_PARAM = 210,  // W, w_r, alpha, beta loads
+  CHK_DEC_IN = 301,     // q, k, v, f (or a), W, w_r, alpha, beta loads
+  CHK_DEC_STATE = 302,  // state loads and stores
+  CHK_DEC_Y = 303,      // y stores
+  CHK_NORM_IN = 401,    // y, g, w, dout, rstd loads
+  CHK_NORM_OUT = 402,   // out, rstd, dy, dg stores, dw reductions
+};
 
 struct FwdParams {
   const void* q;
@@ -91,6 +121,7 @@ struct BwdParams {
   int gated = 0;
   float* dalpha = nullptr;
   float* dbeta = nullptr;
+  int* status = nullptr;  // device status word (index checks of the checked build)
 };
 
 cudaError_t launch_bwd(const BwdParams& p, int V, bool f32_inputs, cudaStream_t stream);
@@ -122,6 +153,7 @@ struct DecodeParams {
   const void* alpha = nullptr;
   const void* beta = nullptr;
   int gated = 0;
+  int* status = nullptr;  // device status word (index checks of the checked build)
 };
 cudaError_t launch_decode(const DecodeParams& p, int V, bool f32_inputs, cudaStream_t stream);
 
@@ -143,6 +175,7 @@ struct NormParams {
   void* dy;         // backward: [rows][d] input dtype
   float* dg;        // backward: [rows][d]
   float* dw;        // backward: [d]
+  int* status = nullptr;  // device status word (index checks of the checked build)
 };
 cudaError_t launch_norm_fwd(const NormParams& p, bool f32_inputs, int sms, cudaStream_t stream);
 cudaError_t launch_norm_bwd(const NormParams& p, bool f32_inputs, int sms, cudaStream_t stream);

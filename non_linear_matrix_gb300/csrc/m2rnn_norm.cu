@@ -19,6 +19,7 @@
 
 #include "m2rnn_internal.h"
 #include "ptx.cuh"
+#include "m2rnn_check.cuh"
 
 namespace m2rnn {
 namespace {
@@ -85,6 +86,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) norm_fwd_kernel(const NormP
     s = __shfl_sync(0xffffffffu, s, 0);
     const size_t base = static_cast<size_t>(row) * d;
     for (int e = lane; e < d8; e += 32) {
+      if (!in_range(p.status, base + 8 * e, 8, static_cast<size_t>(p.rows) * d, CHK_NORM_IN) ||
+          !in_range(p.status, 8 * e, 8, d, CHK_NORM_IN))
+        continue;
       float yy[8], gg[8], ww[8], o[8];
       load8<F32>(y + base + 8 * e, yy);
       load8<F32>(g + base + 8 * e, gg);
@@ -118,6 +122,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) norm_bwd_kernel(const NormP
     const float s = p.rstd[row];
     float r = 0.f;  // sum_d (w dout) (y g)
     for (int e = lane; e < d8; e += 32) {
+      if (!in_range(p.status, base + 8 * e, 8, static_cast<size_t>(p.rows) * d, CHK_NORM_IN) ||
+          !in_range(p.status, 8 * e, 8, d, CHK_NORM_IN))
+        continue;
       float yy[8], gg[8], ww[8], uu[8];
       load8<F32>(y + base + 8 * e, yy);
       load8<F32>(g + base + 8 * e, gg);
@@ -130,6 +137,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) norm_bwd_kernel(const NormP
     for (int m = 16; m >= 1; m >>= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
     const float c = r * s * s * s * inv_d;
     for (int e = lane; e < d8; e += 32) {  // the row again (L1/L2 resident)
+      if (!in_range(p.status, base + 8 * e, 8, static_cast<size_t>(p.rows) * d, CHK_NORM_OUT) ||
+          !in_range(p.status, 8 * e, 8, d, CHK_NORM_OUT))
+        continue;
       float yy[8], gg[8], ww[8], uu[8], dyo[8], dgo[8];
       load8<F32>(y + base + 8 * e, yy);
       load8<F32>(g + base + 8 * e, gg);

@@ -16,12 +16,15 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libm2rnn.so")
+# The checked build (index checks in every kernel, M2RNN_ERR_BOUNDS), loaded
+# instead of LIB_PATH when M2RNN_LIBRARY=checked or after use_library("checked").
+LIB_CHECKED_PATH = os.path.join(_HERE, "_build", "check", "libm2rnn_check.so")
 
 M2RNN_F32, M2RNN_BF16 = 0, 1
 STATUS = {
     0: "M2RNN_OK", -1: "M2RNN_ERR_INVALID_ARG", -2: "M2RNN_ERR_UNSUPPORTED_SHAPE",
     -3: "M2RNN_ERR_MISALIGNED", -4: "M2RNN_ERR_POINTER", -5: "M2RNN_ERR_WORKSPACE",
-    -6: "M2RNN_ERR_CUDA", -7: "M2RNN_ERR_TIMEOUT",
+    -6: "M2RNN_ERR_CUDA", -7: "M2RNN_ERR_TIMEOUT", -8: "M2RNN_ERR_BOUNDS",
 }
 
 _lock = threading.Lock()
@@ -30,6 +33,7 @@ _lib = None
 _VP = ctypes.c_void_p
 _EXPORTS = {
     "m2rnn_version": (ctypes.c_int, []),
+    "m2rnn_checked": (ctypes.c_int, []),
     "m2rnn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "m2rnn_num_checkpoints": (ctypes.c_size_t, [_VP]),
     "m2rnn_fwd": (ctypes.c_int, [_VP] * 12),
@@ -61,22 +65,39 @@ class Shape(ctypes.Structure):
                 ("ckpt_every", ctypes.c_int), ("Nq", ctypes.c_int)]
 
 
+def _load(path: str, how: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           f"`python -m non_linear_matrix_gb300.build{how}` (there is no fallback)")
+    L = ctypes.CDLL(path)
+    for name, (res, args) in _EXPORTS.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib() -> ctypes.CDLL:
     """The loaded native library (raises if it was never built)."""
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise RuntimeError(
-                    f"{LIB_PATH} is missing: build it with "
-                    "`python -m non_linear_matrix_gb300.build` (there is no fallback)")
-            L = ctypes.CDLL(LIB_PATH)
-            for name, (res, args) in _EXPORTS.items():
-                fn = getattr(L, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = L
+            if os.environ.get("M2RNN_LIBRARY") == "checked":
+                _lib = _load(LIB_CHECKED_PATH, " checked")
+            else:
+                _lib = _load(LIB_PATH, "")
     return _lib
+
+
+def use_library(which: str):
+    """Switch every later call to the normal ("normal") or the checked
+    ("checked") build; both must have been built.  Each build keeps its own
+    device status word."""
+    global _lib
+    if which not in ("normal", "checked"):
+        raise ValueError(which)
+    with _lock:
+        _lib = _load(LIB_CHECKED_PATH, " checked") if which == "checked" else _load(LIB_PATH, "")
 
 
 def status_string(code: int) -> str:
