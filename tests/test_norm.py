@@ -171,6 +171,24 @@ def test_backward_norm_gated_grouped_recomputed(m2rnn, oracle_mod):
     _bwd_restart(m2rnn, oracle_mod, x, 32, "bf16", gated=True, give_ckpt=False, label="gated")
 
 
+@pytest.mark.parametrize("K,V,dtype,Nq", [(16, 16, "f32", 1), (32, 16, "bf16", 2),
+                                          (128, 16, "bf16", 1), (64, 32, "f32", 2),
+                                          (128, 32, "bf16", 1)])
+def test_norm_gated_shape_matrix(m2rnn, oracle_mod, K, V, dtype, Nq):
+    """The epilogue with the fused gate at the other K, V and dtype
+    combinations, which run other kernel instances (1-, 2- and 8-slice
+    heads; the serial backward at V = 32; fp32 operands), with and without
+    query/key groups: out and rstd on the GPU's y, every gradient per
+    16-step checkpoint interval, ragged last interval."""
+    x = make_inputs(2, 50, 4, K, V, dtype, 1300 + K + V, with_dy=True, norm=True, gated=True,
+                    groups=Nq)
+    r = _fwd(m2rnn, _dev(x), 1e-6, 16, gated=True)
+    torch.cuda.synchronize()
+    _status_ok(m2rnn)
+    _check_epilogue(oracle_mod, x, r, 1e-6, dtype, f"K{K} V{V} {dtype}")
+    _bwd_restart(m2rnn, oracle_mod, x, 16, dtype, gated=True, label=f"K{K} V{V} {dtype} Nq{Nq}")
+
+
 def test_backward_norm_whole_short(m2rnn, oracle_mod):
     """Whole-sequence gradients of the block against bwd_norm of the oracle."""
     for dtype in ("bf16", "f32"):
