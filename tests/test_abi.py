@@ -38,10 +38,29 @@ def test_exports_every_declared_symbol(lib):
 
 def test_status_strings_and_version(lib):
     from non_linear_matrix_gb300 import m2rnn
-    assert lib.m2rnn_version() >= 100
-    for code in range(-7, 1):
-        assert len(m2rnn.status_string(code)) > 0
+    assert lib.m2rnn_version() >= 201
+    for code in range(-8, 1):
+        assert m2rnn.status_string(code) != "unknown status", code
+        assert code in m2rnn.STATUS, code
     assert m2rnn.status_string(12345) == "unknown status"
+
+
+def test_checked_build_is_a_separate_library(lib):
+    """The normal build reports m2rnn_checked() == 0; the checked build (same
+    sources, -DM2RNN_CHECK=1) reports 1, exports the same functions and
+    describes M2RNN_ERR_BOUNDS."""
+    from non_linear_matrix_gb300 import m2rnn
+    assert lib.m2rnn_checked() == 0
+    path = nb.build(checked=True)
+    assert path == m2rnn.LIB_CHECKED_PATH and path != m2rnn.LIB_PATH
+    chk = ctypes.CDLL(path)
+    chk.m2rnn_checked.restype = ctypes.c_int
+    chk.m2rnn_status_string.restype = ctypes.c_char_p
+    chk.m2rnn_status_string.argtypes = [ctypes.c_int]
+    assert chk.m2rnn_checked() == 1
+    for name in _declared_functions():
+        assert hasattr(chk, name), name
+    assert b"checked build" in chk.m2rnn_status_string(-8)
 
 
 def test_fault_injection_modes(lib):
