@@ -21,7 +21,7 @@ import numpy as np
 import pytest
 import torch
 
-from non_linear_matrix_gb300.inputs import make_inputs
+from non_linear_matrix_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -267,11 +267,11 @@ def test_gate_alpha_zero(m2rnn):
 
 
 def test_gated_workload_interval_parity(m2rnn, oracle_mod):
-    """The fwd+bwd workload's sequence length and heads (T=4096, N=32,
-    C=64) with the gate, on 2 batch items: every gradient, including the
-    dalpha / dbeta sums, per 64-step interval."""
-    x = make_inputs(2, 4096, 32, 64, 16, "bf16", 4, with_dy=True, gated=True)
-    _gated_restart(m2rnn, oracle_mod, x, 64, label="gated b2 t4096 n32")
+    """The gated fwd+bwd workload bench.py times (B=8, T=4096, N=32, C=64),
+    on its own inputs and in its launch configuration: every gradient,
+    including the dalpha / dbeta sums, per 64-step interval."""
+    x = workload_inputs(WORKLOADS["fwdbwd_gated_bf16_b8_t4096_n32"])
+    _gated_restart(m2rnn, oracle_mod, x, 64, label="gated b8 t4096 n32")
 
 
 def test_gated_zero_steps(m2rnn):

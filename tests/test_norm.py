@@ -20,7 +20,7 @@ import numpy as np
 import pytest
 import torch
 
-from non_linear_matrix_gb300.inputs import make_inputs
+from non_linear_matrix_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -207,7 +207,8 @@ def test_backward_norm_whole_short(m2rnn, oracle_mod):
 
 
 def test_norm_workload_interval_parity(m2rnn, oracle_mod):
-    """T=4096, N=32, C=64 on 2 batch items: the epilogue on every token and
-    every gradient per 64-step interval."""
-    x = make_inputs(2, 4096, 32, 64, 16, "bf16", 4, with_dy=True, norm=True)
-    _bwd_restart(m2rnn, oracle_mod, x, 64, "bf16", label="norm t4096")
+    """The readout-epilogue fwd+bwd workload bench.py times (B=8, T=4096,
+    N=32, C=64), on its own inputs and in its launch configuration: the
+    epilogue on every token and every gradient per 64-step interval."""
+    x = workload_inputs(WORKLOADS["fwdbwd_norm_bf16_b8_t4096_n32"])
+    _bwd_restart(m2rnn, oracle_mod, x, 64, "bf16", label="norm b8 t4096")
