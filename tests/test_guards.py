@@ -97,8 +97,9 @@ def test_fwd_bwd_write_only_their_outputs(m2rnn, B, T, N, K, V, dtype, C, Nq):
     assert st == 0
 
 
-def test_gated_and_norm_write_only_their_outputs(m2rnn):
-    B, T, N, K, V, C = 3, 45, 6, 64, 16, 16
+@pytest.mark.parametrize("B,T,N", [(3, 45, 6), (41, 40, 32)])  # the second splits the forward
+def test_gated_and_norm_write_only_their_outputs(m2rnn, B, T, N):
+    K, V, C = 64, 16, 16
     g, copies = _inputs(B, T, N, K, V, "bf16", 5, gated=True, norm=True)
     G = Guarded()
     td = g["v"].dtype
@@ -113,10 +114,11 @@ def test_gated_and_norm_write_only_their_outputs(m2rnn):
     gout = {"dq": G((B, T, K)), "dk": G((B, T, K)), "dv": G((B, T, N, V)), "da": G((B, T, N)),
             "dalpha": G((N,)), "dbeta": G((N,)), "dW": G((N, V, V)), "dw_r": G((N, V)),
             "dg": G((B, T, N, V)), "dw_norm": G((N, V)), "dH0": G((B, N, K, V))}
-    m2rnn.bwd_norm(g["q"], g["k"], g["v"], None, g["W"], g["w_r"], g["g"], g["w_norm"], r["y"],
-                   r["rstd"], g["dy"], ckpt=r["ckpt"], gate=gate, ckpt_every=C, want_dH0=True,
-                   out=gout)
-    G.check("bwd_norm gated")
+    for ckpt in (r["ckpt"], None):  # given, and recomputed (a checkpoint-only forward)
+        m2rnn.bwd_norm(g["q"], g["k"], g["v"], None, g["W"], g["w_r"], g["g"], g["w_norm"],
+                       r["y"], r["rstd"], g["dy"], ckpt=ckpt, gate=gate, ckpt_every=C,
+                       want_dH0=True, out=gout)
+        G.check(f"bwd_norm gated ckpt={'given' if ckpt is not None else 'recomputed'}")
     gg = {"dq": G((B, T, K)), "dk": G((B, T, K)), "dv": G((B, T, N, V)), "da": G((B, T, N)),
           "dalpha": G((N,)), "dbeta": G((N,)), "dW": G((N, V, V)), "dw_r": G((N, V))}
     m2rnn.bwd_gated(g["q"], g["k"], g["v"], *gate, g["W"], g["w_r"], g["dy"], ckpt=r["ckpt"],
