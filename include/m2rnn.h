@@ -258,9 +258,12 @@ int m2rnn_set_wait_limit_ns(long long limit_ns);
  *     refused with M2RNN_ERR_WORKSPACE before any device work.
  *   - Every GPU that loads this part of the library holds the buffer until
  *     the process exits.
+ *   - Shape and argument errors are refused on the host before any CUDA
+ *     call.
  *   - The first call on a device looks up the buffer's device address on
  *     that device (which must be current); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is kept for the life of the process; do
+ *     not use the library on a device again after a cudaDeviceReset of it.
  *   - All calls share the buffer and it keeps the last call's contents;
  *     nothing in it needs to start at zero (the forward recomputation writes
  *     every checkpoint the backward reads).  Calls that overlap on the GPU

@@ -72,7 +72,12 @@ int check_ptr(const void* p, int dev, bool required) {
 // Query/key groups of a shape (0 is read as 1).
 int groups(const m2rnn_shape* s) { return s->Nq == 0 ? 1 : s->Nq; }
 
-int check_shape(const m2rnn_shape* s) {
+int check_shape(const m2rnn_shape* s) { return m2rnn::validate_shape(s); }
+
+}  // namespace
+
+namespace m2rnn {
+int validate_shape(const m2rnn_shape* s) {
   if (s == nullptr) return M2RNN_ERR_INVALID_ARG;
   if (s->B < 1 || s->N < 1 || s->T < 0 || s->ckpt_every < 0) return M2RNN_ERR_INVALID_ARG;
   if (s->Nq < 0 || s->N % groups(s) != 0) return M2RNN_ERR_INVALID_ARG;
@@ -84,6 +89,9 @@ int check_shape(const m2rnn_shape* s) {
   if (static_cast<long long>(s->B) * s->N >= (1LL << 31)) return M2RNN_ERR_UNSUPPORTED_SHAPE;
   return M2RNN_OK;
 }
+}  // namespace m2rnn
+
+namespace {
 
 struct FwdConfig {
   int MT, WPH, G, tc;
@@ -281,6 +289,30 @@ int run_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, c
     p.g = nf->g;
     p.ssq = nf->rstd;
     p.norm = 1;
+  }
+
+  // One-wave kernel: when the heads need more than one wave of the CTAs
+  // planned above (8 heads of two warps per SM) but fit 14 per SM, every head
+  // is made resident at once, G = ceil(B N / SMs) heads per CTA over the
+  // flattened (b, n) order, one warp per head.  M2RNN_FWD_WAVE=0 turns it
+  // off and =1 uses it wherever it applies; M2RNN_FWD_WAVE_G forces G (A/B
+  // measurement and tests).
+  if (!f32 && s->V == 16 && s->K == 64 && nf == nullptr && groups(s) == 1) {
+    const long long heads = static_cast<long long>(s->B) * s->N;
+    int Gw = static_cast<int>((heads + sms - 1) / sms);
+    bool use = heads > 8LL * sms;
+    if (const char* e = std::getenv("M2RNN_FWD_WAVE")) use = e[0] == '1';
+    if (const char* e = std::getenv("M2RNN_FWD_WAVE_G")) Gw = std::atoi(e);
+    if (use && Gw >= 1 && Gw <= m2rnn::fwd_wave_max_heads() && Gw <= s->N) {
+      m2rnn::FwdParams pw = p;
+      pw.G = Gw;
+      pw.WPH = 1;
+      pw.ngroups = 0;
+      int tc = 32;
+      while (tc > 8 && m2rnn::fwd_wave_smem_bytes(64, Gw, tc) > kSmemBudget) tc /= 2;
+      pw.tc = tc;
+      return status_from_cuda(m2rnn::launch_fwd_wave(pw, st));
+    }
   }
 
   // Wave planning.  All CTAs of a launch run equally long, so when the heads

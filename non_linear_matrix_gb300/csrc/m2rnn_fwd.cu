@@ -576,6 +576,32 @@ __device__ __forceinline__ void readout_bf16(const uint32_t (&A)[MT][V / 16][4],
   }
 }
 
+// Z = tanh(acc); H = Z + f (H - Z) for one 16-row slice; then the next
+// step's A operand.  Every forward variant (and the backward's recompute)
+// performs these operations in this order, so the state is the same bit for
+// bit whichever launch shape computed it.
+template <int V, bool F32, bool HALF>
+__device__ __forceinline__ void state_update(float (&H)[V / 8][4], const float (&acc)[V / 8][4],
+                                             float2 f2, uint32_t (&A)[V / 16][4],
+                                             uint32_t (&Al)[V / 16][4]) {
+  const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+  for (int nt = 0; nt < V / 8; ++nt)
+#pragma unroll
+    for (int h = 0; h < (HALF ? 1 : 2); ++h) {
+      float2 z;
+      z.x = F32 ? tanhf(acc[nt][2 * h]) : ptx::tanh_approx(acc[nt][2 * h]);
+      z.y = F32 ? tanhf(acc[nt][2 * h + 1]) : ptx::tanh_approx(acc[nt][2 * h + 1]);
+      const float2 hp = make_float2(H[nt][2 * h], H[nt][2 * h + 1]);
+      const float2 d = __ffma2_rn(m1, z, hp);
+      const float2 hn = __ffma2_rn(f2, d, z);
+      H[nt][2 * h] = hn.x;
+      H[nt][2 * h + 1] = hn.y;
+    }
+  pack_a<V, HALF>(H, A);
+  if (F32) pack_a_lo<V>(H, A, Al);
+}
+
 // Whether a step writes the previous step's readout (bf16, one 16-row slice
 // per warp: the readout's transposes and MMA then fill the latency of the
 // state products) instead of its own (measured slower with two slices per
@@ -645,21 +671,7 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
   };
   // Z = tanh(acc); H = Z + f (H - Z); the next step's A operand
   auto update = [&](int mt, const float (&acc)[NT][4]) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int h = 0; h < (HALF ? 1 : 2); ++h) {
-        float2 z;
-        z.x = F32 ? tanhf(acc[nt][2 * h]) : ptx::tanh_approx(acc[nt][2 * h]);
-        z.y = F32 ? tanhf(acc[nt][2 * h + 1]) : ptx::tanh_approx(acc[nt][2 * h + 1]);
-        const float2 hp = make_float2(S.H[mt][nt][2 * h], S.H[mt][nt][2 * h + 1]);
-        const float2 d = __ffma2_rn(m1, z, hp);
-        const float2 hn = __ffma2_rn(f2, d, z);
-        S.H[mt][nt][2 * h] = hn.x;
-        S.H[mt][nt][2 * h + 1] = hn.y;
-      }
-    pack_a<V, HALF>(S.H[mt], S.A[mt]);
-    if (F32) pack_a_lo<V>(S.H[mt], S.A[mt], S.Al[mt]);
+    state_update<V, F32, HALF>(S.H[mt], acc, f2, S.A[mt], S.Al[mt]);
   };
   if constexpr (DEFER) {
     float acc[MT][NT][4];
@@ -910,6 +922,401 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
   }
 }
 
+// ---------------------------------------------------------------------------
+// One-wave kernel.  When a batch has more heads than one wave of the CTAs
+// above holds (8 heads of two warps each per SM), they run in two waves and
+// each wave pays the latency of every step in full.  This kernel instead
+// keeps all heads resident at once: CTA c takes G = ceil(B N / SMs) heads
+// [c G, c G + G) of the flattened (b, n) order -- at most two batch items,
+// since G <= N -- with one consumer warp per head holding all K rows (KC / 16
+// slices of 16) and storing y itself, and one producer warp that stages q, k
+// (per batch item), v and f.  bf16 inputs, V = 16, N_q = 1.
+// ---------------------------------------------------------------------------
+constexpr int kWaveMaxHeads = 14;
+
+struct WaveLayout {
+  uint32_t q, k;   // [2][TC][K] bf16, one block per batch item of the CTA
+  uint32_t kd;     // [2][TC][K][2] fp32 (k, k) pairs
+  uint32_t v;      // [TC][G][V] bf16
+  uint32_t fd;     // [TC][G][2] fp32 (f, f) pairs
+  uint32_t stage;
+  uint32_t wr;     // [G][V] fp32 w_r of the CTA's heads (outside the ring)
+  uint32_t bars, total;
+};
+
+__host__ __device__ inline WaveLayout wave_layout(int K, int V, int G, int TC) {
+  WaveLayout L;
+  uint32_t o = 0;
+  L.q = o;
+  o = align_up(o + 2 * TC * K * 2, 128);
+  L.k = o;
+  o = align_up(o + 2 * TC * K * 2, 128);
+  L.kd = o;
+  o = align_up(o + 2 * TC * K * 8, 128);
+  L.v = o;
+  o = align_up(o + TC * G * V * 2, 128);
+  L.fd = o;
+  o = align_up(o + TC * G * 8, 128);
+  L.stage = o;
+  L.wr = NSTAGE * L.stage;
+  L.bars = align_up(L.wr + G * V * 4, 128);
+  L.total = L.bars + 8 * 3 * NSTAGE;
+  return L;
+}
+
+// The CTA's heads as up to two runs of consecutive heads: cnt0 heads of
+// batch item b0 from head n0 on, then cnt1 heads of batch item b0 + 1 from
+// head 0 on.
+struct WaveSegs {
+  int b0, n0, cnt0, cnt1, nseg, Geff;
+  __device__ __forceinline__ int b(int sgi) const { return b0 + sgi; }
+  __device__ __forceinline__ int first(int sgi) const { return sgi ? 0 : n0; }
+  __device__ __forceinline__ int cnt(int sgi) const { return sgi ? cnt1 : cnt0; }
+  __device__ __forceinline__ int offset(int sgi) const { return sgi ? cnt0 : 0; }
+};
+
+__device__ __forceinline__ WaveSegs wave_segs(const FwdParams& p) {
+  WaveSegs sg;
+  const long long h0 = static_cast<long long>(blockIdx.x) * p.G;
+  const long long total = static_cast<long long>(p.B) * p.N;
+  sg.Geff = static_cast<int>(min(static_cast<long long>(p.G), total - h0));
+  sg.b0 = static_cast<int>(h0 / p.N);
+  sg.n0 = static_cast<int>(h0 - static_cast<long long>(sg.b0) * p.N);
+  sg.cnt0 = min(sg.Geff, p.N - sg.n0);
+  sg.cnt1 = sg.Geff - sg.cnt0;
+  sg.nseg = sg.cnt1 > 0 ? 2 : 1;
+  return sg;
+}
+
+template <bool GATED>
+__device__ __forceinline__ void wave_producer(const FwdParams& p, const WaveLayout& L, uint32_t sbase,
+                                              const WaveSegs& sg) {
+  using TIn = __nv_bfloat16;
+  constexpr int es = 2, V = 16;
+  const int lane = threadIdx.x & 31;
+  const int K = p.K, T = p.T, N = p.N, G = p.G, TC = p.tc;
+  const uint32_t bars = sbase + L.bars;
+  const int nchunks = (T + TC - 1) / TC;
+  const TIn* q = static_cast<const TIn*>(p.q);
+  const TIn* k = static_cast<const TIn*>(p.k);
+  const TIn* v = static_cast<const TIn*>(p.v);
+  const TIn* f = static_cast<const TIn*>(GATED ? p.a : p.f);
+  const TIn* galpha = static_cast<const TIn*>(p.alpha);
+  const TIn* gbeta = static_cast<const TIn*>(p.beta);
+  const size_t qk_ext = static_cast<size_t>(p.B) * T * K;
+  const size_t v_ext = static_cast<size_t>(p.B) * T * N * V, f_ext = static_cast<size_t>(p.B) * T * N;
+
+  auto issue = [&](int ch) -> bool {
+    const int s = ch % NSTAGE;
+    if (!warp_wait(bar_in_empty(bars, s), ((ch / NSTAGE) & 1) ^ 1, p.wait_limit_ns)) return false;
+    const int t0 = ch * TC;
+    const int Tc = min(TC, T - t0);
+    const uint32_t qk_bytes = static_cast<uint32_t>(Tc * K * es);
+    const uint32_t raw = bar_raw_full(bars, s);
+    if (lane == 0)
+      ptx::mbar_expect_tx(raw, static_cast<uint32_t>(sg.nseg) * 2 * qk_bytes +
+                                   static_cast<uint32_t>(Tc * sg.Geff * V * es));
+    __syncwarp();
+    const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
+    for (int sgi = 0; sgi < sg.nseg; ++sgi) {
+      const size_t bt0 = static_cast<size_t>(sg.b(sgi)) * T + t0;
+      if (lane == 0) {
+        const uint32_t off = static_cast<uint32_t>(sgi * TC * K * es);
+        if (in_range(p.status, bt0 * K, static_cast<size_t>(Tc) * K, qk_ext, CHK_FWD_QK)) {
+          ptx::bulk_g2s(st + L.q + off, q + bt0 * K, qk_bytes, raw);
+          ptx::bulk_g2s(st + L.k + off, k + bt0 * K, qk_bytes, raw);
+        } else {
+          ptx::mbar_complete_tx(raw, 2 * qk_bytes);
+        }
+      }
+      // this batch item's heads of every step: one contiguous run of v
+      const uint32_t v_bytes = static_cast<uint32_t>(sg.cnt(sgi) * V * es);
+      const uint32_t v_off = static_cast<uint32_t>(sg.offset(sgi) * V * es);
+      for (int tl = lane; tl < Tc; tl += 32) {
+        const size_t src = ((bt0 + tl) * N + sg.first(sgi)) * V;
+        if (in_range(p.status, src, static_cast<size_t>(sg.cnt(sgi)) * V, v_ext, CHK_FWD_V))
+          ptx::bulk_g2s(st + L.v + static_cast<uint32_t>(tl * G * V * es) + v_off, v + src, v_bytes, raw);
+        else
+          ptx::mbar_complete_tx(raw, v_bytes);
+      }
+    }
+    // f (or, gated, f from a) -> fp32 pairs [TC][G][2]; loads batched
+    const int Geff = sg.Geff, nf = Tc * Geff;
+    for (int base = 0; base < nf; base += 256) {
+      float fv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = base + lane + 32 * i;
+        const int tl = e / Geff, h = e - tl * Geff;
+        const int sgi = h < sg.cnt0 ? 0 : 1;
+        const int n = sgi ? h - sg.cnt0 : sg.n0 + h;
+        const size_t fi = (static_cast<size_t>(sg.b(sgi)) * T + t0 + tl) * N + n;
+        const bool use = e < nf && in_range(p.status, fi, 1, f_ext, CHK_FWD_F);
+        if constexpr (GATED)
+          fv[i] = use && in_range(p.status, n, 1, N, CHK_FWD_PARAM)
+                      ? gate_f(to_f(f[fi]), to_f(galpha[n]), to_f(gbeta[n]))
+                      : 0.f;
+        else
+          fv[i] = use ? to_f(f[fi]) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = base + lane + 32 * i;
+        const int tl = e / Geff, h = e - tl * Geff;
+        if (e < nf) ptx::sts_f32x2(st + L.fd + static_cast<uint32_t>((tl * G + h) * 8), fv[i], fv[i]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(raw);
+    return true;
+  };
+
+  // k of each batch item as fp32 (k, k) pairs, then the chunk is released
+  auto convert = [&](int ch) -> bool {
+    const int s = ch % NSTAGE;
+    if (!warp_wait(bar_raw_full(bars, s), (ch / NSTAGE) & 1, p.wait_limit_ns)) return false;
+    const int Tc = min(TC, T - ch * TC);
+    const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
+    const int n8 = Tc * K / 8;
+    for (int sgi = 0; sgi < sg.nseg; ++sgi) {
+      const uint32_t src = st + L.k + static_cast<uint32_t>(sgi * TC * K * es);
+      const uint32_t dst = st + L.kd + static_cast<uint32_t>(sgi * TC * K * 8);
+      for (int i = lane; i < n8; i += 32) {
+        const uint4 u = ptx::lds_u32x4(src + 16 * i);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = ptx::bf16x2_lo(w[j]), hi = ptx::bf16x2_hi(w[j]);
+          ptx::sts_f32x4(dst + 64 * i + 16 * j, lo, lo, hi, hi);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar_in_full(bars, s));
+    return true;
+  };
+
+  int issued = 0, converted = 0;
+  bool ok = true;
+  for (int ch = 0; ch < nchunks; ++ch) {
+    if (!(ok = issue(ch))) break;
+    issued = ch + 1;
+    if (ch >= 1) {
+      if (!(ok = convert(ch - 1))) break;
+      converted = ch;
+    }
+  }
+  if (ok && nchunks > 0) {
+    if ((ok = convert(nchunks - 1))) converted = nchunks;
+  }
+  if (!ok && lane == 0) record_timeout(p.status, SITE_FWD_PRODUCER);
+  for (int ch = max(converted, issued - NSTAGE); ch < issued; ++ch) {
+    if (!warp_wait(bar_raw_full(bars, ch % NSTAGE), (ch / NSTAGE) & 1, kDrainLimitNs)) {
+      if (lane == 0) record_timeout(p.status, SITE_FWD_DRAIN);
+      break;
+    }
+  }
+}
+
+// One step of the one-wave kernel's consumer warp (all MT slices of one
+// head): the rank-1 term from the step's fp32 (k, k) pairs, H W on the
+// tensor core, the shared state update, the readout q^T H on the tensor
+// core and y = q^T H + w_r (.) v stored as bf16 to ydst (nullptr: none).
+// The operations per element are those of fwd_step.
+template <int MT>
+__device__ __forceinline__ void wave_step(WarpState<16, MT>& S, uint32_t kdb, uint32_t vb,
+                                          uint32_t qb, uint32_t fdaddr, uint32_t wraddr,
+                                          __nv_bfloat16* ydst, int g, int c) {
+  constexpr int NT = 2;
+  const float2 f2 = ptx::lds_f32x2(fdaddr);
+  uint32_t vraw[NT];
+  float2 vv[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    vraw[nt] = ptx::lds_u32(vb + 2 * (8 * nt + 2 * c));
+    vv[nt] = make_float2(ptx::bf16x2_lo(vraw[nt]), ptx::bf16x2_hi(vraw[nt]));
+  }
+  float ya[NT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const float2 k0 = ptx::lds_f32x2(kdb + 8 * (16 * mt + g));
+    const float2 k1 = ptx::lds_f32x2(kdb + 8 * (16 * mt + 8 + g));
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float2 lo = __fmul2_rn(k0, vv[nt]);
+      const float2 hi = __fmul2_rn(k1, vv[nt]);
+      acc[nt][0] = lo.x;
+      acc[nt][1] = lo.y;
+      acc[nt][2] = hi.x;
+      acc[nt][3] = hi.y;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) ptx::mma_bf16_16816(acc[nt], S.A[mt][0], S.Bw[0][nt][0], S.Bw[0][nt][1]);
+    state_update<16, false, false>(S.H[mt], acc, f2, S.A[mt], S.Al[mt]);
+    const uint32_t q0 = ptx::lds_u32(qb + 2 * (16 * mt + 2 * c));
+    const uint32_t q1 = ptx::lds_u32(qb + 2 * (16 * mt + 8 + 2 * c));
+    const uint32_t Aq[4] = {q0, q0, q1, q1};
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const uint32_t b0 = ptx::movmatrix_trans(S.A[mt][0][2 * h2]);
+      const uint32_t b1 = ptx::movmatrix_trans(S.A[mt][0][2 * h2 + 1]);
+      if (mt == 0)
+        ptx::mma_bf16_16816_zero(ya[h2], Aq, b0, b1);
+      else
+        ptx::mma_bf16_16816(ya[h2], Aq, b0, b1);
+    }
+  }
+  if (g == 0 && ydst != nullptr) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float2 wr2 = ptx::lds_f32x2(wraddr + 4 * (8 * nt + 2 * c));
+      const float2 o = __ffma2_rn(wr2, vv[nt], make_float2(ya[nt][0], ya[nt][1]));
+      *reinterpret_cast<uint32_t*>(ydst + 8 * nt + 2 * c) = ptx::pack_bf16x2(o.x, o.y);
+    }
+  }
+}
+
+template <int KC>
+__device__ __forceinline__ void wave_consumer(const FwdParams& p, const WaveLayout& L, uint32_t sbase,
+                                              const WaveSegs& sg, int hl) {
+  using TIn = __nv_bfloat16;
+  constexpr int V = 16, MT = KC / 16, NT = V / 8, KS = V / 16, es = 2;
+  constexpr int K = KC;
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int T = p.T, N = p.N, G = p.G, TC = p.tc;
+  const int sgi = hl < sg.cnt0 ? 0 : 1;
+  const int b = sg.b(sgi), n = sgi ? hl - sg.cnt0 : sg.n0 + hl;
+  const uint32_t bars = sbase + L.bars;
+
+  WarpState<V, MT> S;
+  const TIn* Wn = static_cast<const TIn*>(p.W) + static_cast<size_t>(n) * V * V;
+  const bool w_ok = in_range(p.status, static_cast<size_t>(n) * V * V, V * V,
+                             static_cast<size_t>(N) * V * V, CHK_FWD_PARAM);
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r0 = 16 * ks + 8 * h + 2 * c, col = 8 * nt + g;
+        const float w0 = w_ok ? to_f(Wn[r0 * V + col]) : 0.f;
+        const float w1 = w_ok ? to_f(Wn[(r0 + 1) * V + col]) : 0.f;
+        S.Bw[ks][nt][h] = ptx::pack_bf16x2(w0, w1);
+        S.Bwl[ks][nt][h] = 0u;
+      }
+  // w_r of this head as fp32 in this warp's shared-memory slot
+  const uint32_t wraddr = sbase + L.wr + static_cast<uint32_t>(hl * V * 4);
+  if (lane < V) {
+    const size_t o = static_cast<size_t>(n) * V + lane;
+    ptx::sts_f32(wraddr + 4 * lane,
+                 in_range(p.status, o, 1, static_cast<size_t>(N) * V, CHK_FWD_PARAM)
+                     ? to_f(static_cast<const TIn*>(p.w_r)[o])
+                     : 0.f);
+  }
+  __syncwarp();
+  const size_t hoff = (static_cast<size_t>(b) * N + n) * K * V;
+  const size_t h_ext = static_cast<size_t>(p.B) * N * K * V;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = 16 * mt + g + 8 * (r >> 1), col = 8 * nt + 2 * c + (r & 1);
+        const size_t o = hoff + row * V + col;
+        S.H[mt][nt][r] = (p.H0 && in_range(p.status, o, 1, h_ext, CHK_FWD_H0)) ? p.H0[o] : 0.f;
+      }
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) pack_a<V, false>(S.H[mt], S.A[mt]);
+
+  float* ckpt = p.ckpt ? p.ckpt + (static_cast<size_t>(b) * N + n) * p.nck * K * V : nullptr;
+  size_t ck_off = (static_cast<size_t>(b) * N + n) * p.nck * K * V;
+  const size_t ck_ext = static_cast<size_t>(p.B) * N * p.nck * K * V;
+  int next_ck = ckpt != nullptr ? 0 : T + 1;
+  // y of this head: row t at y_head + t N V (no y in checkpoint-only runs)
+  TIn* y_head = p.y ? static_cast<TIn*>(p.y) + (static_cast<size_t>(b) * T * N + n) * V : nullptr;
+#if M2RNN_CHECK
+  if (y_head != nullptr &&
+      !in_range(p.status, (static_cast<size_t>(b) * T * N + n) * V + static_cast<size_t>(T - 1) * N * V,
+                V, static_cast<size_t>(p.B) * T * N * V, CHK_FWD_Y))
+    y_head = nullptr;  // (checked build: the head's last row would be out of range)
+#endif
+  const size_t y_step = static_cast<size_t>(N) * V;
+  const int nchunks = (T + TC - 1) / TC;
+  constexpr uint32_t q_stride = K * es, kd_stride = K * 8;
+  const uint32_t v_stride = static_cast<uint32_t>(G * V * es);
+  const uint32_t fd_stride = static_cast<uint32_t>(G * 8);
+  bool ok = true;
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const int s = ch % NSTAGE;
+    if (!warp_wait(bar_in_full(bars, s), (ch / NSTAGE) & 1, p.wait_limit_ns)) {
+      ok = false;
+      break;
+    }
+    const int t0 = ch * TC;
+    const int Tc = min(TC, T - t0);
+    const uint32_t st = sbase + static_cast<uint32_t>(s) * L.stage;
+    const uint32_t qb = st + L.q + static_cast<uint32_t>(sgi * TC * K * es);
+    const uint32_t kdb = st + L.kd + static_cast<uint32_t>(sgi * TC * K * 8);
+    const uint32_t vb = st + L.v + static_cast<uint32_t>(hl * V * es);
+    const uint32_t fdb = st + L.fd + static_cast<uint32_t>(hl * 8);
+    TIn* yt = y_head != nullptr ? y_head + static_cast<size_t>(t0) * y_step : nullptr;
+    int tl = 0;
+    while (tl < Tc) {
+      if (t0 + tl == next_ck) {
+        store_state<V, MT, false>(ckpt, S.H, 0, g, c, p.status, ck_off, ck_ext, CHK_FWD_CKPT);
+        ckpt += K * V;
+        ck_off += static_cast<size_t>(K) * V;
+        next_ck += p.C;
+      }
+      const int seg_end = min(Tc, next_ck - t0);
+#pragma unroll 2
+      for (; tl < seg_end; ++tl) {
+        const uint32_t u = static_cast<uint32_t>(tl);
+        wave_step<MT>(S, kdb + u * kd_stride, vb + u * v_stride, qb + u * q_stride, fdb + u * fd_stride,
+                      wraddr, yt, g, c);
+        if (yt != nullptr) yt += y_step;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar_in_empty(bars, s));
+  }
+  if (!ok) {
+    if (lane == 0) record_timeout(p.status, SITE_FWD_CONSUMER);
+    return;
+  }
+  if (p.HT != nullptr)
+    store_state<V, MT, false>(p.HT + hoff, S.H, 0, g, c, p.status, hoff, h_ext, CHK_FWD_HT);
+}
+
+template <bool GATED, int KC>
+__global__ void __launch_bounds__(32 * (1 + kWaveMaxHeads), 1) fwd_wave_kernel(const FwdParams prm) {
+  FwdParams p = prm;
+  p.K = KC;
+  p.WPH = 1;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5;
+  const WaveSegs sg = wave_segs(p);
+  const WaveLayout L = wave_layout(KC, 16, p.G, p.tc);
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const uint32_t bars = sbase + L.bars;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      ptx::mbar_init(bar_raw_full(bars, s), 1);
+      ptx::mbar_init(bar_in_full(bars, s), 1);
+      ptx::mbar_init(bar_in_empty(bars, s), sg.Geff);
+    }
+    ptx::mbar_init_fence();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    if (p.inject_stall == 0) wave_producer<GATED>(p, L, sbase, sg);
+  } else if (warp - 1 < sg.Geff) {
+    wave_consumer<KC>(p, L, sbase, sg, warp - 1);
+  }
+}
+
 // The kernel instance for p (fused gate, readout epilogue, compile-time K
 // and heads per CTA), with the rank1_pairs choice it was compiled with (the
 // launch's shared-memory layout depends on it).
@@ -970,6 +1377,25 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+int fwd_wave_max_heads() { return kWaveMaxHeads; }
+
+size_t fwd_wave_smem_bytes(int K, int G, int tc) { return wave_layout(K, 16, G, tc).total; }
+
+cudaError_t launch_fwd_wave(const FwdParams& p, cudaStream_t stream) {
+  if (p.K != 64 || p.G < 1 || p.G > kWaveMaxHeads || p.G > p.N || p.Nq != 1 || p.norm != 0 ||
+      p.tc < 2 || p.tc > 32)
+    return cudaErrorInvalidValue;
+  const WaveLayout L = wave_layout(64, 16, p.G, p.tc);
+  auto kern = p.gated ? fwd_wave_kernel<true, 64> : fwd_wave_kernel<false, 64>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(L.total));
+  if (e != cudaSuccess) return e;
+  const long long heads = static_cast<long long>(p.B) * p.N;
+  const unsigned grid = static_cast<unsigned>((heads + p.G - 1) / p.G);
+  kern<<<grid, 32 * (1 + p.G), L.total, stream>>>(p);
+  return cudaGetLastError();
+}
 
 // (with k's fp32 pairs: an upper bound for the planner)
 size_t fwd_smem_bytes(int K, int V, int G, int WPH, bool f32_inputs, int tc) {

@@ -5,7 +5,13 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "m2rnn.h"
+
 namespace m2rnn {
+
+// Host-side validation of a shape (the checks every entry point starts
+// with): M2RNN_OK or the status to return.  Makes no CUDA call.
+int validate_shape(const m2rnn_shape* s);
 
 // Device status word: [0] = first recorded m2rnn_status (0 = OK),
 // [1] = location code of the wait that gave up.
@@ -189,5 +195,12 @@ int fwd_ctas_per_sm(const FwdParams& p, int V, bool f32_inputs, int MT);
 
 // Dynamic shared memory bytes the forward kernel needs.
 size_t fwd_smem_bytes(int K, int V, int G, int WPH, bool f32_inputs, int tc);
+
+// One-wave forward kernel (bf16, K = 64, V = 16, N_q = 1, no readout
+// epilogue): p.G heads per CTA over the flattened (b, n) order, G <= N and
+// G <= fwd_wave_max_heads(), one warp per head.
+int fwd_wave_max_heads();
+size_t fwd_wave_smem_bytes(int K, int G, int tc);
+cudaError_t launch_fwd_wave(const FwdParams& p, cudaStream_t stream);
 
 }  // namespace m2rnn

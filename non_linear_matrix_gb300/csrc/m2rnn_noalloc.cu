@@ -14,13 +14,16 @@
 // library holds it until the process exits.  Host code must not use the
 // array's name as a device address (in host code it is only a stand-in); the
 // device address is obtained once per device with cudaGetSymbolAddress,
-// with that device current, on the first call made on that device.
+// with that device current, on the first call made on that device, and kept
+// for the life of the process (a cudaDeviceReset of that device would make
+// it stale: the library must not be used on a device again after a reset).
 #include <cuda_runtime.h>
 
 #include <cstddef>
 #include <mutex>
 
 #include "m2rnn.h"
+#include "m2rnn_internal.h"
 
 namespace {
 
@@ -57,9 +60,13 @@ int m2rnn_bwd_noalloc(const m2rnn_shape* s, const void* q, const void* k, const 
                       const void* f, const void* W, const void* w_r, const float* H0,
                       const void* dy, const float* dH_T, float* dq, float* dk, float* dv,
                       float* df, float* dW, float* dw_r, float* dH0, void* stream) {
-  if (s == nullptr) return M2RNN_ERR_INVALID_ARG;
+  // Host-side checks first, so that a bad argument is refused before any
+  // CUDA call (the scratch set-up below may load the module on the device).
+  const int rc = m2rnn::validate_shape(s);
+  if (rc != M2RNN_OK) return rc;
+  if (s->ckpt_every <= 0) return M2RNN_ERR_INVALID_ARG;
   // Checkpoints are recomputed into the built-in buffer: refuse problems
-  // whose checkpoints do not fit, before touching the device.
+  // whose checkpoints do not fit.
   const size_t need = m2rnn_bwd_workspace_size(s, 0);
   if (need > kNoAllocScratchBytes) return M2RNN_ERR_WORKSPACE;
   void* scratch = scratch_on_current_device();

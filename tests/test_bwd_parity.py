@@ -70,15 +70,16 @@ def _np64(t):
     return t.detach().cpu().double().numpy()
 
 
-def _restart_parity(m2rnn, oracle_mod, x, C, H0=None, dHT=None, give_ckpt=True, label=""):
-    """Oracle restarted per checkpoint interval from the GPU checkpoint, with
-    the GPU's dckpt of the next interval (or dH_T) as incoming gradient."""
-    gr, ck = _run(m2rnn, x, C, H0, dHT, give_ckpt, with_ckpt=True)
+def _restart_ref(oracle_mod, x, ckn, dckn, C, dHT=None, W=None):
+    """The oracle restarted every interval of C steps from the GPU's
+    checkpoint ckn, with the GPU's gradient of the next checkpoint (dckn, or
+    dH_T after the last) as incoming state gradient.  W replaces x["W"]
+    (sensitivity runs)."""
     q, k, v, f, dy = (x[n] for n in ("q", "k", "v", "f", "dy"))
-    B, T, K = q.shape[0], q.shape[1], q.shape[-1]  # q: [B,T,K] or grouped [B,T,Nq,K]
-    N, V = v.shape[2], v.shape[3]
+    W = x["W"] if W is None else W
+    B, T = q.shape[0], q.shape[1]  # q: [B,T,K] or grouped [B,T,Nq,K]
+    N, V, K = v.shape[2], v.shape[3], ckn.shape[3]
     nck = -(-T // C)
-    ckn, dckn = _np64(ck), _np64(gr["dckpt"])
     last = np.zeros((B, N, 1, K, V)) if dHT is None else dHT.double().numpy()[:, :, None]
     nxt = np.concatenate([dckn[:, :, 1:], last], axis=2)
     ref = {"dq": np.zeros(q.shape), "dk": np.zeros(q.shape), "dv": np.zeros((B, T, N, V)),
@@ -96,7 +97,7 @@ def _restart_parity(m2rnn, oracle_mod, x, C, H0=None, dHT=None, give_ckpt=True, 
 
         def per(a):  # [B, N, nck, K, V][:, :, c0:c1] -> [B*nb, N, K, V]
             return np.ascontiguousarray(np.moveaxis(a[:, :, c0:c1], 2, 1)).reshape(B * nb, N, K, V)
-        r = oracle_mod.bwd(split(q), split(k), split(v), split(f), x["W"], x["w_r"], split(dy),
+        r = oracle_mod.bwd(split(q), split(k), split(v), split(f), W, x["w_r"], split(dy),
                            H0=per(ckn), dHT=per(nxt))
         ref["dq"][:, t0:t1] = r["dq"].reshape(B, nb * L, *q.shape[2:])
         ref["dk"][:, t0:t1] = r["dk"].reshape(B, nb * L, *q.shape[2:])
@@ -105,10 +106,44 @@ def _restart_parity(m2rnn, oracle_mod, x, C, H0=None, dHT=None, give_ckpt=True, 
         ref["dW"] += r["dW"]
         ref["dw_r"] += r["dw_r"]
         ref["dckpt"][:, :, c0:c1] = np.moveaxis(r["dH0"].reshape(B, nb, N, K, V), 1, 2)
-    errs = {n: _rel(gr[n], ref[n]) for n in ref}
-    errs["dH0"] = _rel(gr["dH0"], ref["dckpt"][:, :, 0])
-    assert max(errs.values()) <= TOL, (label, errs)
-    return errs
+    ref["dH0"] = ref["dckpt"][:, :, 0]
+    return ref
+
+
+# Relative size of the random perturbation of W that stands in for the GPU
+# path's own rounding when a draw's conditioning is measured: one bf16 ulp
+# (2^-8, twice the unit roundoff).  The bf16-operand path rounds H to bf16 in
+# H W at every step (up to 2^-9 relative) and, beside it, approximates tanh
+# (about 2^-11) and rounds e = H_{t-1} - Z and D for the parameter products;
+# one ulp covers their combination.  For fp32 operands, carried as bf16
+# hi + lo pairs, one ulp of that pair (2^-16).
+SENS_U = {"bf16": 2.0 ** -8, "f32": 2.0 ** -16}
+
+
+def _restart_parity(m2rnn, oracle_mod, x, C, H0=None, dHT=None, give_ckpt=True, label="",
+                    sens=None):
+    """Oracle restarted per checkpoint interval from the GPU checkpoint, with
+    the GPU's dckpt of the next interval (or dH_T) as incoming gradient.
+
+    sens = "bf16" or "f32": the bound of each gradient is also derived from
+    this draw's own conditioning, max(TOL, kappa) with kappa the oracle's
+    relative change of that gradient (same restarts) when W is perturbed
+    elementwise by a random relative SENS_U[sens]; returns (errs, kappa)."""
+    gr, ck = _run(m2rnn, x, C, H0, dHT, give_ckpt, with_ckpt=True)
+    ckn, dckn = _np64(ck), _np64(gr["dckpt"])
+    ref = _restart_ref(oracle_mod, x, ckn, dckn, C, dHT)
+    errs = {n: _rel(gr[n], ref[n]) for n in NAMES + ("dckpt", "dH0")}
+    if sens is None:
+        assert max(errs.values()) <= TOL, (label, errs)
+        return errs
+    W = x["W"].double().numpy()
+    z = np.random.default_rng(2024).standard_normal(W.shape)
+    alt = _restart_ref(oracle_mod, x, ckn, dckn, C, dHT, W=W * (1.0 + SENS_U[sens] * z))
+    kappa = {n: _rel(alt[n], ref[n]) for n in errs}
+    print(label, {n: (round(errs[n], 5), round(kappa[n], 5)) for n in errs})
+    bad = {n: (errs[n], kappa[n]) for n in errs if errs[n] > max(TOL, kappa[n])}
+    assert not bad, (label, "error above max(1e-2, own sensitivity)", bad, errs, kappa)
+    return errs, kappa
 
 
 def _compare(m2rnn, oracle_mod, x, C, H0=None, dHT=None, give_ckpt=True, label=""):
@@ -227,39 +262,47 @@ def test_kernel_variants(m2rnn, oracle_mod, monkeypatch, kernel, dtype, T, C):
     _restart_parity(m2rnn, oracle_mod, x, C, H0=H0, dHT=dHT, label=f"kernel{kernel} {dtype} T{T} C{C}")
 
 
+SEEDS = [600, 601, 602, 603, 604]
+
+
+@pytest.mark.parametrize("seed", SEEDS)
 @pytest.mark.parametrize("wpc", ["1", "2", "4"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_pipelined_warps_per_cta(m2rnn, oracle_mod, monkeypatch, wpc, dtype):
+def test_pipelined_warps_per_cta(m2rnn, oracle_mod, monkeypatch, wpc, dtype, seed):
     """The pipelined kernel with 1, 2 and 4 warps per CTA (K = 64 split
     into 4, 2 or 1 row slices per head), ragged last interval, the same
-    inputs for every width.  (Some draws of these distributions are chaotic
-    enough that the oracle's own whole-sequence df moves by 3-44 % under a
-    1e-3-4e-3 relative perturbation of W -- seed 604 is one -- and then even
-    32-step restarts leave tanh-approximation differences near the 1 %
-    bound; this draw moves by 0.15 %.)"""
+    inputs for every width, on five draws of the input distributions.  Some
+    draws are ill-conditioned even over 32-step restarts (heads with
+    ||W||_2 > 1 in a transient unstable window); each gradient must stay
+    within max(1e-2, the oracle's own change under a one-ulp
+    perturbation of W on that draw)."""
     monkeypatch.setenv("M2RNN_BWD_KERNEL", "1")
     monkeypatch.setenv("M2RNN_BWD_WPC", wpc)
-    x = make_inputs(2, 150, 3, 64, 16, dtype, 600, with_dy=True)
+    x = make_inputs(2, 150, 3, 64, 16, dtype, seed, with_dy=True)
     gen = torch.Generator().manual_seed(11)
     H0 = torch.rand(2, 3, 64, 16, generator=gen) - 0.5
     dHT = torch.randn(2, 3, 64, 16, generator=gen)
-    _restart_parity(m2rnn, oracle_mod, x, 32, H0=H0, dHT=dHT, label=f"wpc{wpc} {dtype}")
+    _restart_parity(m2rnn, oracle_mod, x, 32, H0=H0, dHT=dHT, sens=dtype,
+                    label=f"wpc{wpc} {dtype} seed{seed}")
 
 
+@pytest.mark.parametrize("seed", SEEDS)
 @pytest.mark.parametrize("wpc,dtype,V", [("1", "bf16", 16), ("2", "bf16", 16), ("1", "f32", 16),
                                           ("2", "f32", 16), ("1", "bf16", 32), ("2", "f32", 32)])
-def test_serial_warps_per_cta(m2rnn, oracle_mod, monkeypatch, wpc, dtype, V):
+def test_serial_warps_per_cta(m2rnn, oracle_mod, monkeypatch, wpc, dtype, V, seed):
     """The serial kernel with 1 and 2 warps per CTA (4 or 2 row slices per
     head, cross-slice atomic sums of dv and df).  The automatic choice takes
     it at large batches, where it fits more CTAs per SM than the pipelined
-    kernel; here it is forced on the same inputs as the pipelined test."""
+    kernel; here it is forced on the pipelined test's draws, with the same
+    per-draw bounds."""
     monkeypatch.setenv("M2RNN_BWD_KERNEL", "0")
     monkeypatch.setenv("M2RNN_BWD_WPC", wpc)
-    x = make_inputs(2, 150, 3, 64, V, dtype, 600, with_dy=True)
+    x = make_inputs(2, 150, 3, 64, V, dtype, seed, with_dy=True)
     gen = torch.Generator().manual_seed(11)
     H0 = torch.rand(2, 3, 64, V, generator=gen) - 0.5
     dHT = torch.randn(2, 3, 64, V, generator=gen)
-    _restart_parity(m2rnn, oracle_mod, x, 32, H0=H0, dHT=dHT, label=f"serial wpc{wpc} {dtype} V{V}")
+    _restart_parity(m2rnn, oracle_mod, x, 32, H0=H0, dHT=dHT, sens=dtype,
+                    label=f"serial wpc{wpc} {dtype} V{V} seed{seed}")
 
 
 @pytest.mark.parametrize("kernel", ["0", "1"])

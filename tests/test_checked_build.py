@@ -116,6 +116,28 @@ def test_bwd_kernels_checked(m2rnn, monkeypatch, kernel, wpc):
     _same(r, q, atomic=("dq", "dk", "dW", "dw_r", "dv", "df"))
 
 
+@pytest.mark.parametrize("G,gated", [("4", False), ("5", True)])
+def test_wave_kernel_checked(m2rnn, monkeypatch, G, gated):
+    """The one-wave forward kernel (CTAs across two batch items), plain and
+    with the fused gate, under both builds."""
+    monkeypatch.setenv("M2RNN_FWD_WAVE", "1")
+    monkeypatch.setenv("M2RNN_FWD_WAVE_G", G)
+    g = _dev(make_inputs(5, 77, 6, 64, 16, "bf16", 77, gated=gated))
+    H0 = (torch.rand(5, 6, 64, 16, generator=torch.Generator().manual_seed(2)) - 0.5).cuda()
+
+    def fwd():
+        if gated:
+            y, HT, ck = m2rnn.fwd_gated(g["q"], g["k"], g["v"], g["a"], g["alpha"], g["beta"],
+                                        g["W"], g["w_r"], H0, ckpt_every=24)
+        else:
+            y, HT, ck = m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], H0,
+                                  ckpt_every=24)
+        return {"y": y, "HT": HT, "ckpt": ck}
+
+    ref, got = _both(m2rnn, fwd)
+    _same(ref, got)
+
+
 def test_gated_norm_noalloc_checked(m2rnn):
     B, T, N, K, V, C = 3, 45, 6, 64, 16, 16
     g = _dev(make_inputs(B, T, N, K, V, "bf16", 5, with_dy=True, gated=True, norm=True))

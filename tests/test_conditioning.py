@@ -1,0 +1,166 @@
+"""The conditioning record (tests/golden/conditioning.json) against the
+oracle, and against what the mathematics of Eqs. (10)-(12) fixes.
+
+The record (written by tests/golden/make_conditioning.py, which calls only
+the oracle) holds, per head of the benchmarked workloads, the step from which
+the fp64 oracle itself departs from its own trajectory under a 1e-7 relative
+perturbation of v (its divergence horizon), the sensitivity of the
+horizon-restricted gradients, and the cancellation and sensitivity of the
+fused gate's parameter gradients.  The GPU parity tests use these numbers to
+decide which steps a finite-precision implementation can be held to along
+the whole trajectory.  These tests check that the stored numbers are what the
+oracle computes (recomputed on a subset of heads, exactly: the oracle is
+deterministic), and that the divergences obey a bound the recurrence must
+satisfy, so that a wrong record or a wrong oracle shows up here.
+
+The bound.  Row r of the state (1 x V) follows
+    h_t = f_t h_{t-1} + (1 - f_t) tanh(h_{t-1} W + k_{t,r} v_t).
+For two input sequences v, v' and e_t = ||h_t - h'_t||_2, |tanh a - tanh a'|
+<= |a - a'| elementwise gives
+    e_t <= (f_t + (1 - f_t) rho) e_{t-1} + (1 - f_t) |k_{t,r}| ||v_t - v'_t||_2
+with rho = ||W||_2.  If rho < 1, induction from e_0 = 0 gives
+e_t <= M_r / (1 - rho), M_r = max_t |k_{t,r}| ||v_t - v'_t||_2, and then
+    |y_t - y'_t|_inf <= ||q_t||_2 sqrt(sum_r M_r^2) / (1 - rho)
+                        + |w_r (.) (v_t - v'_t)|_inf.
+Every recorded head with rho < 1 must stay within it at every step.
+"""
+import json
+import os
+import sys
+
+import numpy as np
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, os.path.join(HERE, "golden"))
+
+import make_conditioning as mc  # noqa: E402
+
+from non_linear_matrix_gb300.inputs import WORKLOADS  # noqa: E402
+
+REC = json.load(open(os.path.join(HERE, "golden", "conditioning.json")))
+
+
+def test_record_settings():
+    assert REC["delta"] == mc.DELTA and REC["perturb_seed"] == mc.PERTURB_SEED
+    assert REC["amp"] == mc.AMP and set(REC["forward"]) == set(mc.FORWARD)
+    for name, r in REC["forward"].items():
+        w = WORKLOADS[name]
+        h = np.asarray(r["h_amp10"])
+        assert h.shape == (len(r["batch_items"]), w.N)
+        assert ((0 <= h) & (h <= w.T)).all()
+        # the 1e-3 horizon can only come after the 10 * delta one
+        assert (np.asarray(r["h_1e3"]) >= h).all()
+
+
+def _subset(name):
+    """Batch items and heads recomputed: every head of one recorded batch
+    item with a window (or the first), bounded in size for the long
+    sequence, where only the heads with a window and two others are taken."""
+    r = REC["forward"][name]
+    w = WORKLOADS[name]
+    h = np.asarray(r["h_amp10"])
+    rows = [i for i in range(h.shape[0]) if (h[i] < w.T).any()] or [0]
+    i = rows[0]
+    heads = None
+    if w.T > 10000:
+        win = [int(n) for n in np.nonzero(h[i] < w.T)[0]]
+        calm = [int(n) for n in np.nonzero(h[i] == w.T)[0][:2]]
+        heads = sorted(win[:3] + calm)
+    return i, heads
+
+
+@pytest.mark.parametrize("name", sorted(mc.FORWARD))
+def test_forward_horizons_reproduce(oracle_mod, name):
+    """The stored horizons and per-head divergences are the oracle's."""
+    r = REC["forward"][name]
+    i, heads = _subset(name)
+    b = r["batch_items"][i]
+    got, _ = mc.forward_divergence(name, [b], heads)
+    hs = list(range(WORKLOADS[name].N)) if heads is None else heads
+    for key in ("h_amp10", "h_1e3"):
+        assert got[key][0] == [r[key][i][n] for n in hs], (name, key)
+    np.testing.assert_allclose(got["head_max_div"][0], [r["head_max_div"][i][n] for n in hs],
+                               rtol=1e-9, atol=0)
+
+
+@pytest.mark.parametrize("rho", [0.5, 0.9, 0.99])
+@pytest.mark.parametrize("name", ["fwd_bf16_b8_t2048_n32", "fwd_bf16_b1_t65536_n64"])
+def test_contraction_bound(oracle_mod, name, rho):
+    """The bound of the module docstring, on the workload's own q, k, v, f
+    and w_r with each head's W rescaled to ||W||_2 = rho < 1 (the workload's
+    W have ||W||_2 near 2, where the bound says nothing): the oracle's
+    divergence under the record's input perturbation must stay within it at
+    every step.  A blend that is not convex, a missing (1 - f) or a wrong
+    tanh argument breaks it; a tight case (rho = 0.99) keeps it from being
+    vacuous."""
+    w = WORKLOADS[name]
+    heads = list(range(8))
+    x, bs = mc.sliced_inputs(name, [0], heads=heads)
+    if w.T > 10000:
+        x = {n: (a[:, :8192] if n in ("q", "k", "v", "f") else a) for n, a in x.items()}
+    W = np.stack([Wn * (rho / np.linalg.norm(Wn, 2)) for Wn in x["W"]])
+    vp = mc.perturbed_v(x["v"], bs, heads)
+    a = oracle_mod.fwd(x["q"], x["k"], x["v"], x["f"], W, x["w_r"])
+    b = oracle_mod.fwd(x["q"], x["k"], vp, x["f"], W, x["w_r"])
+    d = np.abs(a["y"] - b["y"]).max(axis=(1, 3))[0]        # [N]: max over t and j
+    k, q = x["k"][0], x["q"][0]
+    ratios = []
+    for j in range(len(heads)):
+        dv = x["v"][0, :, j] - vp[0, :, j]                   # [T, V]
+        M = (np.abs(k) * np.linalg.norm(dv, axis=1)[:, None]).max(axis=0)  # [K]
+        bound = (np.linalg.norm(q, axis=1).max() * np.sqrt((M ** 2).sum()) / (1.0 - rho) +
+                 np.abs(x["w_r"][j][None, :] * dv).max())
+        assert d[j] <= bound * (1 + 1e-9) + 1e-15, (name, rho, j, d[j], bound)
+        ratios.append(d[j] / bound)
+    assert max(ratios) > 1e-3, ratios  # the divergences are not vanishingly small
+
+
+def test_w_horizons():
+    """The W-perturbation horizons: the gradient one (2e-3) never comes
+    after the y one (5e-3), and at least half of every workload's heads have
+    no window (their y is compared along the whole sequence)."""
+    for name, r in REC["forward"].items():
+        h5, h2 = np.asarray(r["h_w5e3"]), np.asarray(r["h_w2e3"])
+        assert (h2 <= h5).all(), name
+        assert (h5 == WORKLOADS[name].T).mean() >= 0.5, name
+        assert np.asarray(r["head_max_div_w"]).shape == h5.shape
+
+
+def test_windows_are_rare_and_recover():
+    """What the parity tests rely on: on every benchmarked workload most
+    heads never reach amplification 10 (whole-trajectory comparison holds
+    for them), and the steps inside windows are a small fraction."""
+    for name, r in REC["forward"].items():
+        h = np.asarray(r["h_amp10"])
+        T = WORKLOADS[name].T
+        assert (h == T).mean() >= 0.85, name
+        assert r["frac_steps_amp10"] <= 0.01, name
+        assert r["end_div"] <= 1e-4, name
+
+
+def test_gate_record_reproduces(oracle_mod):
+    """The gate section: recomputed exactly; the terms of dalpha and dbeta
+    cancel (the signed sum is a small part of the absolute mass)."""
+    got = mc.gate_record()
+    g = REC["gate"]
+    for key in ("gate_sens",):
+        for n, val in g[key].items():
+            assert got[key][n] == pytest.approx(val, rel=1e-9, abs=1e-15), (key, n)
+    for n in ("dalpha", "dbeta"):
+        np.testing.assert_allclose(got["gate_cancel"][n], g["gate_cancel"][n], rtol=1e-9)
+        assert np.median(g["gate_cancel"][n]) <= 0.5
+
+
+@pytest.mark.slow
+def test_gradient_record_reproduces(oracle_mod):
+    """The gradient sensitivities of the horizon-restricted loss (B=8,
+    T=4096, N=32: three oracle backward passes), and that restricting the
+    loss to t < h_w2e3 makes every gradient insensitive at the bf16 unit
+    roundoff (the premise of the whole-sequence gradient comparison)."""
+    g = REC["gradient"]
+    sens, sens_w = mc.gradient_sensitivity(mc.GRADIENT, REC["forward"][mc.GRADIENT]["h_w2e3"])
+    for n in g["sens"]:
+        assert sens[n] == pytest.approx(g["sens"][n], rel=1e-6, abs=1e-9), n
+        assert sens_w[n] == pytest.approx(g["sens_w"][n], rel=1e-6, abs=1e-12), n
+        assert g["sens_w"][n] <= 1e-2, n

@@ -189,6 +189,50 @@ def test_rows_per_warp_variants(m2rnn, oracle_mod, monkeypatch, mt):
     _compare(m2rnn, oracle_mod, x, "bf16", H0=H0, ckpt_every=16, label=f"MT={mt}")
 
 
+@pytest.mark.parametrize("G", ["1", "4", "5", "14"])
+@pytest.mark.parametrize("gated", [False, True])
+def test_wave_kernel(m2rnn, oracle_mod, monkeypatch, G, gated):
+    """The one-wave kernel (forced through M2RNN_FWD_WAVE; G heads per CTA
+    over the flattened (b, n) order, so with G = 4 or 5 and N = 6 CTAs span
+    two batch items), a ragged T (not a multiple of the 32-step chunk), H0
+    and checkpoints, f given or from the fused gate: whole trajectory."""
+    monkeypatch.setenv("M2RNN_FWD_WAVE", "1")
+    monkeypatch.setenv("M2RNN_FWD_WAVE_G", G)
+    B, T, N = 5, 77, 6 if G != "14" else 16  # (G = 14: a last CTA of 10 heads)
+    x = make_inputs(B, T, N, 64, 16, "bf16", 640 + int(G), gated=gated)
+    H0 = torch.rand(B, N, 64, 16, generator=torch.Generator().manual_seed(int(G))) - 0.5
+    if not gated:
+        _compare(m2rnn, oracle_mod, x, "bf16", H0=H0, ckpt_every=16, label=f"wave G={G}")
+        return
+    g = _dev(x)
+    y, HT, ck = m2rnn.fwd_gated(g["q"], g["k"], g["v"], g["a"], g["alpha"], g["beta"], g["W"],
+                                g["w_r"], H0.cuda(), ckpt_every=16)
+    torch.cuda.synchronize()
+    _check_status(m2rnn)
+    ref = oracle_mod.fwd_gated(x["q"], x["k"], x["v"], x["a"], x["alpha"], x["beta"], x["W"],
+                               x["w_r"], H0=H0, want_states=True)
+    assert np.abs(_np(y) - ref["y"]).max() <= TOL["bf16"]
+    assert np.abs(_np(HT) - ref["HT"]).max() <= TOL["bf16"]
+    assert np.abs(_np(ck) - ref["states"][:, :, list(range(0, T, 16))]).max() <= TOL["bf16"]
+
+
+def test_wave_kernel_checkpoint_only(m2rnn, monkeypatch):
+    """With y = NULL (the backward's own checkpoint recompute) the one-wave
+    kernel writes checkpoints only, bit for bit those of the full run."""
+    monkeypatch.setenv("M2RNN_FWD_WAVE", "1")
+    monkeypatch.setenv("M2RNN_FWD_WAVE_G", "5")
+    x = _dev(make_inputs(4, 100, 6, 64, 16, "bf16", 5, with_dy=True))
+    _, _, ck = m2rnn.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], ckpt_every=20)
+    a = m2rnn.bwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], x["dy"], ckpt=ck, ckpt_every=20)
+    b = m2rnn.bwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], x["dy"], ckpt=None,
+                  ckpt_every=20)
+    torch.cuda.synchronize()
+    _check_status(m2rnn)
+    for n in a:
+        err = (a[n].double() - b[n].double()).norm() / a[n].double().norm().clamp_min(1e-30)
+        assert err <= 1e-5, (n, float(err))
+
+
 def test_many_heads_per_cta_groups(m2rnn, oracle_mod):
     """Shapes whose dispatch uses several heads per CTA and 2-slice warps."""
     for (B, T, N) in [(40, 70, 64), (3, 40, 7)]:
@@ -284,14 +328,17 @@ def test_state_bitwise_across_launch_variants(m2rnn, monkeypatch):
     """The state update is the same per element whatever the launch shape:
     the whole-wave and tail launches with compile-time K and heads per CTA
     (two slices per warp), the generic instance with one slice per warp
-    (previous step's readout deferred) and a single launch all give the same
-    H_T bit for bit (y may differ in the last bits: its row sums are grouped
-    by warp)."""
+    (previous step's readout deferred), a single launch and the one-wave
+    kernel (one warp per head, 9 heads per CTA across batch items) all give
+    the same H_T bit for bit (y may differ in the last bits: its row sums
+    are grouped by warp)."""
     x = _dev(make_inputs(41, 96, 32, 64, 16, "bf16", 733))
     runs = {}
-    for name, env in (("planned", {}), ("one_slice", {"M2RNN_FWD_MT": "1"}),
-                      ("one_launch", {"M2RNN_FWD_ONE_LAUNCH": "1"})):
-        for k in ("M2RNN_FWD_MT", "M2RNN_FWD_ONE_LAUNCH"):
+    for name, env in (("planned", {"M2RNN_FWD_WAVE": "0"}),
+                      ("one_slice", {"M2RNN_FWD_MT": "1", "M2RNN_FWD_WAVE": "0"}),
+                      ("one_launch", {"M2RNN_FWD_ONE_LAUNCH": "1", "M2RNN_FWD_WAVE": "0"}),
+                      ("wave", {"M2RNN_FWD_WAVE": "1", "M2RNN_FWD_WAVE_G": "9"})):
+        for k in ("M2RNN_FWD_MT", "M2RNN_FWD_ONE_LAUNCH", "M2RNN_FWD_WAVE", "M2RNN_FWD_WAVE_G"):
             monkeypatch.delenv(k, raising=False)
         for k, v in env.items():
             monkeypatch.setenv(k, v)
@@ -299,6 +346,6 @@ def test_state_bitwise_across_launch_variants(m2rnn, monkeypatch):
         torch.cuda.synchronize()
         runs[name] = (y.float(), HT)
     _check_status(m2rnn)
-    for name in ("one_slice", "one_launch"):
+    for name in ("one_slice", "one_launch", "wave"):
         assert torch.equal(runs[name][1], runs["planned"][1]), name
         assert (runs[name][0] - runs["planned"][0]).abs().max().item() <= 2e-2, name

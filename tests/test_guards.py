@@ -97,6 +97,26 @@ def test_fwd_bwd_write_only_their_outputs(m2rnn, B, T, N, K, V, dtype, C, Nq):
     assert st == 0
 
 
+@pytest.mark.parametrize("G", ["4", "14"])
+def test_wave_kernel_writes_only_its_outputs(m2rnn, monkeypatch, G):
+    """The one-wave forward kernel (CTAs across two batch items with G = 4
+    of N = 6 heads; with G = 14 of N = 16 also a last CTA of 6 heads) with
+    y, H_T and checkpoints in guarded buffers."""
+    monkeypatch.setenv("M2RNN_FWD_WAVE", "1")
+    monkeypatch.setenv("M2RNN_FWD_WAVE_G", G)
+    B, T, N, C = (5, 77, 6, 24) if G == "4" else (3, 45, 16, 16)
+    g, copies = _inputs(B, T, N, 64, 16, "bf16", 90 + T)
+    Gd = Guarded()
+    nck = -(-T // C)
+    out = {"y": Gd((B, T, N, 16), torch.bfloat16), "HT": Gd((B, N, 64, 16)),
+           "ckpt": Gd((B, N, nck, 64, 16))}
+    m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], ckpt_every=C, out=out)
+    Gd.check(f"wave G={G}")
+    _inputs_unchanged(g, copies, "wave")
+    st, _ = m2rnn.device_status()
+    assert st == 0
+
+
 @pytest.mark.parametrize("B,T,N", [(3, 45, 6), (41, 40, 32)])  # the second splits the forward
 def test_gated_and_norm_write_only_their_outputs(m2rnn, B, T, N):
     K, V, C = 64, 16, 16
