@@ -291,18 +291,19 @@ int run_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, c
     p.norm = 1;
   }
 
-  // One-wave kernel: when the heads need more than one wave of the CTAs
-  // planned above (8 heads of two warps per SM) but fit 14 per SM, every head
-  // is made resident at once, G = ceil(B N / SMs) heads per CTA over the
-  // flattened (b, n) order, one warp per head.  M2RNN_FWD_WAVE=0 turns it
-  // off and =1 uses it wherever it applies; M2RNN_FWD_WAVE_G forces G (A/B
-  // measurement and tests).
+  // One-wave kernel (opt-in, M2RNN_FWD_WAVE=1): every head resident at once,
+  // G = ceil(B N / SMs) heads per CTA over the flattened (b, n) order, one
+  // warp per head; M2RNN_FWD_WAVE_G forces G.  Measured slower than the
+  // two-launch plan below at B=64, T=4096, N=32 (3.07 against 2.78 ms): one
+  // warp's four 16-row tiles follow each other in its in-order instruction
+  // stream, and 14 such warps per SM hide less latency than 16 warps of two
+  // tiles.  It stays for A/B measurement and is tested like the others.
   if (!f32 && s->V == 16 && s->K == 64 && nf == nullptr && groups(s) == 1) {
     const long long heads = static_cast<long long>(s->B) * s->N;
     int Gw = static_cast<int>((heads + sms - 1) / sms);
-    bool use = heads > 8LL * sms;
-    if (const char* e = std::getenv("M2RNN_FWD_WAVE")) use = e[0] == '1';
-    if (const char* e = std::getenv("M2RNN_FWD_WAVE_G")) Gw = std::atoi(e);
+    const char* e = std::getenv("M2RNN_FWD_WAVE");
+    const bool use = e != nullptr && e[0] == '1';
+    if (const char* eg = std::getenv("M2RNN_FWD_WAVE_G")) Gw = std::atoi(eg);
     if (use && Gw >= 1 && Gw <= m2rnn::fwd_wave_max_heads() && Gw <= s->N) {
       m2rnn::FwdParams pw = p;
       pw.G = Gw;

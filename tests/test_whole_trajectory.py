@@ -7,9 +7,12 @@ oracle alone by tests/golden/make_conditioning.py and pinned by
 tests/test_conditioning.py).  They mark where the oracle departs from its own
 trajectory when the product H W is perturbed by the bf16 unit roundoff, the
 size of the rounding the bf16-operand path applies to it at every step:
-  * y of head (b, n) is compared at every step t < h_w5e3[b][n] (the oracle
-    itself moves by at most 5e-3 there, a quarter of the 2e-2 bound), and
-    H_T of every head without a window (h_w5e3 = T);
+  * y of head (b, n) is compared at every step t < h_y[b][n] = min(h_w5e3,
+    h_amp10)[b][n]: the oracle itself moves by at most 5e-3 there (a quarter
+    of the 2e-2 bound) under that perturbation, and its amplification of a
+    1e-7 input perturbation stays below 10 (one random perturbation of W can
+    miss a window that the input perturbation shows); H_T of every head with
+    no window (h_y = T) is compared too;
   * the gradients of the loss restricted to t < h_w2e3[b][n] (dy zeroed from
     the horizon on, so no head's backward crosses its window) are compared
     whole, relative L2 <= 1e-2 per tensor, at the fwd+bwd workload's full
@@ -67,7 +70,7 @@ def test_forward_whole_trajectory(m2rnn, oracle_mod, name):
     ref = oracle_mod.fwd(xs["q"], xs["k"], xs["v"], xs["f"], xs["W"], xs["w_r"])
     yg = y[bs].float().cpu().double().numpy()
     e = np.abs(yg - ref["y"]).max(axis=3)                 # [B', T, N]
-    h = np.asarray(r["h_w5e3"])
+    h = np.minimum(np.asarray(r["h_w5e3"]), np.asarray(r["h_amp10"]))
     inside = np.arange(w.T)[None, :, None] < h[:, None, :]
     worst_y = float(np.where(inside, e, 0.0).max())
     whole = h == w.T
