@@ -48,9 +48,16 @@ oracle's own relative L2 change of that gradient under the 1e-7 input
 perturbation, divided by DELTA (its amplification); sens_w[name] is its
 relative L2 change under the W perturbation above.
 
-For the fused input gate (frame "The gate preserves a direct path through
-time", Eq. 13) it records, on the first 64 steps of the gated forward +
-backward workload (one checkpoint interval, H0 = 0):
+The gated forward + backward workload (f = exp(-alpha softplus(a + beta)),
+frame "The gate preserves a direct path through time", Eq. 13) gets the same
+forward horizons (its trajectory differs from the ungated one) and the same
+gradient record (gradient_gated, through the gate: da, dalpha, dbeta).  The
+readout-epilogue workload draws the ungated workload's inputs first and g,
+w_norm after them, so its recurrence and horizons are those of
+fwdbwd_bf16_b8_t4096_n32.
+
+For the fused input gate it also records, on the first 64 steps of the gated
+workload (one checkpoint interval, H0 = 0):
   * gate_cancel[n]: |dalpha_n| / sum_{b,t} |term_{b,t,n}| and the same for
     dbeta: how far the signed per-step terms of these two sums cancel;
   * gate_sens[name]: the oracle's own relative L2 change of each gradient
@@ -87,8 +94,10 @@ FORWARD = {
     "fwd_bf16_b64_t4096_n32_k128": [0, 17, 33, 63],
     "fwd_bf16_b64_t4096_n32_v32": [0, 17, 33, 63],
     "fwdbwd_bf16_b8_t4096_n32": None,
+    "fwdbwd_gated_bf16_b8_t4096_n32": None,
 }
 GRADIENT = "fwdbwd_bf16_b8_t4096_n32"
+GRADIENT_GATED = "fwdbwd_gated_bf16_b8_t4096_n32"
 GATED = "fwdbwd_gated_bf16_b8_t4096_n32"
 GATE_T = 64
 U = 2.0 ** -9       # bf16 unit roundoff
@@ -147,6 +156,25 @@ def perturbed_w(W):
     return W * (1.0 + U * np.random.default_rng(W_SEED).standard_normal(W.shape))
 
 
+def run_fwd(name, x, v=None, W=None):
+    """The oracle's forward of the workload (gated where it is), with v or W
+    replaced."""
+    v = x["v"] if v is None else v
+    W = x["W"] if W is None else W
+    if WORKLOADS[name].gated:
+        return oracle.fwd_gated(x["q"], x["k"], v, x["a"], x["alpha"], x["beta"], W, x["w_r"])
+    return oracle.fwd(x["q"], x["k"], v, x["f"], W, x["w_r"])
+
+
+def run_bwd(name, x, dy, v=None, W=None):
+    """The oracle's backward of the workload (through the gate where it is)."""
+    v = x["v"] if v is None else v
+    W = x["W"] if W is None else W
+    if WORKLOADS[name].gated:
+        return oracle.bwd_gated(x["q"], x["k"], v, x["a"], x["alpha"], x["beta"], W, x["w_r"], dy)
+    return oracle.bwd(x["q"], x["k"], v, x["f"], W, x["w_r"], dy)
+
+
 def forward_divergence(name, batch_items=None, heads=None):
     """d[b, t, n] of the oracle under the input perturbation, plus the
     horizons (both perturbations).  batch_items, heads: indices into the
@@ -155,9 +183,9 @@ def forward_divergence(name, batch_items=None, heads=None):
     N_all = WORKLOADS[name].N
     hs = list(range(N_all)) if heads is None else list(heads)
     z = np.random.default_rng(W_SEED).standard_normal((N_all,) + x["W"].shape[1:])[hs]
-    a = oracle.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"])
-    b = oracle.fwd(x["q"], x["k"], perturbed_v(x["v"], bs, heads), x["f"], x["W"], x["w_r"])
-    c = oracle.fwd(x["q"], x["k"], x["v"], x["f"], x["W"] * (1.0 + U * z), x["w_r"])
+    a = run_fwd(name, x)
+    b = run_fwd(name, x, v=perturbed_v(x["v"], bs, heads))
+    c = run_fwd(name, x, W=x["W"] * (1.0 + U * z))
     d = np.abs(a["y"] - b["y"]).max(axis=3)  # [B, T, N]
     dw = np.abs(a["y"] - c["y"]).max(axis=3)
     return {
@@ -188,10 +216,9 @@ def gradient_sensitivity(name, h):
     x, bs = sliced_inputs(name, None, with_dy=True)
     T = x["v"].shape[1]
     dy = x["dy"] * horizon_mask(h, T)[..., None]
-    args = (x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"], dy)
-    a = oracle.bwd(*args)
-    b = oracle.bwd(x["q"], x["k"], perturbed_v(x["v"], bs), x["f"], x["W"], x["w_r"], dy)
-    c = oracle.bwd(x["q"], x["k"], x["v"], x["f"], perturbed_w(x["W"]), x["w_r"], dy)
+    a = run_bwd(name, x, dy)
+    b = run_bwd(name, x, dy, v=perturbed_v(x["v"], bs))
+    c = run_bwd(name, x, dy, W=perturbed_w(x["W"]))
     sens, sens_w = {}, {}
     for n in a:
         den = np.linalg.norm(a[n])
@@ -222,8 +249,26 @@ def gate_record():
             "gate_sens": sens, "gate_cancel": cancel}
 
 
+def add_gated_gradient(rec):
+    t0 = time.time()
+    sens, sens_w = gradient_sensitivity(GRADIENT_GATED, rec["forward"][GRADIENT_GATED]["h_w2e3"])
+    rec["gradient_gated"] = {"workload": GRADIENT_GATED,
+                             "loss": "sum over t < h_w2e3[b][n] of <dy, y>",
+                             "sens": sens, "sens_w": sens_w, "u": U, "w_seed": W_SEED}
+    print("gated gradient sensitivity", sens, sens_w, f"({time.time() - t0:.1f} s)")
+
+
 def main():
     oracle.build()
+    if "--only-gated" in sys.argv:  # the gated workload's sections, added to an existing record
+        rec = json.load(open(OUT))
+        r, _ = forward_divergence(GRADIENT_GATED, FORWARD[GRADIENT_GATED])
+        rec["forward"][GRADIENT_GATED] = r
+        add_gated_gradient(rec)
+        with open(OUT, "w") as fh:
+            json.dump(rec, fh, separators=(",", ":"))
+            fh.write("\n")
+        return
     if "--only-gate" in sys.argv:
         rec = json.load(open(OUT))
         sens, sens_w = gradient_sensitivity(GRADIENT, rec["forward"][GRADIENT]["h_w2e3"])
@@ -252,6 +297,7 @@ def main():
     rec["gradient"] = {"workload": GRADIENT, "loss": "sum over t < h_w2e3[b][n] of <dy, y>",
                        "sens": sens, "sens_w": sens_w, "u": U, "w_seed": W_SEED}
     print("gradient sensitivity", sens, sens_w, f"({time.time() - t0:.1f} s)")
+    add_gated_gradient(rec)
     rec["gate"] = gate_record()
     print("gate", rec["gate"]["gate_sens"])
     with open(OUT, "w") as fh:

@@ -153,14 +153,17 @@ def test_gate_record_reproduces(oracle_mod):
 
 
 @pytest.mark.slow
-def test_gradient_record_reproduces(oracle_mod):
+@pytest.mark.parametrize("name,key", [(mc.GRADIENT, "gradient"), (mc.GRADIENT_GATED, "gradient_gated")])
+def test_gradient_record_reproduces(oracle_mod, name, key):
     """The gradient sensitivities of the horizon-restricted loss (B=8,
-    T=4096, N=32: three oracle backward passes), and that restricting the
-    loss to t < h_w2e3 makes every gradient insensitive at the bf16 unit
-    roundoff (the premise of the whole-sequence gradient comparison)."""
-    g = REC["gradient"]
-    sens, sens_w = mc.gradient_sensitivity(mc.GRADIENT, REC["forward"][mc.GRADIENT]["h_w2e3"])
+    T=4096, N=32, f given or from the gate: three oracle backward passes
+    each), and that without the gate, restricting the loss to t < h_w2e3
+    makes every gradient insensitive at the bf16 unit roundoff (the gated
+    dW stays at 3 %; its test bound follows the record)."""
+    g = REC[key]
+    sens, sens_w = mc.gradient_sensitivity(name, REC["forward"][name]["h_w2e3"])
     for n in g["sens"]:
         assert sens[n] == pytest.approx(g["sens"][n], rel=1e-6, abs=1e-9), n
         assert sens_w[n] == pytest.approx(g["sens_w"][n], rel=1e-6, abs=1e-12), n
-        assert g["sens_w"][n] <= 1e-2, n
+    if name == mc.GRADIENT:
+        assert max(g["sens_w"].values()) <= 1e-2
