@@ -8,11 +8,22 @@
 //   * latency (clocks) of dependent tanh, FFMA, mma and cvt chains;
 //   * one recurrence step of a 16x16 state tile (mma -> tanh -> blend ->
 //     bf16 repack), alone (the serial step latency) and with many warps per
-//     SM (the throughput the step reaches).
+//     SM (the throughput the step reaches);
+//   * the 5th-generation tensor core (tcgen05.mma, accumulator in tensor
+//     memory) at the recurrence's shapes: a correctness check of one M=64 and
+//     one M=128 product against the host (A K-major, B MN-major, no swizzle),
+//     the issue-to-completion latency of one MMA, the rate of independent
+//     MMAs from one thread and from four warps, and one recurrence step of a
+//     64-row head on it (MMA -> commit -> tcgen05.ld -> tanh -> blend -> bf16
+//     rows back to shared memory).
 // Every global access is out[gid] / cyc[blockIdx.x] / bw[0..7] with buffers
-// sized for the largest launch below.
+// sized for the largest launch below; the tcgen05 kernel runs as one CTA of
+// 128 threads whose descriptors address only its 16 KB operand buffer and
+// whose accumulators lie inside its 512 allocated tensor-memory columns, at
+// column offsets that are multiples of N.
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -165,6 +176,207 @@ __global__ void step_kernel(float* out, long long* cyc, const uint32_t* bw, int 
   if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
 }
 
+// ---- tcgen05 -----------------------------------------------------------------
+
+// Shared-memory matrix descriptor, no swizzle: start, leading (K-direction
+// core-matrix) and stride (M/N-direction) byte offsets, descriptor version 1.
+__device__ __forceinline__ uint64_t umma_sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, B MN-major.
+__device__ __forceinline__ uint32_t umma_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t id) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d), "l"(a), "l"(b),
+               "r"(id));
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 16 lanes x 256 bits, twice along the columns: the mma.sync accumulator
+// fragment of a 16x16 fp32 tile (rows g, g+8; columns 2c, 2c+1, +8).
+__device__ __forceinline__ void tc_ld16x256x2(uint32_t ta, float (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+               "tcgen05.wait::ld.sync.aligned;"
+               : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]),
+                 "=f"(r[6]), "=f"(r[7])
+               : "r"(ta)
+               : "memory");
+}
+// One lane per row, 16 columns.
+__device__ __forceinline__ void tc_ld32x32x16(uint32_t ta, float (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]),
+        "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]),
+        "=f"(r[14]), "=f"(r[15])
+      : "r"(ta)
+      : "memory");
+}
+
+constexpr int kUmmaCols = 512;           // tensor-memory columns allocated
+constexpr int kUmmaSmem = 16384;         // operand buffer: A at 0 (4 KB), B at 8 KB (8 KB)
+constexpr uint32_t kUmmaB = 8192;
+constexpr uint64_t kUmmaWaitNs = 200000000ull;
+
+// A (M x 16, K-major): core (m/8, k/8) at (m/8)*256 + (k/8)*128, row m%8 at
+// 16*(m%8).  B (16 x N, MN-major): core (k/8, n/8) at (k/8)*(N/8)*128 +
+// (n/8)*128.  So A: LBO 128, SBO 256; B: LBO (N/8)*128, SBO 128.
+__device__ __forceinline__ uint32_t umma_a_off(int m, int k) {
+  return (uint32_t)((m / 8) * 256 + (k / 8) * 128 + 16 * (m % 8) + 2 * (k % 8));
+}
+
+// mode 0: D = A B, M=64 N=16, read as 16x256b.x2 fragments -> out[tid*8 + r]
+// mode 1: D = A B, M=128 N=16, read one lane per row -> out[tid*16 + i]
+// mode 2: thread 0: cyc[0] one MMA issue -> completion (mean of 8), cyc[1] 64
+//         independent M=64 N=16 MMAs, cyc[2] 64 independent M=128 N=256
+// mode 3: four warps issue 16 M=64 N=16 MMAs each: cyc[3]
+// mode 4: `iters` recurrence steps of one 64-row head: cyc[4]
+__global__ void __launch_bounds__(128, 1) umma_kernel(float* out, long long* cyc, const uint4* img,
+                                                      int mode, int iters, int* status) {
+  extern __shared__ __align__(1024) uint8_t usm[];
+  __shared__ __align__(8) uint64_t bars[4];
+  __shared__ uint32_t tslot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  for (int i = tid; i < kUmmaSmem / 16; i += 128) reinterpret_cast<uint4*>(usm)[i] = img[i];
+  if (tid < 4) mbar_init(smem_addr(&bars[tid]), 1);
+  mbar_init_fence();
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tslot)),
+                 "r"(kUmmaCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = tslot, base = smem_addr(usm);
+  const uint32_t lanes = (uint32_t)(warp * 32) << 16;  // this warp's lane quarter
+  const uint64_t a64 = umma_sdesc(base, 128, 256);
+  bool ok = true;
+  uint32_t par = 0;
+  if (mode == 0 || mode == 1) {
+    const int M = mode == 0 ? 64 : 128;
+    if (tid == 0) {
+      umma(tm, a64, umma_sdesc(base + kUmmaB, 256, 128), umma_idesc(M, 16));
+      umma_commit(smem_addr(&bars[0]));
+    }
+    ok = mbar_wait(smem_addr(&bars[0]), 0, kUmmaWaitNs);
+    tc_fence_after();
+    if (mode == 0) {
+      float r[8];
+      tc_ld16x256x2(tm + lanes, r);
+      for (int i = 0; i < 8; ++i) out[tid * 8 + i] = r[i];
+    } else {
+      float r[16];
+      tc_ld32x32x16(tm + lanes, r);
+      for (int i = 0; i < 16; ++i) out[tid * 16 + i] = r[i];
+    }
+  } else if (mode == 2) {
+    if (tid == 0) {
+      const uint32_t bar = smem_addr(&bars[0]);
+      const uint64_t b16 = umma_sdesc(base + kUmmaB, 256, 128);
+      const uint64_t b256 = umma_sdesc(base + kUmmaB, 4096, 128);
+      long long t0 = clock64();
+      for (int r = 0; r < 8; ++r) {
+        umma(tm, a64, b16, umma_idesc(64, 16));
+        umma_commit(bar);
+        ok = ok && mbar_wait(bar, par, kUmmaWaitNs);
+        par ^= 1;
+      }
+      cyc[0] = (clock64() - t0) / 8;
+      t0 = clock64();
+#pragma unroll
+      for (int i = 0; i < 64; ++i) umma(tm + 16 * (i & 15), a64, b16, umma_idesc(64, 16));
+      umma_commit(bar);
+      ok = ok && mbar_wait(bar, par, kUmmaWaitNs);
+      par ^= 1;
+      cyc[1] = clock64() - t0;
+      t0 = clock64();
+#pragma unroll
+      for (int i = 0; i < 64; ++i) umma(tm + 256 * (i & 1), a64, b256, umma_idesc(128, 256));
+      umma_commit(bar);
+      ok = ok && mbar_wait(bar, par, kUmmaWaitNs);
+      par ^= 1;
+      cyc[2] = clock64() - t0;
+    }
+  } else if (mode == 3) {
+    __syncthreads();
+    const long long t0 = clock64();
+    if (lane == 0) {
+      const uint64_t b16 = umma_sdesc(base + kUmmaB, 256, 128);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) umma(tm + 128 * warp + 16 * (i & 7), a64, b16, umma_idesc(64, 16));
+      umma_commit(smem_addr(&bars[warp]));
+      ok = mbar_wait(smem_addr(&bars[warp]), 0, kUmmaWaitNs);
+    }
+    __syncthreads();
+    if (tid == 0) cyc[3] = clock64() - t0;
+  } else if (mode == 4) {
+    // A = bf16(H) rows (K-major), B = W (MN-major); each warp owns rows
+    // 16w..16w+15 in the fragment layout of the M=64 accumulator.
+    float H[8];
+    for (int i = 0; i < 8; ++i) H[i] = 0.01f * (lane + i);
+    const float f = 0.9f;
+    const int R0 = 16 * warp + g, R1 = R0 + 8;
+    const uint32_t w0 = base + umma_a_off(R0, 2 * c), w1 = base + umma_a_off(R1, 2 * c);
+    const uint32_t w2 = base + umma_a_off(R0, 8 + 2 * c), w3 = base + umma_a_off(R1, 8 + 2 * c);
+    const uint32_t bar = smem_addr(&bars[0]);
+    const uint64_t b16 = umma_sdesc(base + kUmmaB, 256, 128);
+    const uint32_t id = umma_idesc(64, 16);
+    __syncthreads();
+    const long long t0 = clock64();
+    for (int it = 0; it < iters; ++it) {
+      if (tid == 0) {
+        tc_fence_after();
+        umma(tm, a64, b16, id);
+        umma_commit(bar);
+      }
+      ok = mbar_wait(bar, par, kUmmaWaitNs);
+      par ^= 1;
+      tc_fence_after();
+      float acc[8];
+      tc_ld16x256x2(tm + lanes, acc);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float z = tanh_approx(acc[r]);
+        H[r] = fmaf(f, H[r] - z, z);
+      }
+      sts_u32(w0, pack_bf16x2(H[0], H[1]));
+      sts_u32(w1, pack_bf16x2(H[2], H[3]));
+      sts_u32(w2, pack_bf16x2(H[4], H[5]));
+      sts_u32(w3, pack_bf16x2(H[6], H[7]));
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      if (!__syncthreads_and(ok)) break;  // every thread leaves together
+    }
+    if (tid == 0) cyc[4] = (clock64() - t0) / iters;
+    float s = 0.f;
+    for (int i = 0; i < 8; ++i) s += H[i];
+    out[tid] = s;
+  }
+  if (!ok) atomicOr(status, 1);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(kUmmaCols)
+                 : "memory");
+}
+
 __global__ void clock_probe(long long* c, unsigned long long* g, int spin) {
   unsigned long long g0 = globaltimer_ns();
   const long long c0 = clock64();
@@ -259,6 +471,82 @@ int main() {
       run_step("MT=4", step_kernel<4>, 4, sms, 16) || run_step("MT=2", step_kernel<2>, 2, sms, 16) ||
       run_step("MT=1", step_kernel<1>, 1, sms, 16) || run_step("MT=1", step_kernel<1>, 1, sms, 32))
     return 1;
+  // ---- tcgen05 at the recurrence's shapes
+  {
+    // A[m][k] and W[k][n]: small integers, exact in bf16 and in fp32 sums
+    static uint8_t himg[kUmmaSmem];
+    memset(himg, 0, sizeof(himg));
+    auto bf = [](float x) -> uint16_t {
+      uint32_t u;
+      memcpy(&u, &x, 4);
+      return (uint16_t)(u >> 16);
+    };
+    static float A[128][16], Wm[16][16];
+    for (int m = 0; m < 128; ++m)
+      for (int k = 0; k < 16; ++k) {
+        A[m][k] = (float)((m * 7 + k * 3) % 9 - 4);
+        const uint16_t h = bf(A[m][k]);
+        memcpy(himg + (m / 8) * 256 + (k / 8) * 128 + 16 * (m % 8) + 2 * (k % 8), &h, 2);
+      }
+    for (int k = 0; k < 16; ++k)
+      for (int n = 0; n < 16; ++n) {
+        Wm[k][n] = (float)((k * 5 + n * 11) % 7 - 3);
+        const uint16_t h = bf(Wm[k][n]);
+        memcpy(himg + kUmmaB + (k / 8) * 256 + (n / 8) * 128 + 16 * (k % 8) + 2 * (n % 8), &h, 2);
+      }
+    uint4* dimg;
+    int* dstat;
+    CK(cudaMalloc(&dimg, kUmmaSmem));
+    CK(cudaMalloc(&dstat, sizeof(int)));
+    CK(cudaMemcpy(dimg, himg, kUmmaSmem, cudaMemcpyHostToDevice));
+    CK(cudaMemset(dstat, 0, sizeof(int)));
+    CK(cudaFuncSetAttribute(umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUmmaSmem));
+    static float ho[128 * 16];
+    auto ref = [&](int m, int n) {
+      float s = 0.f;
+      for (int k = 0; k < 16; ++k) s += A[m][k] * Wm[k][n];
+      return s;
+    };
+    // M = 64: thread t of warp w, register r: row 16w + t/4 + 8((r/2)%2),
+    // column 2(t%4) + r%2 + 8(r/4)
+    umma_kernel<<<1, 128, kUmmaSmem>>>(out, cyc, dimg, 0, 0, dstat);
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(ho, out, sizeof(float) * 128 * 8, cudaMemcpyDeviceToHost));
+    int bad = 0;
+    for (int t = 0; t < 128; ++t)
+      for (int r = 0; r < 8; ++r) {
+        const int w = t / 32, l = t % 32;
+        const int m = 16 * w + l / 4 + 8 * ((r / 2) % 2), n = 2 * (l % 4) + r % 2 + 8 * (r / 4);
+        bad += ho[t * 8 + r] != ref(m, n);
+      }
+    printf("tcgen05 check M=64 N=16 K=16 (accumulator row 16w+i in lane 32w+i): %s\n",
+           bad ? "MISMATCH" : "exact");
+    umma_kernel<<<1, 128, kUmmaSmem>>>(out, cyc, dimg, 1, 0, dstat);
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(ho, out, sizeof(float) * 128 * 16, cudaMemcpyDeviceToHost));
+    bad = 0;
+    for (int m = 0; m < 128; ++m)
+      for (int n = 0; n < 16; ++n) bad += ho[m * 16 + n] != ref(m, n);
+    printf("tcgen05 check M=128 N=16 K=16 (row m in lane m): %s\n", bad ? "MISMATCH" : "exact");
+    for (int mode = 2; mode <= 4; ++mode) {
+      umma_kernel<<<1, 128, kUmmaSmem>>>(out, cyc, dimg, mode, 2000, dstat);
+      CK(cudaDeviceSynchronize());
+    }
+    int st = 0;
+    CK(cudaMemcpy(hc, cyc, sizeof(long long) * 5, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(&st, dstat, sizeof(int), cudaMemcpyDeviceToHost));
+    printf("tcgen05 one MMA (M=64 N=16 K=16), issue -> completion on an mbarrier: %lld clk\n", hc[0]);
+    printf("tcgen05 64 independent M=64 N=16 K=16 MMAs, one thread: %.1f clk per MMA\n",
+           hc[1] / 64.0);
+    printf("tcgen05 64 independent M=128 N=256 K=16 MMAs, one thread: %.1f clk per MMA "
+           "(%.0f FMA/clk/SM)\n", hc[2] / 64.0, 64.0 * 128 * 256 * 16 / (double)hc[2]);
+    printf("tcgen05 4 warps x 16 M=64 N=16 K=16 MMAs: %.1f clk per MMA\n", hc[3] / 64.0);
+    printf("tcgen05 recurrence step, one 64-row head (MMA -> commit -> ld -> tanh -> blend -> "
+           "rows to shared memory): %lld clk/step\n", hc[4]);
+    if (st) printf("tcgen05: a completion wait timed out\n");
+    CK(cudaFree(dimg));
+    CK(cudaFree(dstat));
+  }
   printf("done\n");
   return 0;
 }
