@@ -176,6 +176,19 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
   const size_t qk_ext = static_cast<size_t>(p.B) * T * Nq * K;
   const size_t v_ext = static_cast<size_t>(p.B) * T * N * V, f_ext = static_cast<size_t>(p.B) * T * N;
 
+  // bf16 f (or a) of Geff in {1, 2, 4, 8} heads is read with one vector load
+  // per step (aligned: n0 and N are multiples of Geff); the gate's alpha and
+  // beta of those heads are read once.
+  const bool fvec = !F32 && (Geff == 1 || Geff == 2 || Geff == 4 || Geff == 8) && N % Geff == 0;
+  float ga[8], gb[8];
+  bool gok[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    gok[h] = GATED && h < Geff && in_range(p.status, n0 + h, 1, N, CHK_FWD_PARAM);
+    ga[h] = gok[h] ? to_f(galpha[n0 + h]) : 0.f;
+    gb[h] = gok[h] ? to_f(gbeta[n0 + h]) : 0.f;
+  }
+
   // Waits for a free stage, starts the bulk copies of chunk ch and writes
   // its f (or, gated, f computed from a) as fp32 pairs.
   auto issue = [&](int ch) -> bool {
@@ -219,8 +232,42 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
       else
         ptx::mbar_complete_tx(raw, v_bytes);
     }
-    // f[b, t0:t0+Tc, n0:n0+Geff] -> fp32 pairs [TC][G][2]; loads batched.
-    const int nf = Tc * Geff;
+    // f[b, t0:t0+Tc, n0:n0+Geff] -> fp32 pairs [TC][G][2].
+    if (fvec) {  // a step per lane: one 2-, 4-, 8- or 16-byte load of its Geff values
+      for (int tl = lane; tl < Tc; tl += 32) {
+        const size_t fi = (bt0 + tl) * N + n0;
+        uint32_t fw[4] = {0u, 0u, 0u, 0u};
+        if (in_range(p.status, fi, Geff, f_ext, CHK_FWD_F)) {
+          const void* src = f + fi;
+          if (Geff == 8) {
+            const uint4 u = *static_cast<const uint4*>(src);
+            fw[0] = u.x; fw[1] = u.y; fw[2] = u.z; fw[3] = u.w;
+          } else if (Geff == 4) {
+            const uint2 u = *static_cast<const uint2*>(src);
+            fw[0] = u.x; fw[1] = u.y;
+          } else if (Geff == 2) {
+            fw[0] = *static_cast<const uint32_t*>(src);
+          } else {
+            fw[0] = *static_cast<const uint16_t*>(src);
+          }
+        }
+        const uint32_t dst = st + L.fd + static_cast<uint32_t>(tl * G * 8);
+#pragma unroll
+        for (int h = 0; h < 8; h += 2) {
+          if (h >= Geff) break;
+          float a = ptx::bf16x2_lo(fw[h / 2]), a1 = ptx::bf16x2_hi(fw[h / 2]);
+          if constexpr (GATED) {
+            a = gok[h] ? gate_f(a, ga[h], gb[h]) : 0.f;
+            a1 = gok[h + 1] ? gate_f(a1, ga[h + 1], gb[h + 1]) : 0.f;
+          }
+          if (h + 1 < Geff)
+            ptx::sts_f32x4(dst + 8 * h, a, a, a1, a1);
+          else
+            ptx::sts_f32x2(dst + 8 * h, a, a);
+        }
+      }
+    }
+    const int nf = fvec ? 0 : Tc * Geff;  // otherwise element by element, loads batched
     for (int base = 0; base < nf; base += 256) {
       float fv[8];
 #pragma unroll
@@ -360,12 +407,17 @@ __device__ __forceinline__ void ldg8(const void* src, float (&o)[8]) {
 // Sums the per-warp readout partials, adds w_r (.) v and stores y.  NORM
 // (the readout epilogue): also adds this CTA's share of sum (y (.) g)^2 of
 // every token into p.ssq[b, t] (the normalisation kernel finishes the norm).
-template <int V, bool F32, bool NORM>
+//
+// The epilogue runs on NEPI warps (e = 0 .. NEPI-1) that split each chunk's
+// outputs between them, so that no SMSP carries all of it next to its
+// consumer warps.
+template <int V, bool F32, bool NORM, int NEPI>
 __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout& L, uint32_t sbase,
-                                             int b, int n0, int Geff) {
+                                             int b, int n0, int Geff, int e) {
   using TIn = typename InType<F32>::T;
   constexpr int es = sizeof(TIn);
-  const int lane = threadIdx.x & 31;
+  constexpr int LANES = 32 * NEPI;
+  const int lane = threadIdx.x & 31, id = 32 * e + lane;
   const int T = p.T, N = p.N, G = p.G, WPH = p.WPH;
   const uint32_t bars = sbase + L.bars;
   const int TC = p.tc;
@@ -373,11 +425,25 @@ __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout
   const TIn* w_r = static_cast<const TIn*>(p.w_r) + static_cast<size_t>(n0) * V;
   const int GV = Geff * V;
   const size_t y_ext = static_cast<size_t>(p.B) * T * N * V;  // y and g (index checks)
-  for (int e = lane; e < GV; e += 32)
-    if (in_range(p.status, static_cast<size_t>(n0) * V + e, 1, static_cast<size_t>(N) * V, CHK_FWD_PARAM))
-      ptx::sts_f32(sbase + L.wr + 4 * e, to_f(w_r[e]));
+  // (each epilogue warp writes the same w_r values; it reads only its own)
+  for (int i = lane; i < GV; i += 32)
+    if (in_range(p.status, static_cast<size_t>(n0) * V + i, 1, static_cast<size_t>(N) * V, CHK_FWD_PARAM))
+      ptx::sts_f32(sbase + L.wr + 4 * i, to_f(w_r[i]));
   __syncwarp();
   const int R8 = GV / 8;  // 8-element groups per time step
+  // Where R8 divides the epilogue's lanes, every lane keeps one group (heads
+  // hl, columns j..j+7) and walks the steps id / R8, + LANES / R8, ...; its
+  // w_r stays in registers.
+  const bool fixed = R8 > 0 && R8 <= LANES && LANES % R8 == 0;
+  const int gi = fixed ? id % R8 : 0;
+  const int fr = gi * 8, fhl = fr / V, fj = fr - fhl * V;
+  float2 wrf[4];
+  {
+    const float4 w0 = ptx::lds_f32x4(sbase + L.wr + 4 * fr);
+    const float4 w1 = ptx::lds_f32x4(sbase + L.wr + 4 * fr + 16);
+    wrf[0] = make_float2(w0.x, w0.y); wrf[1] = make_float2(w0.z, w0.w);
+    wrf[2] = make_float2(w1.x, w1.y); wrf[3] = make_float2(w1.z, w1.w);
+  }
   for (int ch = 0; ch < nchunks; ++ch) {
     const int s = ch % NSTAGE, ys = ch % NYSTAGE;
     if (!warp_wait(bar_in_full(bars, s), (ch / NSTAGE) & 1, p.wait_limit_ns) ||
@@ -391,7 +457,50 @@ __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout
     const uint32_t yp = sbase + L.yp_base + static_cast<uint32_t>(ys) * L.yp_stage;
     TIn* y = static_cast<TIn*>(p.y) + ((static_cast<size_t>(b) * T + t0) * N + n0) * V;
     const int nidx = p.y != nullptr ? Tc * R8 : 0;  // no y in checkpoint-only runs
-    for (int idx = lane; idx < nidx; idx += 32) {
+    if (fixed && nidx > 0) {
+      const int tstep = LANES / R8;
+#pragma unroll 1
+      for (int tl = id / R8; tl < Tc; tl += tstep) {
+        const uint32_t pa = yp + static_cast<uint32_t>((((tl * G + fhl) * WPH) * V + fj) * 4);
+        float2 o[4];
+        {
+          const float4 a = ptx::lds_f32x4(pa), c = ptx::lds_f32x4(pa + 16);
+          o[0] = make_float2(a.x, a.y); o[1] = make_float2(a.z, a.w);
+          o[2] = make_float2(c.x, c.y); o[3] = make_float2(c.z, c.w);
+        }
+        for (int w = 1; w < WPH; ++w) {  // the warps' partials, in order
+          const float4 a = ptx::lds_f32x4(pa + w * V * 4), c = ptx::lds_f32x4(pa + w * V * 4 + 16);
+          o[0] = __fadd2_rn(o[0], make_float2(a.x, a.y));
+          o[1] = __fadd2_rn(o[1], make_float2(a.z, a.w));
+          o[2] = __fadd2_rn(o[2], make_float2(c.x, c.y));
+          o[3] = __fadd2_rn(o[3], make_float2(c.z, c.w));
+        }
+        float vv[8];
+        load8<F32>(vs + static_cast<uint32_t>((tl * G * V + fr) * es), vv);
+        float oo[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 r2 = __ffma2_rn(wrf[i], make_float2(vv[2 * i], vv[2 * i + 1]), o[i]);
+          oo[2 * i] = r2.x;
+          oo[2 * i + 1] = r2.y;
+        }
+        const size_t yo = ((static_cast<size_t>(b) * T + t0 + tl) * N + n0) * V + fr;
+        if (in_range(p.status, yo, 8, y_ext, CHK_FWD_Y)) store8(y + static_cast<size_t>(tl) * N * V + fr, oo);
+        if constexpr (NORM) {
+          float gg[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (in_range(p.status, yo, 8, y_ext, CHK_FWD_G)) ldg8<F32>(static_cast<const TIn*>(p.g) + yo, gg);
+          float part = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float og = oo[i] * gg[i];
+            part = fmaf(og, og, part);
+          }
+          const size_t so = static_cast<size_t>(b) * T + t0 + tl;
+          if (in_range(p.status, so, 1, static_cast<size_t>(p.B) * T, CHK_FWD_SSQ)) atomicAdd(p.ssq + so, part);
+        }
+      }
+    }
+    for (int idx = fixed ? nidx : id; idx < nidx; idx += LANES) {
       const int tl = idx / R8;
       const int r = (idx - tl * R8) * 8;
       const int hl = r / V, j = r - hl * V;
@@ -878,8 +987,16 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
 // KC, GC (0 = taken from the parameters): K and heads per CTA fixed at
 // compile time, so that every shared-memory stride of the step loops is an
 // immediate (instances for the common K = 64 launches).
+// Epilogue warps per CTA: three in the dense 8-head CTAs (with the producer,
+// one helper warp per SMSP), one elsewhere (smaller CTAs share SMs, and
+// more warps would cost them occupancy).
+template <int GC>
+__host__ __device__ constexpr int fwd_epilogue_warps() {
+  return GC >= 8 ? 3 : 1;
+}
+
 template <int V, int MT, bool F32, bool GATED, bool NORM, int KC = 0, int GC = 0>
-__global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1)
+__global__ void __launch_bounds__(32 * (1 + fwd_epilogue_warps<GC>() + max_consumer_warps<V, MT, F32>()), 1)
     fwd_kernel(const FwdParams prm) {
   FwdParams p = prm;
   if constexpr (KC > 0) {
@@ -895,6 +1012,7 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
   const int Geff = min(p.G, p.N - n0);
   const int ncons = Geff * p.WPH;
   constexpr bool PAIRS = rank1_pairs<V, F32, GC>();
+  constexpr int NEPI = fwd_epilogue_warps<GC>();
   const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, sizeof(TIn), p.tc, PAIRS);
   const uint32_t sbase = ptx::smem_addr(smem);
   const uint32_t bars = sbase + L.bars;
@@ -902,11 +1020,11 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
     for (int s = 0; s < NSTAGE; ++s) {
       ptx::mbar_init(bar_raw_full(bars, s), 1);
       ptx::mbar_init(bar_in_full(bars, s), 1);
-      ptx::mbar_init(bar_in_empty(bars, s), ncons + 1);
+      ptx::mbar_init(bar_in_empty(bars, s), ncons + NEPI);
     }
     for (int s = 0; s < NYSTAGE; ++s) {
       ptx::mbar_init(bar_yp_full(bars, s), ncons);
-      ptx::mbar_init(bar_yp_empty(bars, s), 1);
+      ptx::mbar_init(bar_yp_empty(bars, s), NEPI);
     }
     ptx::mbar_init_fence();
   }
@@ -915,10 +1033,10 @@ __global__ void __launch_bounds__(32 * (2 + max_consumer_warps<V, MT, F32>()), 1
     // With fault injection on, the producer issues nothing, so every wait of
     // the other warps runs into its time limit (tests of the time-out path).
     if (p.inject_stall == 0) fwd_producer<V, F32, GATED, PAIRS>(p, L, sbase, b, n0, Geff);
-  } else if (warp == 1) {
-    fwd_epilogue<V, F32, NORM>(p, L, sbase, b, n0, Geff);
-  } else if (warp - 2 < ncons) {
-    fwd_consumer<V, MT, F32, PAIRS>(p, L, sbase, b, n0, warp - 2);
+  } else if (warp <= NEPI) {
+    fwd_epilogue<V, F32, NORM, NEPI>(p, L, sbase, b, n0, Geff, warp - 1);
+  } else if (warp - 1 - NEPI < ncons) {
+    fwd_consumer<V, MT, F32, PAIRS>(p, L, sbase, b, n0, warp - 1 - NEPI);
   }
 }
 
@@ -1324,6 +1442,7 @@ template <int V, int MT, bool F32>
 struct Selected {
   decltype(&fwd_kernel<V, MT, F32, false, false>) kern;
   bool pairs;
+  int nepi = 1;  // epilogue warps
 };
 
 template <int V, int MT, bool F32>
@@ -1333,9 +1452,11 @@ Selected<V, MT, F32> select_kernel(const FwdParams& p) {
   if constexpr (V == 16 && MT == 2 && !F32) {
     if (!p.norm && !p.gated && p.K == 64 && p.WPH == 2) {
       if (p.G == 8)
-        return {fwd_kernel<16, 2, false, false, false, 64, 8>, rank1_pairs<16, false, 8>()};
+        return {fwd_kernel<16, 2, false, false, false, 64, 8>, rank1_pairs<16, false, 8>(),
+                fwd_epilogue_warps<8>()};
       if (p.G == 2)
-        return {fwd_kernel<16, 2, false, false, false, 64, 2>, rank1_pairs<16, false, 2>()};
+        return {fwd_kernel<16, 2, false, false, false, 64, 2>, rank1_pairs<16, false, 2>(),
+                fwd_epilogue_warps<2>()};
     }
   }
   constexpr bool pairs = rank1_pairs<V, F32>();
@@ -1355,7 +1476,8 @@ int ctas_per_sm_t(const FwdParams& p) {
                            static_cast<int>(L.total)) != cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * (2 + p.G * p.WPH), L.total) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * (1 + sel.nepi + p.G * p.WPH),
+                                                    L.total) !=
       cudaSuccess)
     return 0;
   return n;
@@ -1372,7 +1494,7 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
                                        static_cast<int>(L.total));
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.B) * static_cast<unsigned>(p.ngroups);
-  kern<<<grid, 32 * (2 + p.G * p.WPH), L.total, stream>>>(p);
+  kern<<<grid, 32 * (1 + sel.nepi + p.G * p.WPH), L.total, stream>>>(p);
   return cudaGetLastError();
 }
 
