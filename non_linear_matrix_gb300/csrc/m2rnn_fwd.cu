@@ -150,6 +150,15 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
   return __all_sync(0xffffffffu, ok);
 }
 
+// The same for the producer's and epilogue's waits: those warps share SMSPs
+// with consumer warps and mostly wait, so a waiting lane is suspended inside
+// try_wait (2 us at a time, woken when the phase completes) rather than
+// taking issue slots to poll.
+__device__ __forceinline__ bool warp_wait_idle(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const bool ok = ptx::mbar_wait_idle(bar, parity, limit_ns, 2000u);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------------------
 // producer warp
 // ---------------------------------------------------------------------------
@@ -193,7 +202,7 @@ __device__ __forceinline__ void fwd_producer(const FwdParams& p, const FwdLayout
   // its f (or, gated, f computed from a) as fp32 pairs.
   auto issue = [&](int ch) -> bool {
     const int s = ch % NSTAGE;
-    if (!warp_wait(bar_in_empty(bars, s), ((ch / NSTAGE) & 1) ^ 1, p.wait_limit_ns)) return false;
+    if (!warp_wait_idle(bar_in_empty(bars, s), ((ch / NSTAGE) & 1) ^ 1, p.wait_limit_ns)) return false;
     const int t0 = ch * TC;
     const int Tc = min(TC, T - t0);
     const uint32_t qk_bytes = static_cast<uint32_t>(Tc * K * es);
@@ -446,8 +455,8 @@ __device__ __forceinline__ void fwd_epilogue(const FwdParams& p, const FwdLayout
   }
   for (int ch = 0; ch < nchunks; ++ch) {
     const int s = ch % NSTAGE, ys = ch % NYSTAGE;
-    if (!warp_wait(bar_in_full(bars, s), (ch / NSTAGE) & 1, p.wait_limit_ns) ||
-        !warp_wait(bar_yp_full(bars, ys), (ch / NYSTAGE) & 1, p.wait_limit_ns)) {
+    if (!warp_wait_idle(bar_in_full(bars, s), (ch / NSTAGE) & 1, p.wait_limit_ns) ||
+        !warp_wait_idle(bar_yp_full(bars, ys), (ch / NYSTAGE) & 1, p.wait_limit_ns)) {
       if (lane == 0) record_timeout(p.status, SITE_FWD_EPILOGUE);
       break;
     }
