@@ -24,7 +24,11 @@ Extra keys on the JSON line:
   e2e           the same metric with host (pinned) inputs: host->device
                 copies, the C-ABI call and the device->host copy of y inside
                 the timed region;
-  clocks        nvidia-smi SM clock samples taken during the timed region.
+  clocks        nvidia-smi SM clock samples taken during the timed region;
+  fwd_bwd       the backward rows of the path: a forward + backward step of
+                B=8, T=4096, N=32 (checkpoints every 64 steps) with its own
+                roofline, roofline_bwd, roofline_alu and cpu_baseline (the
+                oracle's forward + backward on a bounded sample).
 For N > 1 (torchrun) every rank runs its own batch on its own GPU (weak
 scaling, no collective on the data path); rank 0 prints.
 """
@@ -710,6 +714,10 @@ def main():
                                   _oracle_rate(w, 12.0))
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "sample": desc}
+        if nested is not None:  # the fwd+bwd step's own oracle baseline (forward + backward)
+            rate, desc, threads, _ = _oracle_rate(WORKLOADS["fwdbwd_bf16_b8_t4096_n32"], 12.0)
+            nested["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads,
+                                      "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
