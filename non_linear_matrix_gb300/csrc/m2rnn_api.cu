@@ -138,6 +138,13 @@ FwdConfig choose_fwd(const m2rnn_shape* s, int sms) {
     const long long ctas = static_cast<long long>(s->B) * (s->N / G);
     if (G == 1 || ctas >= sms) best = G;
   }
+  // Tuning override: M2RNN_FWD_G=g forces g heads per CTA where it is valid.
+  if (const char* e = std::getenv("M2RNN_FWD_G")) {
+    const int g = std::atoi(e);
+    if (g >= 1 && g <= s->N && hpg % g == 0 && g * WPH <= maxw &&
+        m2rnn::fwd_smem_bytes(s->K, s->V, g, WPH, f32, 8) <= kSmemBudget)
+      best = g;
+  }
   int tc = 32;  // shorter ring chunks where the layout would not fit
   while (tc > 8 && m2rnn::fwd_smem_bytes(s->K, s->V, best, WPH, f32, tc) > kSmemBudget) tc /= 2;
   return {MT, WPH, best, tc};
