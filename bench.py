@@ -417,16 +417,21 @@ class Runner:
             torch.cuda.synchronize()
             tot = fw = e0.elapsed_time(e1)
         else:
-            for _ in range(steps):  # per-step events split fwd and bwd
-                e0.record(stream)
+            # per-step events split fwd and bwd; all steps are queued back to
+            # back and read after one synchronize, so no step waits for the
+            # host to enqueue it
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+            for a, b, c in evs:
+                a.record(stream)
                 self.fwd()
-                e1.record(stream)
+                b.record(stream)
                 self.bwd()
-                e2.record(stream)
-                e2.synchronize()
-                fw += e0.elapsed_time(e1)
-                bw += e1.elapsed_time(e2)
-            tot = fw + bw
+                c.record(stream)
+            torch.cuda.synchronize()
+            for a, b, c in evs:
+                fw += a.elapsed_time(b)
+                bw += b.elapsed_time(c)
+            tot = evs[0][0].elapsed_time(evs[-1][2])
         return tot / steps, fw / steps, bw / steps
 
 
