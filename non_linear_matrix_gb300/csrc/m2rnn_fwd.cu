@@ -17,9 +17,12 @@
 //            a chunk has landed it writes k as duplicated fp32 pairs (k_i,
 //            k_i) and f as (f, f), the operand form of the packed fp32
 //            multiplies below, then releases the chunk to the consumers.
-//   warp 1   epilogue: sums the per-warp readout partials, adds w_r (.) v_t,
-//            converts and stores y (16-byte vector stores).
-//   warps 2+ consumers: WPH warps per head, each holding MT 16-row slices of
+//   warps 1 .. NEPI  epilogue (three warps in the dense 8-head CTAs, one
+//            elsewhere): sums the per-warp readout partials, adds
+//            w_r (.) v_t, converts and stores y (16-byte vector stores).
+//            The producer's and epilogue's waits suspend instead of polling:
+//            these warps share SMSPs with consumer warps.
+//   then     consumers: WPH warps per head, each holding MT 16-row slices of
 //            the fp32 state in registers for all T steps, in the accumulator
 //            layout of mma.sync m16n8k16.  Per step and slice:
 //              acc  = k v^T           (packed fp32 multiplies, exact for
