@@ -6,7 +6,9 @@
 A step is one forward pass of the recurrence over the workload's whole batch
 (default: B=64, T=4096, N=32, K=64, V=16, bf16 inputs, fp32 state: the
 throughput shape), through the C ABI, with inputs resident in HBM.  The
-inputs (~0.32 GB) exceed the 129 MB L2, so no flush is needed between steps.
+inputs (~0.32 GB) exceed the 129 MB L2, so no flush is needed between steps;
+workloads whose working set fits in L2 write a buffer of twice its size
+before every timed step (outside the step's events).
 Metric: tokens x heads per second (B*T*N / step time).
 
 Extra keys on the JSON line:
@@ -56,6 +58,7 @@ METRIC = ("M2RNN fwd(+bwd) tokens\u00d7heads/s on 1 GB300; % of roofline "
           "(tensor/HBM/serial bound)")
 UNIT = "tokens*heads/s"
 DEFAULT_WORKLOAD = "fwd_bf16_b64_t4096_n32"
+L2_BYTES = 129 * 10**6  # GB300 L2
 
 # Rates measured on this machine's GB300 by non_linear_matrix_gb300/csrc/m2rnn_microbench.cu
 # (profiles/microbench_gb300.txt): tanh.approx results per clock per SM (f32,
@@ -371,6 +374,21 @@ class Runner:
                   else m2rnn.bwd_workspace_size(shape, True))
             self.ws = torch.empty(max(16, ws), device="cuda", dtype=torch.uint8)
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        # bytes a step reads or writes (all its device tensors); below the L2
+        # size the timed steps are separated by an L2 flush
+        tensors = list(self.g.values()) + list(self.out.values())
+        if w.backward:
+            tensors += list(self.gout.values()) + [self.ws]
+        self.working_set = sum(t.numel() * t.element_size() for t in tensors)
+        self.flush = (torch.empty(2 * L2_BYTES, device="cuda", dtype=torch.uint8)
+                      if self.working_set <= L2_BYTES else None)
+
+    def l2_note(self):
+        mb = self.working_set / 1e6
+        if self.flush is None:
+            return "working set %.0f MB larger than L2 (129 MB); no flush" % mb
+        return ("working set %.0f MB fits in L2 (129 MB): a %.0f MB buffer is written "
+                "before every timed step, outside its events" % (mb, self.flush.numel() / 1e6))
 
     def fwd(self):
         g = self.g
@@ -409,6 +427,21 @@ class Runner:
         """Times `steps` steps; returns (ms/step, fwd ms/step, bwd ms/step)."""
         e0, e1, e2 = self.ev
         tot = fw = bw = 0.0
+        if self.flush is not None:  # L2-resident working set: flush, then time each step
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+            for a, b, c in evs:
+                self.flush.fill_(1)
+                a.record(stream)
+                self.fwd()
+                b.record(stream)
+                if self.w.backward:
+                    self.bwd()
+                c.record(stream)
+            torch.cuda.synchronize()
+            for a, b, c in evs:
+                fw += a.elapsed_time(b)
+                bw += b.elapsed_time(c)
+            return (fw + bw) / steps, fw / steps, bw / steps
         if not self.w.backward:
             e0.record(stream)
             for _ in range(steps):
@@ -704,7 +737,7 @@ def main():
                             "forward"),
                    "l2": ("state (%.0f MB) larger than L2 (129 MB); no flush"
                           % (w.B * w.N * w.K * w.V * 4 / 1e6) if w.decode else
-                          "inputs larger than L2 (129 MB); no flush")},
+                          run.l2_note())},
         "roofline": roof, **extra,
         "e2e": e2e, "clocks": clocks,
         "gpu_launches": launches * args.steps if launches is not None else args.steps,
