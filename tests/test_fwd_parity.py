@@ -349,3 +349,66 @@ def test_state_bitwise_across_launch_variants(m2rnn, monkeypatch):
     for name in ("one_slice", "one_launch", "wave"):
         assert torch.equal(runs[name][1], runs["planned"][1]), name
         assert (runs[name][0] - runs["planned"][0]).abs().max().item() <= 2e-2, name
+
+
+SHAPES = [  # (B, T, N, env): one-head CTAs; 8-head + 2-head tail instances; one-wave kernel
+    (2, 37, 8, {}),
+    (41, 24, 32, {}),
+    (5, 33, 32, {"M2RNN_FWD_WAVE": "1", "M2RNN_FWD_WAVE_G": "9"}),
+]
+
+
+@pytest.mark.parametrize("B,T,N,env", SHAPES)
+def test_degenerate_f_one(m2rnn, monkeypatch, B, T, N, env):
+    """f = 1 from H0 = 0 (Eq. 11 then never admits the candidate): the state
+    stays exactly 0 and y = w_r (.) v, i.e. the bf16 rounding of the fp32
+    product, bit for bit, in every launch shape."""
+    for k in ("M2RNN_FWD_WAVE", "M2RNN_FWD_WAVE_G"):
+        monkeypatch.delenv(k, raising=False)
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    x = make_inputs(B, T, N, 64, 16, "bf16", 900 + B)
+    x["f"] = torch.ones_like(x["f"])
+    g = _dev(x)
+    y, HT, _ = m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"])
+    torch.cuda.synchronize()
+    _check_status(m2rnn)
+    assert torch.count_nonzero(HT) == 0
+    expect = (x["w_r"].float()[None, None] * x["v"].float()).to(torch.bfloat16)
+    assert torch.equal(y.cpu(), expect)
+
+
+@pytest.mark.parametrize("B,T,N,env", SHAPES)
+def test_degenerate_no_transition(m2rnn, oracle_mod, monkeypatch, B, T, N, env):
+    """W = 0 and f = 0: every step forgets the past and H_t = tanh(k_t v_t^T)
+    (Eqs. 10-11), so H_T depends on the last step only; y against the oracle."""
+    for k in ("M2RNN_FWD_WAVE", "M2RNN_FWD_WAVE_G"):
+        monkeypatch.delenv(k, raising=False)
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    x = make_inputs(B, T, N, 64, 16, "bf16", 950 + B)
+    x["f"] = torch.zeros_like(x["f"])
+    x["W"] = torch.zeros_like(x["W"])
+    g = _dev(x)
+    y, HT, _ = m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"])
+    torch.cuda.synchronize()
+    _check_status(m2rnn)
+    kT = x["k"][:, -1].double()                       # [B, K]
+    vT = x["v"][:, -1].double()                       # [B, N, V]
+    expect = torch.tanh(kT[:, None, :, None] * vT[:, :, None, :])
+    assert (HT.cpu().double() - expect).abs().max().item() <= 1e-3  # tanh.approx, |.| <= 1
+    ref = oracle_mod.fwd(x["q"], x["k"], x["v"], x["f"], x["W"], x["w_r"])
+    assert np.abs(_np(y) - ref["y"]).max() <= TOL["bf16"]
+
+
+def test_state_bound_full_size(m2rnn):
+    """|H_t| <= 1: H is a convex blend of tanh values starting from 0 (Eq. 11),
+    which holds at any size; checked on H_T of the B=64, T=4096, N=32 forward
+    in the launch plan the benchmark times (up to fp32 rounding of the blend)."""
+    w = WORKLOADS["fwd_bf16_b64_t4096_n32"]
+    g = _dev(workload_inputs(w, with_dy=False))
+    _, HT, _ = m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"])
+    torch.cuda.synchronize()
+    _check_status(m2rnn)
+    assert torch.isfinite(HT).all()
+    assert HT.abs().max().item() <= 1.0 + 1e-6
