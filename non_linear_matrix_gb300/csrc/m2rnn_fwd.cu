@@ -959,15 +959,53 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
       auto ro = [](uint32_t u) -> uint32_t {
         return defer_readout<MT, F32>() ? (u > 0 ? u - 1 : 0) : u;
       };
+      if constexpr (defer_readout<MT, F32>()) {
+        // One-slice warps (these launches take their strides at run time):
+        // running addresses, one add per stream and two steps, instead of a
+        // multiply-add per address and step.
+        uint32_t kp = kdb + static_cast<uint32_t>(tl) * kd_stride;
+        uint32_t vp = vb + static_cast<uint32_t>(tl) * v_stride;
+        uint32_t fp = fdb + static_cast<uint32_t>(tl) * fd_stride;
+        if (tl + 1 < seg_end) {  // first pair: step tl writes the readout slot ro(tl)
+          const uint32_t q0 = qb + ro(static_cast<uint32_t>(tl)) * q_stride;
+          const uint32_t y0 = yb + ro(static_cast<uint32_t>(tl)) * yp_stride;
+          load_step<V, MT, F32, HALF, PAIRS>(in1, kp + kd_stride, vp + v_stride, g, c);
+          fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, q0, fp, y0, g, c);
+          load_step<V, MT, F32, HALF, PAIRS>(in0, kp + 2 * kd_stride, vp + 2 * v_stride, g, c);
+          fwd_step<V, MT, F32, HALF, PAIRS>(S, in1, qb + static_cast<uint32_t>(tl) * q_stride,
+                                            fp + fd_stride, yb + static_cast<uint32_t>(tl) * yp_stride,
+                                            g, c);
+          tl += 2;
+          kp += 2 * kd_stride;
+          vp += 2 * v_stride;
+          fp += 2 * fd_stride;
+        }
+        uint32_t qp = qb + static_cast<uint32_t>(tl - 1) * q_stride;  // readout of step tl - 1
+        uint32_t ypp = yb + static_cast<uint32_t>(tl - 1) * yp_stride;
 #pragma unroll 1
-      for (; tl + 1 < seg_end; tl += 2) {
-        const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1, u2 = u0 + 2;
-        load_step<V, MT, F32, HALF, PAIRS>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
-        fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, qb + ro(u0) * q_stride, fdb + u0 * fd_stride,
-                             yb + ro(u0) * yp_stride, g, c);
-        load_step<V, MT, F32, HALF, PAIRS>(in0, kdb + u2 * kd_stride, vb + u2 * v_stride, g, c);
-        fwd_step<V, MT, F32, HALF, PAIRS>(S, in1, qb + ro(u1) * q_stride, fdb + u1 * fd_stride,
-                             yb + ro(u1) * yp_stride, g, c);
+        for (; tl + 1 < seg_end; tl += 2) {
+          load_step<V, MT, F32, HALF, PAIRS>(in1, kp + kd_stride, vp + v_stride, g, c);
+          fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, qp, fp, ypp, g, c);
+          load_step<V, MT, F32, HALF, PAIRS>(in0, kp + 2 * kd_stride, vp + 2 * v_stride, g, c);
+          fwd_step<V, MT, F32, HALF, PAIRS>(S, in1, qp + q_stride, fp + fd_stride, ypp + yp_stride,
+                                            g, c);
+          kp += 2 * kd_stride;
+          vp += 2 * v_stride;
+          fp += 2 * fd_stride;
+          qp += 2 * q_stride;
+          ypp += 2 * yp_stride;
+        }
+      } else {
+#pragma unroll 1
+        for (; tl + 1 < seg_end; tl += 2) {
+          const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1, u2 = u0 + 2;
+          load_step<V, MT, F32, HALF, PAIRS>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
+          fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, qb + ro(u0) * q_stride, fdb + u0 * fd_stride,
+                               yb + ro(u0) * yp_stride, g, c);
+          load_step<V, MT, F32, HALF, PAIRS>(in0, kdb + u2 * kd_stride, vb + u2 * v_stride, g, c);
+          fwd_step<V, MT, F32, HALF, PAIRS>(S, in1, qb + ro(u1) * q_stride, fdb + u1 * fd_stride,
+                               yb + ro(u1) * yp_stride, g, c);
+        }
       }
       if (tl < seg_end) {  // odd remainder of the segment
         const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1;
