@@ -606,7 +606,10 @@ def main():
         h2d = sum(t.numel() * t.element_size() for t in hx.values())
         d2h = sum(t.numel() * t.element_size() for t in hres)
 
-        e_steps = max(3, min(args.steps, 50))
+        # at least 50 pipelined steps: the first batch's copy in and the
+        # last batch's copy out are not overlapped, and over 20 steps that
+        # fill and drain alone add ~0.15 ms per step at B=64
+        e_steps = max(50, min(args.steps, 200))
         if w.decode:
             # one decode stream: each step needs the state the previous step wrote
             def e2e_step():
