@@ -11,7 +11,9 @@
 // The forward kernel's epilogue warp already added sum_d o^2 of every token
 // into rstd (fused, per CTA, as it stored y); the forward kernel here only
 // scales.  Both kernels are bound by HBM traffic: one warp per token row,
-// 16-byte vector loads and stores, grid-stride over rows.
+// 16-byte vector loads and stores, grid-stride over rows.  For d <= 512 the
+// backward keeps a row in registers between its two passes and its share of
+// dw in registers across rows.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -161,6 +163,91 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) norm_bwd_kernel(const NormP
   for (int e = threadIdx.x; e < d; e += blockDim.x) atomicAdd(p.dw + e, dw_s[e]);
 }
 
+// The same for d <= 512 (at most two 8-column groups per lane): a lane's
+// columns are the same in every row, so it keeps the row's values in
+// registers between the two passes and its share of dw in registers across
+// rows, summing it over the CTA's warps in shared memory once at the end.
+// dy and dg are computed by the same operations as above.
+template <bool F32>
+__global__ void __launch_bounds__(32 * kWarpsPerCta) norm_bwd_kernel_reg(const NormParams p) {
+  using TIn = typename NormT<F32>::T;
+  constexpr int kG = 2;  // 8-column groups per lane
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = static_cast<long long>(gridDim.x) * kWarpsPerCta;
+  const int d = p.d, d8 = d / 8;
+  const float inv_d = 1.f / static_cast<float>(d);
+  const TIn* y = static_cast<const TIn*>(p.y);
+  const TIn* g = static_cast<const TIn*>(p.g);
+  const TIn* w = static_cast<const TIn*>(p.w);
+  const TIn* dout = static_cast<const TIn*>(p.dout);
+  TIn* dy = static_cast<TIn*>(p.dy);
+  float ww[kG][8], dwa[kG][8];
+  bool col_ok[kG];
+#pragma unroll
+  for (int j = 0; j < kG; ++j) {
+    const int e = lane + 32 * j;
+    col_ok[j] = e < d8 && in_range(p.status, 8 * e, 8, d, CHK_NORM_IN);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ww[j][i] = dwa[j][i] = 0.f;
+    if (col_ok[j]) load8<F32>(w + 8 * e, ww[j]);
+  }
+  for (long long row = static_cast<long long>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+       row < p.rows; row += nwarps) {
+    const size_t base = static_cast<size_t>(row) * d;
+    const float s = p.rstd[row];
+    float yy[kG][8], gg[kG][8], uu[kG][8];
+    bool ok[kG];
+    float r = 0.f;  // sum_d (w dout) (y g)
+#pragma unroll
+    for (int j = 0; j < kG; ++j) {
+      const int e = lane + 32 * j;
+      ok[j] = col_ok[j] &&
+              in_range(p.status, base + 8 * e, 8, static_cast<size_t>(p.rows) * d, CHK_NORM_IN);
+      if (ok[j]) {
+        load8<F32>(y + base + 8 * e, yy[j]);
+        load8<F32>(g + base + 8 * e, gg[j]);
+        load8<F32>(dout + base + 8 * e, uu[j]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r = fmaf(ww[j][i] * uu[j][i], yy[j][i] * gg[j][i], r);
+      }
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
+    const float c = r * s * s * s * inv_d;
+#pragma unroll
+    for (int j = 0; j < kG; ++j) {
+      const int e = lane + 32 * j;
+      if (!ok[j] || !in_range(p.status, base + 8 * e, 8, static_cast<size_t>(p.rows) * d,
+                              CHK_NORM_OUT))
+        continue;
+      float dyo[8], dgo[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float o = yy[j][i] * gg[j][i];
+        const float dov = fmaf(s, ww[j][i] * uu[j][i], -c * o);
+        dyo[i] = dov * gg[j][i];
+        dgo[i] = dov * yy[j][i];
+        dwa[j][i] += uu[j][i] * o * s;
+      }
+      store8<F32>(dy + base + 8 * e, dyo);
+      store8<true>(p.dg + base + 8 * e, dgo);
+    }
+  }
+  // dw: the CTA's warps first (shared memory), then one global add per column
+  __shared__ float dw_s[512];
+  for (int e = threadIdx.x; e < d; e += blockDim.x) dw_s[e] = 0.f;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kG; ++j) {
+    const int e = lane + 32 * j;
+    if (col_ok[j])
+#pragma unroll
+      for (int i = 0; i < 8; ++i) atomicAdd(dw_s + 8 * e + i, dwa[j][i]);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < d; e += blockDim.x) atomicAdd(p.dw + e, dw_s[e]);
+}
+
 unsigned norm_grid(long long rows, int sms, int ctas_per_sm) {
   const long long need = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
   const long long cap = static_cast<long long>(sms) * ctas_per_sm;
@@ -185,6 +272,14 @@ cudaError_t launch_norm_fwd(const NormParams& p, bool f32_inputs, int sms, cudaS
 cudaError_t launch_norm_bwd(const NormParams& p, bool f32_inputs, int sms, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;
   if (p.d % 8 != 0) return cudaErrorInvalidValue;
+  if (p.d <= 512) {  // two 8-column groups per lane at most: registers only
+    const unsigned grid = norm_grid(p.rows, sms, 2);  // (126 registers: two CTAs per SM)
+    if (f32_inputs)
+      norm_bwd_kernel_reg<true><<<grid, 32 * kWarpsPerCta, 0, stream>>>(p);
+    else
+      norm_bwd_kernel_reg<false><<<grid, 32 * kWarpsPerCta, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
   const size_t smem = norm_bwd_smem_bytes(p.d);
   auto kern = f32_inputs ? norm_bwd_kernel<true> : norm_bwd_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -163,6 +163,15 @@ def test_backward_norm(m2rnn, oracle_mod, monkeypatch, kernel, dtype):
     _bwd_restart(m2rnn, oracle_mod, x, 24, dtype, label=f"k{kernel} {dtype}")
 
 
+@pytest.mark.parametrize("N", [32, 40])
+def test_backward_norm_row_widths(m2rnn, oracle_mod, N):
+    """A token's d = N V features on either side of the normalisation
+    backward's switch: d = 512 (the register kernel, two full 8-column
+    groups per lane) and d = 640 (the kernel with dw in shared memory)."""
+    x = make_inputs(2, 40, N, 64, 16, "bf16", 1250 + N, with_dy=True, norm=True)
+    _bwd_restart(m2rnn, oracle_mod, x, 16, "bf16", label=f"d={16 * N}")
+
+
 def test_backward_norm_gated_grouped_recomputed(m2rnn, oracle_mod):
     """The epilogue with the fused gate, 2 query/key groups and checkpoints
     recomputed into the workspace (after the epilogue's dL/dy)."""
