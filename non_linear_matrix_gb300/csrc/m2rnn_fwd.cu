@@ -20,8 +20,8 @@
 //   warps 1 .. NEPI  epilogue (three warps in the dense 8-head CTAs, one
 //            elsewhere): sums the per-warp readout partials, adds
 //            w_r (.) v_t, converts and stores y (16-byte vector stores).
-//            The producer's and epilogue's waits suspend instead of polling:
-//            these warps share SMSPs with consumer warps.
+//            The producer's and epilogue's waits sleep between tries instead
+//            of polling: these warps share SMSPs with consumer warps.
 //   then     consumers: WPH warps per head, each holding MT 16-row slices of
 //            the fp32 state in registers for all T steps, in the accumulator
 //            layout of mma.sync m16n8k16.  Per step and slice:
@@ -154,11 +154,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
 }
 
 // The same for the producer's and epilogue's waits: those warps share SMSPs
-// with consumer warps and mostly wait, so a waiting lane is suspended inside
-// try_wait (2 us at a time, woken when the phase completes) rather than
-// taking issue slots to poll.
+// with consumer warps and mostly wait, so a waiting lane sleeps between its
+// tries rather than taking issue slots to poll.  The rings give these warps
+// at least a chunk of slack, several microseconds, against the sleep.
+constexpr uint32_t kHelperSleepNs = 256;
 __device__ __forceinline__ bool warp_wait_idle(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const bool ok = ptx::mbar_wait_idle(bar, parity, limit_ns, 2000u);
+  const bool ok = ptx::mbar_wait_sleep(bar, parity, limit_ns, kHelperSleepNs);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -202,28 +202,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// As mbar_try_wait, but a thread whose phase is not complete may be
-// suspended for up to hint_ns nanoseconds (it resumes when the phase
-// completes) instead of returning at once: for warps that mostly wait.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
-// mbar_wait with suspended (not polling) retries; the same time limit.
-__device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                               uint32_t hint_ns) {
-  if (mbar_try_wait_hint(bar, parity, hint_ns)) return true;
+// mbar_wait for warps that mostly wait: after a first try, each retry comes
+// after a nanosleep of sleep_ns (the hardware sleeps between 0 and twice
+// that), so that a waiting warp takes few issue slots from the warps that
+// share its SMSP.  The same time limit.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait_hint(bar, parity, hint_ns)) return true;
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
