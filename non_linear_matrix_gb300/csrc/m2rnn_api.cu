@@ -150,6 +150,29 @@ FwdConfig choose_fwd(const m2rnn_shape* s, int sms) {
   return {MT, WPH, best, tc};
 }
 
+// Ring chunk length of the main launch.  64 steps where the CTAs still fit
+// on the SMs as they do with 32 (every CTA at once, or as many per SM): a
+// consumer's waits and hand-offs at chunk boundaries then come half as often.
+// M2RNN_FWD_TC=n (2..64) forces it where the layout fits.
+int refine_tc(const m2rnn::FwdParams& p, const m2rnn_shape* s, int sms, const FwdConfig& cfg,
+              bool f32) {
+  if (const char* e = std::getenv("M2RNN_FWD_TC")) {
+    const int t = std::atoi(e);
+    if (t >= 2 && t <= 64 &&
+        m2rnn::fwd_smem_bytes(s->K, s->V, cfg.G, cfg.WPH, f32, t) <= kSmemBudget)
+      return t;
+  }
+  if (cfg.tc != 32 || m2rnn::fwd_smem_bytes(s->K, s->V, cfg.G, cfg.WPH, f32, 64) > kSmemBudget)
+    return cfg.tc;
+  m2rnn::FwdParams q = p;
+  q.tc = 32;
+  const int r32 = m2rnn::fwd_ctas_per_sm(q, s->V, f32, cfg.MT);
+  q.tc = 64;
+  const int r64 = m2rnn::fwd_ctas_per_sm(q, s->V, f32, cfg.MT);
+  const long long ctas = static_cast<long long>(s->B) * p.ngroups;
+  return r64 > 0 && (r64 >= r32 || static_cast<long long>(r64) * sms >= ctas) ? 64 : 32;
+}
+
 struct WavePlan {
   int B1;       // leading batch items run with the main configuration (0 = one launch)
   int tail_G;   // heads per CTA of the launch covering the remaining batch items
@@ -297,6 +320,7 @@ int run_fwd(const m2rnn_shape* s, const void* q, const void* k, const void* v, c
     p.ssq = nf->rstd;
     p.norm = 1;
   }
+  p.tc = refine_tc(p, s, sms, cfg, f32);
 
   // One-wave kernel (opt-in, M2RNN_FWD_WAVE=1): every head resident at once,
   // G = ceil(B N / SMs) heads per CTA over the flattened (b, n) order, one

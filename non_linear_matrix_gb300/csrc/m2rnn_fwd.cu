@@ -92,7 +92,7 @@ struct FwdLayout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// TC: time steps per ring chunk (<= 32).
+// TC: time steps per ring chunk (<= 64).
 // pairs: k also as fp32 (k, k) pairs (rank1_pairs).
 __host__ __device__ inline FwdLayout fwd_layout(int K, int V, int G, int WPH, int es, int TC,
                                                 bool pairs = true) {
@@ -1538,7 +1538,7 @@ template <int V, int MT, bool F32>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
   const auto sel = select_kernel<V, MT, F32>(p);
   const FwdLayout L = fwd_layout(p.K, V, p.G, p.WPH, F32 ? 4 : 2, p.tc, sel.pairs);
-  if (p.tc < 2 || p.tc > 32) return cudaErrorInvalidValue;
+  if (p.tc < 2 || p.tc > 64) return cudaErrorInvalidValue;
   if (p.G * p.WPH > max_consumer_warps<V, MT, F32>()) return cudaErrorInvalidConfiguration;
   auto kern = sel.kern;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
