@@ -157,8 +157,8 @@ def test_throughput_workloads_sampled(m2rnn, oracle_mod, name):
 @pytest.mark.parametrize("K,V", [(16, 16), (32, 16), (64, 16), (128, 16), (64, 32), (128, 32)])
 @pytest.mark.parametrize("T", [1, 33, 100])
 def test_shapes_ragged(m2rnn, oracle_mod, dtype, K, V, T):
-    """Ragged time (not a multiple of the 32-step ring chunk), heads not a
-    multiple of the per-CTA group, every supported K and V, random H0."""
+    """Ragged time (not a multiple of the ring chunk, 32 or 64 steps), heads
+    not a multiple of the per-CTA group, every supported K and V, random H0."""
     B, N = 2, 5
     x = make_inputs(B, T, N, K, V, dtype, 1000 + K + V + T)
     H0 = torch.rand(B, N, K, V, generator=torch.Generator().manual_seed(T)) - 0.5
@@ -176,6 +176,31 @@ def test_restart_parity_ragged_tail_and_H0(m2rnn, oracle_mod):
     torch.cuda.synchronize()
     _check_status(m2rnn)
     _restart_parity(oracle_mod, x, y, HT, ck, 48, TOL["bf16"], "ragged", H0=H0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_ring_chunk_lengths(m2rnn, oracle_mod, monkeypatch, dtype):
+    """Ring chunks of 2, 5, 32 and 64 steps (forced through M2RNN_FWD_TC) on a
+    ragged T with checkpoints that fall inside chunks and a given H0: each
+    against the oracle, and the same H_T and checkpoints bit for bit, since
+    the chunk length changes when a step's inputs arrive, not its
+    arithmetic."""
+    B, T, N = 2, 147, 5
+    x = make_inputs(B, T, N, 64, 16, dtype, 820)
+    H0 = torch.rand(B, N, 64, 16, generator=torch.Generator().manual_seed(9)) - 0.5
+    g = _dev(x)
+    runs = {}
+    for tc in ("2", "5", "32", "64"):
+        monkeypatch.setenv("M2RNN_FWD_TC", tc)
+        _compare(m2rnn, oracle_mod, x, dtype, H0=H0, ckpt_every=24, label=f"TC={tc}")
+        y, HT, ck = m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], H0.cuda(),
+                              ckpt_every=24)
+        torch.cuda.synchronize()
+        runs[tc] = (HT, ck)
+    _check_status(m2rnn)
+    for tc in ("2", "5", "32"):
+        assert torch.equal(runs[tc][0], runs["64"][0]), tc
+        assert torch.equal(runs[tc][1], runs["64"][1]), tc
 
 
 @pytest.mark.parametrize("mt", ["0", "1", "2", "4"])
