@@ -181,10 +181,10 @@ def test_restart_parity_ragged_tail_and_H0(m2rnn, oracle_mod):
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_ring_chunk_lengths(m2rnn, oracle_mod, monkeypatch, dtype):
     """Ring chunks of 2, 5, 32 and 64 steps (forced through M2RNN_FWD_TC) on a
-    ragged T with checkpoints that fall inside chunks and a given H0: each
-    against the oracle, and the same H_T and checkpoints bit for bit, since
-    the chunk length changes when a step's inputs arrive, not its
-    arithmetic."""
+    ragged T with checkpoints that fall inside chunks and a given H0: the
+    same y, H_T and checkpoints bit for bit (the chunk length changes when a
+    step's inputs arrive, not its arithmetic), and those against the oracle
+    restarted at every checkpoint."""
     B, T, N = 2, 147, 5
     x = make_inputs(B, T, N, 64, 16, dtype, 820)
     H0 = torch.rand(B, N, 64, 16, generator=torch.Generator().manual_seed(9)) - 0.5
@@ -192,15 +192,16 @@ def test_ring_chunk_lengths(m2rnn, oracle_mod, monkeypatch, dtype):
     runs = {}
     for tc in ("2", "5", "32", "64"):
         monkeypatch.setenv("M2RNN_FWD_TC", tc)
-        _compare(m2rnn, oracle_mod, x, dtype, H0=H0, ckpt_every=24, label=f"TC={tc}")
         y, HT, ck = m2rnn.fwd(g["q"], g["k"], g["v"], g["f"], g["W"], g["w_r"], H0.cuda(),
                               ckpt_every=24)
         torch.cuda.synchronize()
-        runs[tc] = (HT, ck)
-    _check_status(m2rnn)
+        _check_status(m2rnn)
+        runs[tc] = (y, HT, ck)
     for tc in ("2", "5", "32"):
-        assert torch.equal(runs[tc][0], runs["64"][0]), tc
-        assert torch.equal(runs[tc][1], runs["64"][1]), tc
+        for a, b2, what in zip(runs[tc], runs["64"], ("y", "H_T", "ckpt")):
+            assert torch.equal(a, b2), (tc, what)
+    y, HT, ck = runs["64"]
+    _restart_parity(oracle_mod, x, y, HT, ck, 24, TOL[dtype], f"chunks {dtype}", H0=H0)
 
 
 @pytest.mark.parametrize("mt", ["0", "1", "2", "4"])
