@@ -737,13 +737,17 @@ __host__ __device__ constexpr bool defer_readout() {
 // (columns 8nt+2c, +1, on lanes with g == 0) to ypaddr from q at qb: the
 // step's own, or with defer_readout() the previous step's, formed from the
 // bf16(H) operand of this step's H W products before they are used (the last
-// step of a run then needs readout_bf16 afterwards).
-template <int V, int MT, bool F32, bool HALF, bool PAIRS>
+// step of a run then needs readout_bf16 afterwards).  next() reads the next
+// step's inputs: first, or with defer_readout() right behind this step's
+// H W products, so that its loads and k v^T products do not hold up this
+// step's chain in the warp's in-order issue.
+template <int V, int MT, bool F32, bool HALF, bool PAIRS, typename Next>
 __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V / 8, F32>& in,
                                          uint32_t qb, uint32_t fdaddr, uint32_t ypaddr, int g,
-                                         int c) {
+                                         int c, Next&& next) {
   constexpr int NT = V / 8, KS = V / 16;
   constexpr bool DEFER = defer_readout<MT, F32>();
+  if constexpr (!DEFER) next();
   // q (for the readout) and f are read here; their use is tens of cycles on.
   uint32_t qa[MT][2];
   float qf[MT][2];
@@ -799,6 +803,7 @@ __device__ __forceinline__ void fwd_step(WarpState<V, MT>& S, const StepIn<MT, V
     float acc[MT][NT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) products(mt, acc[mt]);
+    next();
     readout_bf16<V, MT, HALF>(S.A, qb, ypaddr, g, c);  // the previous step's, in the MMAs' shadow
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) update(mt, acc[mt]);
@@ -941,7 +946,8 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
     const uint32_t fdb = st + L.fd + static_cast<uint32_t>(hl * 8);
     const uint32_t yb = sbase + L.yp_base + static_cast<uint32_t>(ys) * L.yp_stage +
                         static_cast<uint32_t>(((hl * WPH) + w) * V * 4);
-    // The rank-1 inputs of step tl+1 are read while step tl computes.  The
+    // The rank-1 inputs of step tl+1 are read while step tl computes (by the
+    // next() of each fwd_step below).  The
     // read past the chunk's last step (slot Tc <= TC) stays inside this
     // stage's shared memory and its values are never used.
     load_step<V, MT, F32, HALF, PAIRS>(in0, kdb, vb, g, c);
@@ -970,12 +976,12 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
         if (tl + 1 < seg_end) {  // first pair: step tl writes the readout slot ro(tl)
           const uint32_t q0 = qb + ro(static_cast<uint32_t>(tl)) * q_stride;
           const uint32_t y0 = yb + ro(static_cast<uint32_t>(tl)) * yp_stride;
-          load_step<V, MT, F32, HALF, PAIRS>(in1, kp + kd_stride, vp + v_stride, g, c);
-          fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, q0, fp, y0, g, c);
-          load_step<V, MT, F32, HALF, PAIRS>(in0, kp + 2 * kd_stride, vp + 2 * v_stride, g, c);
+          fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, q0, fp, y0, g, c,
+              [&] { load_step<V, MT, F32, HALF, PAIRS>(in1, kp + kd_stride, vp + v_stride, g, c); });
           fwd_step<V, MT, F32, HALF, PAIRS>(S, in1, qb + static_cast<uint32_t>(tl) * q_stride,
-                                            fp + fd_stride, yb + static_cast<uint32_t>(tl) * yp_stride,
-                                            g, c);
+                                            fp + fd_stride,
+                                            yb + static_cast<uint32_t>(tl) * yp_stride, g, c,
+              [&] { load_step<V, MT, F32, HALF, PAIRS>(in0, kp + 2 * kd_stride, vp + 2 * v_stride, g, c); });
           tl += 2;
           kp += 2 * kd_stride;
           vp += 2 * v_stride;
@@ -985,11 +991,11 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
         uint32_t ypp = yb + static_cast<uint32_t>(tl - 1) * yp_stride;
 #pragma unroll 1
         for (; tl + 1 < seg_end; tl += 2) {
-          load_step<V, MT, F32, HALF, PAIRS>(in1, kp + kd_stride, vp + v_stride, g, c);
-          fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, qp, fp, ypp, g, c);
-          load_step<V, MT, F32, HALF, PAIRS>(in0, kp + 2 * kd_stride, vp + 2 * v_stride, g, c);
-          fwd_step<V, MT, F32, HALF, PAIRS>(S, in1, qp + q_stride, fp + fd_stride, ypp + yp_stride,
-                                            g, c);
+          fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, qp, fp, ypp, g, c,
+              [&] { load_step<V, MT, F32, HALF, PAIRS>(in1, kp + kd_stride, vp + v_stride, g, c); });
+          fwd_step<V, MT, F32, HALF, PAIRS>(S, in1, qp + q_stride, fp + fd_stride,
+                                            ypp + yp_stride, g, c,
+              [&] { load_step<V, MT, F32, HALF, PAIRS>(in0, kp + 2 * kd_stride, vp + 2 * v_stride, g, c); });
           kp += 2 * kd_stride;
           vp += 2 * v_stride;
           fp += 2 * fd_stride;
@@ -1000,19 +1006,19 @@ __device__ __forceinline__ void fwd_consumer(const FwdParams& p, const FwdLayout
 #pragma unroll 1
         for (; tl + 1 < seg_end; tl += 2) {
           const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1, u2 = u0 + 2;
-          load_step<V, MT, F32, HALF, PAIRS>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
           fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, qb + ro(u0) * q_stride, fdb + u0 * fd_stride,
-                               yb + ro(u0) * yp_stride, g, c);
-          load_step<V, MT, F32, HALF, PAIRS>(in0, kdb + u2 * kd_stride, vb + u2 * v_stride, g, c);
+                                            yb + ro(u0) * yp_stride, g, c,
+              [&] { load_step<V, MT, F32, HALF, PAIRS>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c); });
           fwd_step<V, MT, F32, HALF, PAIRS>(S, in1, qb + ro(u1) * q_stride, fdb + u1 * fd_stride,
-                               yb + ro(u1) * yp_stride, g, c);
+                                            yb + ro(u1) * yp_stride, g, c,
+              [&] { load_step<V, MT, F32, HALF, PAIRS>(in0, kdb + u2 * kd_stride, vb + u2 * v_stride, g, c); });
         }
       }
       if (tl < seg_end) {  // odd remainder of the segment
         const uint32_t u0 = static_cast<uint32_t>(tl), u1 = u0 + 1;
-        load_step<V, MT, F32, HALF, PAIRS>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c);
         fwd_step<V, MT, F32, HALF, PAIRS>(S, in0, qb + ro(u0) * q_stride, fdb + u0 * fd_stride,
-                             yb + ro(u0) * yp_stride, g, c);
+                                          yb + ro(u0) * yp_stride, g, c,
+            [&] { load_step<V, MT, F32, HALF, PAIRS>(in1, kdb + u1 * kd_stride, vb + u1 * v_stride, g, c); });
         in0 = in1;
         ++tl;
       }
